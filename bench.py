@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Throughput of one GPT-2 training iteration (forward + backward + clip +
+AdamW) on B300 through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2_124m|gpt2_24l_1024d|char] [--no-cpu-baseline]
+
+Prints one JSON line on rank 0. A step is one pass of the whole hot path over
+one synthetic batch (Zipf(1.1) token ids, seeded) with inputs resident in HBM;
+`value` is whole-job tokens/s. Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU and batch (no collective on the data path:
+the gradient exchange of data parallelism is not part of this single-GPU
+build); timing is the max over ranks.
+
+`--impl reference` times the CPU oracle (plain fp64 numpy) on a bounded sample
+of the same workload on the host cores, as the comparison arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthdata  # noqa: E402
+
+METRIC = "tokens/s and MFU, GPT-2 124M fwd+bwd+AdamW step, B=16 T=1024, 1 B300"
+NOMINAL_BF16_DENSE = 2.25e15     # B300 dense bf16 tensor peak (NVIDIA nominal)
+
+WORKLOADS = {
+    # name: (n_layer, n_head, d_model, vocab, padded, T, B, stream kind)
+    "gpt2_124m": (12, 12, 768, 50257, 50304, 1024, 16, "zipf"),
+    "gpt2_24l_1024d": (24, 16, 1024, 50257, 50304, 1024, 8, "zipf"),
+    "char": (6, 6, 384, 65, 0, 256, 64, "markov"),
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+def flops_per_token(L, C, V_padded, T, block):
+    """6N + 12 L T d with N the non-position parameters, padded vocabulary
+    (nanoGPT guide Part IV Stage 6, estimate_mfu)."""
+    n = V_padded * C + L * (12 * C * C + 13 * C) + 2 * C
+    return 6 * n + 12 * L * T * C
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier_max(x: float, world: int, torch):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_time(workload: str, tokens: int, steps: int = 1):
+    """Time the oracle's fwd+bwd+AdamW on a bounded sample: one sequence of
+    `tokens` tokens of the workload's model (all parameters, real vocabulary).
+    Returns (seconds per step, threads used, sample description)."""
+    from oracle import gpt2_oracle as O
+    L, H, C, V, Vp, T, B, kind = WORKLOADS[workload]
+    c = O.Config(n_layer=L, n_head=H, d_model=C, vocab_size=V, padded_vocab=Vp, block_size=T,
+                 batch_size=1, seq_len=tokens)
+    tr = O.Trainer(c, 1337)
+    x, y = synthdata.batch_for(kind, V, 1, tokens, 1337)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        tr.forward(x, y)
+        tr.backward()
+        tr.step(lr=6e-4)
+        tr.zero_grad()
+        times.append(time.perf_counter() - t0)
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(i.get("num_threads", 1) for i in threadpool_info()) or os.cpu_count()
+    except Exception:
+        cores = os.cpu_count()
+    sample = (f"oracle (fp64 numpy) fwd+bwd+AdamW of the full {workload} model on 1 sequence x "
+              f"{tokens} tokens (of the {B}x{T} batch), {steps} step(s)")
+    return times, cores, sample
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    n = args.steps + args.warmup
+    # size the sample so that the whole run stays within ~3 minutes
+    budget = 180.0
+    tokens = 64
+    for cand in (1024, 512, 256, 128, 64):
+        est = 4.0 * (L / 12) + 25.0 * (L * C * C) / (12 * 768 * 768) * cand / 1024
+        if cand <= T and n * est <= budget:
+            tokens = cand
+            break
+    times, cores, sample = cpu_oracle_time(args.workload, tokens, n)
+    timed = times[args.warmup:] if len(times) > args.warmup else times
+    sec = sum(timed) / len(timed)
+    value = tokens / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * sec, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "global_batch": 1, "seq_len": tokens,
+                   "sample_of": f"B={B} T={T}"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def traffic_from_profiles(kernel_src: str):
+    """DRAM traffic per launch of the dominant kernel from the committed ncu
+    summary, if that summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "gemm_tc_gpt2_124m_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(kernel_src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != h:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from decoder_only_transformer_06_b300 import gpt2
+
+    L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    cfg = gpt2.Config(n_layer=L, n_head=H, d_model=C, vocab_size=V, padded_vocab=Vp,
+                      block_size=T, batch_size=B, seq_len=T, precision=gpt2.GPT2_BF16)
+    stream = torch.cuda.Stream()
+    model = gpt2.GPT2(cfg, seed=1337, stream=stream)
+    nb = args.warmup + args.steps
+    host = [synthdata.batch_for(kind, V, B, T, 1337 + 1000 * rank + i) for i in range(nb)]
+    toks = [torch.from_numpy(x.reshape(-1)).cuda() for x, _ in host]
+    tgts = [torch.from_numpy(y.reshape(-1)).cuda() for _, y in host]
+    lr = lambda it: gpt2.lr_schedule(it, 715, 19073, 6e-4, 6e-5)
+
+    def train_step(i, it):
+        model.forward(toks[i], tgts[i], sync_loss=False)
+        model.backward()
+        model.step(lr(it), sync_norm=False)
+        model.zero_grad()
+
+    for i in range(args.warmup):
+        train_step(i, i)
+    model.sync()
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        train_step(args.warmup + k, args.warmup + k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    model.sync()
+    ms = barrier_max(ms, world, torch)
+    ms_step = ms / args.steps
+    tokens_step = B * T * world
+    value = tokens_step / (ms_step / 1000.0)
+
+    # ---- per-kernel measurement: CUDA events around every launch site, same
+    # workload, a few steps after the timed region
+    model.profile(True)
+    psteps = max(1, min(3, args.steps))
+    for k in range(psteps):
+        train_step(k % nb, args.warmup + args.steps + k)
+    rep = model.profile_report()
+    model.profile(False)
+    per_step = {r["name"]: r for r in rep}
+    kernels_per_step = sum(r["kernels"] for r in rep) / psteps
+    peaks = load_peaks()
+    gemm = [r for r in rep if r["name"].startswith("gemm_")]
+    g_ms = sum(r["ms"] for r in gemm)
+    g_flops = sum(r["flops"] for r in gemm)
+    g_launch = sum(r["calls"] for r in gemm)
+    achieved_tf = g_flops / (g_ms / 1000.0) / 1e12 if g_ms > 0 else None
+    total_ms = sum(r["ms"] for r in rep)
+    traffic = traffic_from_profiles(os.path.join(ROOT, "decoder_only_transformer_06_b300", "csrc",
+                                                 "k_gemm_tc.cu"))
+    roofline = {
+        "bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05; every Linear fwd/dX/dW)",
+        "achieved": achieved_tf, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
+        "frac": (achieved_tf / peaks["bf16_sus"]) if achieved_tf else None,
+        "traffic": traffic,
+        "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside the step)",
+        "launches_per_step": g_launch / psteps,
+        "share_of_step": g_ms / total_ms if total_ms else None,
+    }
+    mem_kernels = {}
+    for name in ("layernorm_fwd", "layernorm_bwd", "cross_entropy", "adamw", "grad_norm",
+                 "embed_fwd", "embed_bwd", "bias_colsum", "splitk_reduce"):
+        r = per_step.get(name)
+        if r and r["ms"] > 0:
+            gbs = r["bytes"] / (r["ms"] / 1000.0) / 1e9
+            mem_kernels[name] = {"GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm"], 3),
+                                 "frac_of_8TBs": round(gbs / 8000.0, 3),
+                                 "ms_per_step": round(r["ms"] / psteps, 4)}
+    attn = {}
+    for name in ("attention_fwd", "attention_bwd"):
+        r = per_step.get(name)
+        if r and r["ms"] > 0:
+            attn[name] = {"TFLOP/s": round(r["flops"] / (r["ms"] / 1000.0) / 1e12, 1),
+                          "ms_per_step": round(r["ms"] / psteps, 4)}
+    sites = {r["name"]: round(r["ms"] / psteps, 4) for r in sorted(rep, key=lambda r: -r["ms"])}
+
+    # ---- end to end through the public API with host buffers
+    pin_t = [torch.from_numpy(x.reshape(-1)).pin_memory() for x, _ in host]
+    pin_y = [torch.from_numpy(y.reshape(-1)).pin_memory() for _, y in host]
+    dt, dy = torch.empty_like(toks[0]), torch.empty_like(tgts[0])
+    e2e_steps = max(2, min(args.steps, 10))
+
+    def e2e_step(i, it):
+        with torch.cuda.stream(stream):
+            dt.copy_(pin_t[i], non_blocking=True)
+            dy.copy_(pin_y[i], non_blocking=True)
+        model.forward(dt, dy, sync_loss=False)
+        model.backward()
+        model.step(lr(it), sync_norm=False)
+        model.zero_grad()
+        return model.loss()          # device -> host read of the step's loss
+
+    for i in range(2):
+        e2e_step(i % nb, i)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for k in range(e2e_steps):
+        e2e_step(k % nb, k)
+    e2e_s = barrier_max(time.perf_counter() - t0, world, torch)
+    e2e_value = tokens_step * e2e_steps / e2e_s
+
+    fpt = flops_per_token(L, C, Vp, T, T)
+    step_flops = fpt * B * T * world
+    achieved = step_flops / (ms_step / 1000.0)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic Zipf(1.1) token ids (seeded), random-init weights",
+        "config": {"workload": args.workload, "global_batch": B * world, "seq_len": T,
+                   "n_layer": L, "n_head": H, "d_model": C, "vocab": V, "padded_vocab": Vp,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "working set (7+ GB of weights and activations) far larger than L2"},
+        "mfu": {"flops_per_token": fpt, "achieved_tflops": achieved / 1e12,
+                "vs_nominal_2.25PF": achieved / NOMINAL_BF16_DENSE / world,
+                "vs_measured_burst": achieved / (peaks["bf16"] * 1e12) / world},
+        "roofline": roofline,
+        "memory_bound_kernels": mem_kernels,
+        "attention": attn,
+        "site_ms_per_step": sites,
+        "gpu_launches": int(round(kernels_per_step * args.steps)),
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(2 * B * T * 4), "d2h_bytes_per_step": 4,
+                "steps": e2e_steps},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, cores, sample = cpu_oracle_time(args.workload, min(T, 1024), 1)
+        line["cpu_baseline"] = {"value": min(T, 1024) / times[0], "unit": "tokens/s",
+                                "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2_124m")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,963 @@
+// C ABI of the GPT-2 training-step library: model state, memory plan, host
+// init, and the orchestration of one forward / backward / optimizer step.
+#include "gpt2.h"
+#include "common.cuh"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#define GPT2_VERSION "gpt2-b300 0.1.0 (sm_103a)"
+static const double PI_D = 3.14159265358979323846;
+
+namespace {
+
+struct TensorRec {
+    std::string name;
+    int ndim;
+    int64_t shape[2];
+    int64_t offset;   // elements into the arenas
+    int64_t numel;
+    bool decays;
+};
+
+struct LayerActs {
+    float* x_in;      // residual stream entering the layer (fp32 [M,C])
+    float* x_mid;     // after the attention branch
+    void* u1;         // ln_1 output (act [M,C])
+    float* mu1;
+    float* rs1;
+    void* qkv;        // act [M,3C]
+    void* att;        // attention output, heads side by side (act [M,C])
+    float* lse;       // [B,H,T]
+    void* u2;
+    float* mu2;
+    float* rs2;
+    void* hpre;       // fc output before GELU (act [M,4C])
+    void* hgel;       // after GELU
+};
+
+// canonical per-layer tensor order (after wte, wpe)
+enum { T_LN1G, T_LN1B, T_ATTW, T_ATTB, T_APW, T_APB, T_LN2G, T_LN2B, T_FCW, T_FCB, T_MPW, T_MPB,
+       T_PER_LAYER };
+
+std::string g_create_error = "no error";
+
+}  // namespace
+
+struct gpt2_model {
+    gpt2_config cfg{};
+    int L = 0, H = 0, C = 0, hs = 0, V = 0, Vp = 0, T = 0, B = 0, M = 0, accum = 1;
+    bool use_bf16 = false;
+    size_t act_bytes = 4;
+    cudaStream_t stream = nullptr;
+
+    std::vector<TensorRec> tensors;
+    int64_t n_arena = 0, decay_end = 0;
+    float* params = nullptr;
+    float* grads = nullptr;
+    float* adam_m = nullptr;
+    float* adam_v = nullptr;
+    bf16* pbf = nullptr;        // bf16 copy of [0, decay_end)
+
+    std::vector<LayerActs> la;
+    float* x_final = nullptr;
+    void* uf = nullptr;
+    float* muf = nullptr;
+    float* rsf = nullptr;
+    void* logits = nullptr;
+    float* row_loss = nullptr;
+
+    float* dres = nullptr;
+    void* dres_act = nullptr;
+    void* du = nullptr;
+    void* dqkv = nullptr;
+    void* datt = nullptr;
+    void* dh = nullptr;
+    float* Dbuf = nullptr;
+    float* ln_partial = nullptr;
+    float* cs_partial = nullptr;
+    float* splitk_ws = nullptr;
+    size_t splitk_ws_floats = 0;
+    void* emb_ws = nullptr;
+    double* norm_partial = nullptr;
+    int norm_parts = 0;
+    DevState* st = nullptr;
+
+    const int32_t* last_tok = nullptr;
+    bool have_targets = false;
+
+    // profiling (see gpt2_profile)
+    struct SiteAcc {
+        const char* name;
+        int64_t calls, kernels;
+        double ms, flops, bytes;
+    };
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;
+    int prof_next = 0;
+    std::vector<std::pair<int, int>> prof_pending;   // (site, event index)
+    std::vector<SiteAcc> sites;
+    std::string err = "no error";
+    std::vector<void*> allocs;
+
+    // --- helpers
+    float* P(int i) const { return params + tensors[i].offset; }
+    float* G(int i) const { return grads + tensors[i].offset; }
+    // GEMM view of a weight: bf16 copy in bf16 mode, fp32 master otherwise
+    const void* W(int i) const {
+        return use_bf16 ? (const void*)(pbf + tensors[i].offset) : (const void*)(params + tensors[i].offset);
+    }
+    int lt(int l, int k) const { return 2 + l * T_PER_LAYER + k; }
+    int lnf_g() const { return 2 + L * T_PER_LAYER; }
+};
+
+static int fail(gpt2_model* m, int code, const std::string& msg) {
+    if (m) m->err = msg;
+    else g_create_error = msg;
+    return code;
+}
+static int fail_cuda(gpt2_model* m, const char* what, cudaError_t e) {
+    return fail(m, GPT2_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+#define CK(m, expr)                                                 \
+    do {                                                            \
+        cudaError_t e__ = (expr);                                   \
+        if (e__ != cudaSuccess) return fail_cuda((m), #expr, e__);  \
+    } while (0)
+
+// ------------------------------------------------------------------ host init
+// SplitMix64 (Steele, Lea & Flood 2014): output of a generator advanced once
+// from `state`.
+static inline uint64_t mix64(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+static const uint64_t GOLDEN = 0x9E3779B97F4A7C15ull;
+
+// Standard normal for element i of tensor k: state = seed ^ (k*2^40 + i);
+// r1, r2 the first two SplitMix64 outputs; u1 = ((r1>>11)+1)*2^-53 in (0,1],
+// u2 = (r2>>11)*2^-53 in [0,1); z = sqrt(-2 ln u1) cos(2 pi u2) (Box-Muller).
+static inline double init_normal(uint64_t seed, int k, uint64_t i) {
+    uint64_t state = seed ^ ((uint64_t)k * (1ull << 40) + i);
+    uint64_t r1 = mix64(state + GOLDEN);
+    uint64_t r2 = mix64(state + 2 * GOLDEN);
+    double u1 = ((double)(r1 >> 11) + 1.0) * (1.0 / 9007199254740992.0);
+    double u2 = (double)(r2 >> 11) * (1.0 / 9007199254740992.0);
+    return std::sqrt(-2.0 * std::log(u1)) * std::cos(2.0 * PI_D * u2);
+}
+
+struct Plan {
+    std::vector<TensorRec> t;
+    int64_t n_arena = 0, decay_end = 0;
+};
+
+static int validate_cfg(const gpt2_config* c, std::string& why) {
+    if (!c) { why = "config is NULL"; return GPT2_EINVAL; }
+    if (c->n_layer <= 0 || c->n_head <= 0 || c->d_model <= 0 || c->vocab_size <= 0 ||
+        c->block_size <= 0 || c->batch_size <= 0 || c->seq_len <= 0) {
+        why = "every size must be positive"; return GPT2_EINVAL;
+    }
+    if (c->d_model % c->n_head) { why = "d_model must be a multiple of n_head"; return GPT2_EINVAL; }
+    if (c->seq_len > c->block_size) { why = "seq_len exceeds block_size"; return GPT2_EINVAL; }
+    if (c->precision != GPT2_FP32 && c->precision != GPT2_BF16) {
+        why = "precision must be GPT2_FP32 or GPT2_BF16"; return GPT2_EINVAL;
+    }
+    int Vp = c->padded_vocab ? c->padded_vocab : ((c->vocab_size + 127) / 128) * 128;
+    if (Vp < c->vocab_size || Vp % 64) {
+        why = "padded_vocab must be >= vocab_size and a multiple of 64"; return GPT2_EINVAL;
+    }
+    if (c->d_model % 32) { why = "d_model must be a multiple of 32"; return GPT2_EINVAL; }
+    if (c->d_model > 2048) { why = "d_model above 2048 is not supported"; return GPT2_EINVAL; }
+    int hs = c->d_model / c->n_head;
+    if (hs > 128) { why = "head size above 128 is not supported"; return GPT2_EINVAL; }
+    int64_t M = (int64_t)c->batch_size * c->seq_len;
+    if (M > 32768) { why = "batch_size*seq_len above 32768 is not supported"; return GPT2_EINVAL; }
+    if ((uint64_t)Vp * (uint64_t)M >= (1ull << 32)) {
+        why = "padded_vocab*batch_size*seq_len must be below 2^32"; return GPT2_EINVAL;
+    }
+    if (c->precision == GPT2_BF16) {
+        if (hs != 64) { why = "bf16 mode needs head size 64"; return GPT2_EINVAL; }
+        if (c->d_model % 64) { why = "bf16 mode needs d_model % 64 == 0"; return GPT2_EINVAL; }
+    }
+    if (c->grad_accum_steps < 0) { why = "grad_accum_steps must be >= 0"; return GPT2_EINVAL; }
+    return GPT2_OK;
+}
+
+// Canonical tensor list; the arena keeps every 2-D tensor first (so AdamW's
+// decay mask is one comparison) and aligns each tensor to 64 elements.
+static Plan make_plan(const gpt2_config* c) {
+    Plan p;
+    const int C = c->d_model, L = c->n_layer;
+    const int Vp = c->padded_vocab ? c->padded_vocab : ((c->vocab_size + 127) / 128) * 128;
+    auto add = [&](const std::string& n, int64_t a, int64_t b) {
+        TensorRec r;
+        r.name = n;
+        r.ndim = b ? 2 : 1;
+        r.shape[0] = a;
+        r.shape[1] = b;
+        r.numel = b ? a * b : a;
+        r.decays = b != 0;
+        r.offset = -1;
+        p.t.push_back(r);
+    };
+    add("wte", Vp, C);
+    add("wpe", c->block_size, C);
+    for (int l = 0; l < L; l++) {
+        std::string h = "h" + std::to_string(l) + ".";
+        add(h + "ln1.g", C, 0);
+        add(h + "ln1.b", C, 0);
+        add(h + "attn.W", 3 * C, C);
+        add(h + "attn.b", 3 * C, 0);
+        add(h + "attn_proj.W", C, C);
+        add(h + "attn_proj.b", C, 0);
+        add(h + "ln2.g", C, 0);
+        add(h + "ln2.b", C, 0);
+        add(h + "fc.W", 4 * C, C);
+        add(h + "fc.b", 4 * C, 0);
+        add(h + "mlp_proj.W", C, 4 * C);
+        add(h + "mlp_proj.b", C, 0);
+    }
+    add("lnf.g", C, 0);
+    add("lnf.b", C, 0);
+    int64_t off = 0;
+    for (int pass = 0; pass < 2; pass++) {
+        for (auto& r : p.t) {
+            if (r.decays != (pass == 0)) continue;
+            r.offset = off;
+            off += (r.numel + 63) / 64 * 64;
+        }
+        if (pass == 0) p.decay_end = off;
+    }
+    p.n_arena = off;
+    return p;
+}
+
+static void host_init_tensor(const gpt2_config* c, const TensorRec& r, int k, uint64_t seed,
+                             float* dst) {
+    const bool gain = r.name.size() >= 2 && r.name.compare(r.name.size() - 2, 2, ".g") == 0;
+    const bool is_resid = r.name.find("attn_proj.W") != std::string::npos ||
+                          r.name.find("mlp_proj.W") != std::string::npos;
+    if (r.ndim == 1) {
+        for (int64_t i = 0; i < r.numel; i++) dst[i] = gain ? 1.0f : 0.0f;
+        return;
+    }
+    const double std_ = is_resid ? 0.02 / std::sqrt(2.0 * c->n_layer) : 0.02;
+    const int nthreads = r.numel > (1 << 20) ? 8 : 1;
+    std::vector<std::thread> th;
+    for (int w = 0; w < nthreads; w++) {
+        th.emplace_back([&, w]() {
+            int64_t a = r.numel * w / nthreads, b = r.numel * (w + 1) / nthreads;
+            for (int64_t i = a; i < b; i++) dst[i] = (float)(std_ * init_normal(seed, k, (uint64_t)i));
+        });
+    }
+    for (auto& t : th) t.join();
+}
+
+// ------------------------------------------------------------------ create
+static int alloc_dev(gpt2_model* m, void** p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(m, GPT2_ENOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed: " +
+                                        cudaGetErrorString(e));
+    }
+    m->allocs.push_back(*p);
+    return GPT2_OK;
+}
+#define ALLOC(m, ptr, bytes)                                              \
+    do {                                                                  \
+        void* p__ = nullptr;                                              \
+        int r__ = alloc_dev((m), &p__, (bytes));                          \
+        if (r__) return r__;                                              \
+        (ptr) = (decltype(ptr))p__;                                       \
+    } while (0)
+
+static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
+    m->cfg = *cfg;
+    m->L = cfg->n_layer;
+    m->H = cfg->n_head;
+    m->C = cfg->d_model;
+    m->hs = m->C / m->H;
+    m->V = cfg->vocab_size;
+    m->Vp = cfg->padded_vocab ? cfg->padded_vocab : ((m->V + 127) / 128) * 128;
+    m->T = cfg->seq_len;
+    m->B = cfg->batch_size;
+    m->M = m->B * m->T;
+    m->accum = cfg->grad_accum_steps > 0 ? cfg->grad_accum_steps : 1;
+    m->use_bf16 = cfg->precision == GPT2_BF16;
+    m->act_bytes = m->use_bf16 ? 2 : 4;
+    Plan p = make_plan(cfg);
+    m->tensors = p.t;
+    m->n_arena = p.n_arena;
+    m->decay_end = p.decay_end;
+
+    const size_t nb = (size_t)m->n_arena * sizeof(float);
+    ALLOC(m, m->params, nb);
+    ALLOC(m, m->grads, nb);
+    ALLOC(m, m->adam_m, nb);
+    ALLOC(m, m->adam_v, nb);
+    if (m->use_bf16) ALLOC(m, m->pbf, (size_t)m->decay_end * sizeof(bf16));
+    ALLOC(m, m->st, sizeof(DevState));
+
+    const size_t M = m->M, C = m->C, A = m->act_bytes;
+    m->la.resize(m->L);
+    for (int l = 0; l < m->L; l++) {
+        LayerActs& a = m->la[l];
+        ALLOC(m, a.x_in, M * C * 4);
+        ALLOC(m, a.x_mid, M * C * 4);
+        ALLOC(m, a.u1, M * C * A);
+        ALLOC(m, a.mu1, M * 4);
+        ALLOC(m, a.rs1, M * 4);
+        ALLOC(m, a.qkv, M * 3 * C * A);
+        ALLOC(m, a.att, M * C * A);
+        ALLOC(m, a.lse, M * m->H * 4);
+        ALLOC(m, a.u2, M * C * A);
+        ALLOC(m, a.mu2, M * 4);
+        ALLOC(m, a.rs2, M * 4);
+        ALLOC(m, a.hpre, M * 4 * C * A);
+        ALLOC(m, a.hgel, M * 4 * C * A);
+    }
+    ALLOC(m, m->x_final, M * C * 4);
+    ALLOC(m, m->uf, M * C * A);
+    ALLOC(m, m->muf, M * 4);
+    ALLOC(m, m->rsf, M * 4);
+    ALLOC(m, m->logits, M * (size_t)m->Vp * A);
+    ALLOC(m, m->row_loss, M * 4);
+
+    ALLOC(m, m->dres, M * C * 4);
+    if (m->use_bf16) ALLOC(m, m->dres_act, M * C * A);
+    else m->dres_act = m->dres;
+    ALLOC(m, m->du, M * C * A);
+    ALLOC(m, m->dqkv, M * 3 * C * A);
+    ALLOC(m, m->datt, M * C * A);
+    ALLOC(m, m->dh, M * 4 * C * A);
+    ALLOC(m, m->Dbuf, M * m->H * 4);
+    ALLOC(m, m->ln_partial, k::layernorm_bwd_partial_floats(m->M, m->C) * 4);
+    size_t cs = k::colsum_partial_floats(m->M, 4 * m->C);
+    ALLOC(m, m->cs_partial, cs * 4);
+    ALLOC(m, m->emb_ws, k::embed_bwd_workspace(m->M, m->C));
+    m->norm_parts = 2 * k::num_sms();
+    ALLOC(m, m->norm_partial, (size_t)m->norm_parts * sizeof(double));
+    // split-K workspace for the weight gradients (tensor-core path)
+    if (m->use_bf16) {
+        size_t need = 0;
+        const int dims[4][2] = {{3 * m->C, m->C}, {m->C, m->C}, {4 * m->C, m->C}, {m->C, 4 * m->C}};
+        for (auto& d : dims) {
+            int tiles = ((d[0] + 127) / 128) * ((d[1] + (d[1] % 256 == 0 ? 255 : 127)) /
+                                                (d[1] % 256 == 0 ? 256 : 128));
+            int splits = (k::num_sms() + tiles - 1) / tiles;
+            if (splits > 16) splits = 16;
+            if (splits > 1) need = std::max(need, (size_t)splits * d[0] * d[1]);
+        }
+        m->splitk_ws_floats = need;
+        if (need) ALLOC(m, m->splitk_ws, need * 4);
+    }
+
+    // host init in canonical order, then upload
+    std::vector<float> host((size_t)m->n_arena, 0.0f);
+    for (size_t k = 0; k < m->tensors.size(); k++)
+        host_init_tensor(cfg, m->tensors[k], (int)k, seed, host.data() + m->tensors[k].offset);
+    CK(m, cudaMemcpy(m->params, host.data(), nb, cudaMemcpyHostToDevice));
+    CK(m, cudaMemset(m->grads, 0, nb));
+    CK(m, cudaMemset(m->adam_m, 0, nb));
+    CK(m, cudaMemset(m->adam_v, 0, nb));
+    CK(m, cudaMemset(m->st, 0, sizeof(DevState)));
+    if (m->use_bf16) CK(m, k::f32_to_bf16(m->params, m->pbf, m->decay_end, nullptr));
+    CK(m, cudaDeviceSynchronize());
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+// Optional per-site timing: CUDA events recorded on the model's stream around
+// each launch site, with the site's algorithmic FLOPs and HBM bytes.
+struct ProfRec {
+    int site;
+    int ev;
+    int kernels;
+    double flops, bytes;
+};
+
+static int site_id(gpt2_model* m, const char* name);
+static int prof_begin(gpt2_model* m);
+static void prof_end(gpt2_model* m, int ev, const char* site, int kernels, double flops,
+                     double bytes);
+
+#define RUN(m, site, nk, flops, bytes, expr)            \
+    do {                                                \
+        int ev__ = prof_begin(m);                       \
+        CK(m, expr);                                    \
+        prof_end(m, ev__, site, nk, flops, bytes);      \
+    } while (0)
+
+static int site_id(gpt2_model* m, const char* name) {
+    for (size_t i = 0; i < m->sites.size(); i++)
+        if (m->sites[i].name == name || std::strcmp(m->sites[i].name, name) == 0) return (int)i;
+    m->sites.push_back({name, 0, 0, 0.0, 0.0, 0.0});
+    return (int)m->sites.size() - 1;
+}
+
+static int prof_begin(gpt2_model* m) {
+    if (!m->prof_on) return -1;
+    while ((int)m->prof_ev.size() < m->prof_next + 2) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return -1;
+        m->prof_ev.push_back(e);
+    }
+    int ev = m->prof_next;
+    m->prof_next += 2;
+    cudaEventRecord(m->prof_ev[ev], m->stream);
+    return ev;
+}
+
+static void prof_end(gpt2_model* m, int ev, const char* site, int kernels, double flops,
+                     double bytes) {
+    int id = site_id(m, site);
+    auto& a = m->sites[id];
+    a.calls += 1;
+    a.kernels += kernels;
+    a.flops += flops;
+    a.bytes += bytes;
+    if (ev >= 0) {
+        cudaEventRecord(m->prof_ev[ev + 1], m->stream);
+        m->prof_pending.push_back({id, ev});
+    }
+}
+
+static int prof_collect(gpt2_model* m) {
+    CK(m, cudaStreamSynchronize(m->stream));
+    for (auto& pr : m->prof_pending) {
+        float ms = 0.f;
+        CK(m, cudaEventElapsedTime(&ms, m->prof_ev[pr.second], m->prof_ev[pr.second + 1]));
+        m->sites[pr.first].ms += ms;
+    }
+    m->prof_pending.clear();
+    m->prof_next = 0;
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ GEMM dispatch
+struct Op {
+    gpt2_model* m;
+    // D[M,N] = A B^T with epilogue e; `site` names the Linear for profiling.
+    int gemm(const char* site, int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& e) {
+        const double ab = m->act_bytes;
+        double bytes = ab * ((double)M * K + (double)N * K);
+        double ob = (e.kind == EPI_RESID || e.kind == EPI_ACCUM_F32) ? 8.0 : (e.kind == EPI_GELU ? 2 * ab : ab);
+        if (e.kind == EPI_GELU_BWD) ob = 2 * ab;
+        bytes += ob * (double)M * N;
+        if (m->use_bf16)
+            RUN(m, site, 1, 2.0 * M * N * K, bytes, k::gemm_bf16_tc(M, N, K, A, B, e, 1, m->st, m->stream));
+        else
+            RUN(m, site, 1, 2.0 * M * N * K, bytes, k::gemm_f32(M, N, K, A, B, e, m->stream));
+        return GPT2_OK;
+    }
+    // dW[N_out, K_in] += dY^T X, dY [M, N_out] (ld ldy), X [M, K_in] (ld ldx).
+    int gemm_dw(const char* site, int n_out, int k_in, const void* dy, int64_t ldy, const void* x,
+                int64_t ldx, float* dW) {
+        GemmOperand A{dy, ldy, false}, B{x, ldx, false};
+        const int M = m->M;
+        const double flops = 2.0 * n_out * k_in * (double)M;
+        const double bytes = m->act_bytes * (double)M * (n_out + k_in) + 8.0 * n_out * k_in;
+        if (!m->use_bf16) {
+            GemmEpi e{EPI_ACCUM_F32, nullptr, dW, k_in, nullptr, 0, nullptr, 0};
+            RUN(m, site, 1, flops, bytes, k::gemm_f32(n_out, k_in, M, A, B, e, m->stream));
+            return GPT2_OK;
+        }
+        const int bn = (k_in % 256 == 0 || k_in > 2048) ? 256 : 128;
+        int tiles = ((n_out + 127) / 128) * ((k_in + bn - 1) / bn);
+        int splits = (k::num_sms() + tiles - 1) / tiles;
+        if (splits > 16) splits = 16;
+        if (splits > 1 && (size_t)splits * n_out * k_in <= m->splitk_ws_floats) {
+            GemmEpi e{EPI_STORE_F32, nullptr, m->splitk_ws, k_in, nullptr, 0, nullptr, 0};
+            // the launcher lowers `splits` so that every split owns k-blocks
+            int kblocks = (M + 63) / 64;
+            int kpb = (kblocks + splits - 1) / splits;
+            int eff = (kblocks + kpb - 1) / kpb;
+            RUN(m, site, 1, flops, bytes - 8.0 * n_out * k_in + 4.0 * eff * n_out * k_in,
+                k::gemm_bf16_tc(n_out, k_in, M, A, B, e, splits, m->st, m->stream));
+            RUN(m, "splitk_reduce", 1, 0.0, 4.0 * (eff + 2) * n_out * (double)k_in,
+                k::splitk_reduce_add(m->splitk_ws, eff, (int64_t)n_out * k_in, dW, m->stream));
+            return GPT2_OK;
+        }
+        GemmEpi e{EPI_ACCUM_F32, nullptr, dW, k_in, nullptr, 0, nullptr, 0};
+        RUN(m, site, 1, flops, bytes, k::gemm_bf16_tc(n_out, k_in, M, A, B, e, 1, m->st, m->stream));
+        return GPT2_OK;
+    }
+};
+
+#define OPR(expr)                 \
+    do {                          \
+        int r__ = (expr);         \
+        if (r__) return r__;      \
+    } while (0)
+
+// causal attention algorithmic FLOPs: two T x T x hs products over the
+// visible (i, j <= i) pairs forward; five in the backward (S recomputed, dV,
+// dP, dQ, dK).
+static double attn_flops(const gpt2_model* m, int products) {
+    double pairs = (double)m->T * (m->T + 1) / 2.0;
+    return 2.0 * products * pairs * m->hs * (double)m->B * m->H;
+}
+
+template <typename Act>
+static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
+    cudaStream_t s = m->stream;
+    const int M = m->M, C = m->C, L = m->L, T = m->T, B = m->B, H = m->H;
+    const double A = m->act_bytes, MC = (double)M * C;
+    Op op{m};
+    RUN(m, "validate", 1, 0, 8.0 * M, k::validate_inputs(tok, tgt, M, m->V, m->st, m->accum, s));
+    RUN(m, "embed_fwd", 1, 0, 4.0 * M + 12.0 * MC,
+        k::embed_fwd(tok, m->P(0), m->P(1), m->la[0].x_in, M, T, C, m->V, s));
+    const double ln_bytes = MC * (4 + A) + 8.0 * M;
+    for (int l = 0; l < L; l++) {
+        LayerActs& a = m->la[l];
+        float* x_next = (l + 1 < L) ? m->la[l + 1].x_in : m->x_final;
+        RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
+            k::layernorm_fwd<Act>(a.x_in, m->P(m->lt(l, T_LN1G)), m->P(m->lt(l, T_LN1B)), (Act*)a.u1,
+                                  a.mu1, a.rs1, M, C, s));
+        {
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_ATTB)), a.qkv, 3 * C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("gemm_qkv_fwd", M, 3 * C, C, {a.u1, C, true}, {m->W(m->lt(l, T_ATTW)), C, true}, e));
+        }
+        if (m->use_bf16)
+            RUN(m, "attention_fwd", 1, attn_flops(m, 2), MC * A * 4,
+                k::attention_fwd_bf16((const bf16*)a.qkv, (bf16*)a.att, a.lse, B, T, H, m->hs, s));
+        else
+            RUN(m, "attention_fwd", 1, attn_flops(m, 2), MC * A * 4,
+                k::attention_fwd_f32((const float*)a.qkv, (float*)a.att, a.lse, B, T, H, m->hs, s));
+        {
+            GemmEpi e{EPI_RESID, m->P(m->lt(l, T_APB)), a.x_mid, C, nullptr, 0, a.x_in, C};
+            OPR(op.gemm("gemm_attproj_fwd", M, C, C, {a.att, C, true}, {m->W(m->lt(l, T_APW)), C, true}, e));
+        }
+        RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
+            k::layernorm_fwd<Act>(a.x_mid, m->P(m->lt(l, T_LN2G)), m->P(m->lt(l, T_LN2B)), (Act*)a.u2,
+                                  a.mu2, a.rs2, M, C, s));
+        {
+            GemmEpi e{EPI_GELU, m->P(m->lt(l, T_FCB)), a.hpre, 4 * C, a.hgel, 4 * C, nullptr, 0};
+            OPR(op.gemm("gemm_fc_fwd", M, 4 * C, C, {a.u2, C, true}, {m->W(m->lt(l, T_FCW)), C, true}, e));
+        }
+        {
+            GemmEpi e{EPI_RESID, m->P(m->lt(l, T_MPB)), x_next, C, nullptr, 0, a.x_mid, C};
+            OPR(op.gemm("gemm_mlpproj_fwd", M, C, 4 * C, {a.hgel, 4 * C, true},
+                        {m->W(m->lt(l, T_MPW)), 4 * C, true}, e));
+        }
+    }
+    RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
+        k::layernorm_fwd<Act>(m->x_final, m->P(m->lnf_g()), m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf,
+                              m->rsf, M, C, s));
+    {
+        // tied LM head: logits = uf wte^T over all Vp rows of wte (pad columns
+        // are masked by the cross-entropy)
+        GemmEpi e{EPI_STORE_ACT, nullptr, m->logits, m->Vp, nullptr, 0, nullptr, 0};
+        OPR(op.gemm("gemm_lmhead_fwd", M, m->Vp, C, {m->uf, C, true}, {m->W(0), C, true}, e));
+    }
+    if (tgt) {
+        RUN(m, "cross_entropy", 1, 0, 2.0 * A * M * m->Vp + 8.0 * M,
+            k::cross_entropy<Act>((Act*)m->logits, tgt, m->row_loss, M, m->V, m->Vp, m->st, s));
+        RUN(m, "loss_reduce", 1, 0, 4.0 * M, k::loss_reduce(m->row_loss, M, m->st, s));
+    }
+    return GPT2_OK;
+}
+
+template <typename Act>
+static int backward_impl(gpt2_model* m) {
+    cudaStream_t s = m->stream;
+    const int M = m->M, C = m->C, L = m->L, T = m->T, B = m->B, H = m->H, Vp = m->Vp;
+    const double A = m->act_bytes, MC = (double)M * C;
+    Op op{m};
+    // LN backward: read du, x, read+write dres (first call writes only), write dres_act
+    auto ln_bytes = [&](bool acc) { return MC * (A + 4 + (acc ? 8 : 4) + (m->use_bf16 ? A : 0)); };
+    // LM head: du = dz wte ; dwte += dz^T uf
+    {
+        GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
+        OPR(op.gemm("gemm_lmhead_dx", M, C, Vp, {m->logits, Vp, true}, {m->W(0), C, false}, e));
+        OPR(op.gemm_dw("gemm_lmhead_dw", Vp, C, m->logits, Vp, m->uf, C, m->G(0)));
+    }
+    RUN(m, "layernorm_bwd", 2, 0, ln_bytes(false),
+        k::layernorm_bwd<Act>((const Act*)m->du, m->x_final, m->P(m->lnf_g()), m->muf, m->rsf, m->dres,
+                              (Act*)m->dres_act, false, m->G(m->lnf_g()), m->G(m->lnf_g() + 1), M, C,
+                              m->ln_partial, s));
+    for (int l = L - 1; l >= 0; l--) {
+        LayerActs& a = m->la[l];
+        // MLP projection: x_out = x_mid + hgel W_mp^T + b_mp
+        {
+            GemmEpi e{EPI_GELU_BWD, nullptr, m->dh, 4 * C, nullptr, 0, a.hpre, 4 * C};
+            OPR(op.gemm("gemm_mlpproj_dx", M, 4 * C, C, {m->dres_act, C, true},
+                        {m->W(m->lt(l, T_MPW)), 4 * C, false}, e));
+            OPR(op.gemm_dw("gemm_mlpproj_dw", C, 4 * C, m->dres_act, C, a.hgel, 4 * C, m->G(m->lt(l, T_MPW))));
+            RUN(m, "bias_colsum", 2, 0, 4.0 * MC,
+                k::colsum_add<float>(m->dres, C, M, C, m->G(m->lt(l, T_MPB)), m->cs_partial, s));
+        }
+        // fc: hpre = u2 W_fc^T + b_fc
+        {
+            GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("gemm_fc_dx", M, C, 4 * C, {m->dh, 4 * C, true}, {m->W(m->lt(l, T_FCW)), C, false}, e));
+            OPR(op.gemm_dw("gemm_fc_dw", 4 * C, C, m->dh, 4 * C, a.u2, C, m->G(m->lt(l, T_FCW))));
+            RUN(m, "bias_colsum", 2, 0, 4.0 * MC * A,
+                k::colsum_add<Act>((const Act*)m->dh, 4 * C, M, 4 * C, m->G(m->lt(l, T_FCB)),
+                                   m->cs_partial, s));
+        }
+        RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
+            k::layernorm_bwd<Act>((const Act*)m->du, a.x_mid, m->P(m->lt(l, T_LN2G)), a.mu2, a.rs2,
+                                  m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN2G)),
+                                  m->G(m->lt(l, T_LN2B)), M, C, m->ln_partial, s));
+        // attention projection: x_mid = x_in + att W_ap^T + b_ap
+        {
+            GemmEpi e{EPI_STORE_ACT, nullptr, m->datt, C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("gemm_attproj_dx", M, C, C, {m->dres_act, C, true}, {m->W(m->lt(l, T_APW)), C, false}, e));
+            OPR(op.gemm_dw("gemm_attproj_dw", C, C, m->dres_act, C, a.att, C, m->G(m->lt(l, T_APW))));
+            RUN(m, "bias_colsum", 2, 0, 4.0 * MC,
+                k::colsum_add<float>(m->dres, C, M, C, m->G(m->lt(l, T_APB)), m->cs_partial, s));
+        }
+        if (m->use_bf16)
+            RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
+                k::attention_bwd_bf16((const bf16*)a.qkv, (const bf16*)a.att, a.lse, (const bf16*)m->datt,
+                                      (bf16*)m->dqkv, m->Dbuf, B, T, H, m->hs, s));
+        else
+            RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
+                k::attention_bwd_f32((const float*)a.qkv, (const float*)a.att, a.lse, (const float*)m->datt,
+                                     (float*)m->dqkv, m->Dbuf, B, T, H, m->hs, s));
+        // qkv: qkv = u1 W_attn^T + b_attn
+        {
+            GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("gemm_qkv_dx", M, C, 3 * C, {m->dqkv, 3 * C, true}, {m->W(m->lt(l, T_ATTW)), C, false}, e));
+            OPR(op.gemm_dw("gemm_qkv_dw", 3 * C, C, m->dqkv, 3 * C, a.u1, C, m->G(m->lt(l, T_ATTW))));
+            RUN(m, "bias_colsum", 2, 0, 3.0 * MC * A,
+                k::colsum_add<Act>((const Act*)m->dqkv, 3 * C, M, 3 * C, m->G(m->lt(l, T_ATTB)),
+                                   m->cs_partial, s));
+        }
+        RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
+            k::layernorm_bwd<Act>((const Act*)m->du, a.x_in, m->P(m->lt(l, T_LN1G)), a.mu1, a.rs1,
+                                  m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN1G)),
+                                  m->G(m->lt(l, T_LN1B)), M, C, m->ln_partial, s));
+    }
+    RUN(m, "embed_bwd", 4, 0, 4.0 * M + 8.0 * MC,
+        k::embed_bwd(m->last_tok, m->dres, m->G(0), m->G(1), M, T, C, m->V, m->emb_ws, s));
+    return GPT2_OK;
+}
+
+static int check_device_status(gpt2_model* m) {
+    DevState st;
+    CK(m, cudaMemcpyAsync(&st, m->st, sizeof(DevState), cudaMemcpyDeviceToHost, m->stream));
+    CK(m, cudaStreamSynchronize(m->stream));
+    if (st.err) {
+        unsigned zero = 0;
+        CK(m, cudaMemcpy(&m->st->err, &zero, sizeof(unsigned), cudaMemcpyHostToDevice));
+        if (st.err & ERR_TIMEOUT)
+            return fail(m, GPT2_ETIMEOUT, "a bounded device wait expired (site " +
+                                              std::to_string(st.timeout_site) + ")");
+        if (st.err & ERR_TOKEN_RANGE) return fail(m, GPT2_ERANGE, "token id outside [0, vocab_size)");
+        return fail(m, GPT2_ERANGE, "target id outside [0, vocab_size) and not -1");
+    }
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+const char* gpt2_version(void) { return GPT2_VERSION; }
+
+const char* gpt2_last_error(const gpt2_model* m) {
+    return m ? m->err.c_str() : g_create_error.c_str();
+}
+
+int gpt2_create(const gpt2_config* cfg, uint64_t seed, gpt2_model** out) {
+    if (!out) return fail(nullptr, GPT2_EINVAL, "out is NULL");
+    *out = nullptr;
+    std::string why;
+    int r = validate_cfg(cfg, why);
+    if (r) return fail(nullptr, r, why);
+    gpt2_model* m = new gpt2_model();
+    r = create_impl(m, cfg, seed);
+    if (r) {
+        g_create_error = m->err;
+        gpt2_destroy(m);
+        return r;
+    }
+    *out = m;
+    return GPT2_OK;
+}
+
+void gpt2_destroy(gpt2_model* m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    for (void* p : m->allocs) cudaFree(p);
+    delete m;
+}
+
+int gpt2_set_stream(gpt2_model* m, void* stream) {
+    if (!m) return GPT2_EINVAL;
+    m->stream = (cudaStream_t)stream;
+    return GPT2_OK;
+}
+
+int gpt2_forward(gpt2_model* m, const int32_t* tok, const int32_t* tgt, float* h_loss) {
+    if (!m) return GPT2_EINVAL;
+    if (!tok) return fail(m, GPT2_EINVAL, "tokens pointer is NULL");
+    int r = m->use_bf16 ? forward_impl<bf16>(m, tok, tgt) : forward_impl<float>(m, tok, tgt);
+    m->have_targets = false;
+    if (r) return r;
+    m->last_tok = tok;
+    m->have_targets = tgt != nullptr;
+    if (h_loss) {
+        if (!tgt) return fail(m, GPT2_EINVAL, "h_loss requested without targets");
+        return gpt2_get_loss(m, h_loss);
+    }
+    return GPT2_OK;
+}
+
+int gpt2_backward(gpt2_model* m) {
+    if (!m) return GPT2_EINVAL;
+    if (!m->have_targets) return fail(m, GPT2_ESTATE, "backward needs a forward with targets");
+    m->have_targets = false;   // the logits buffer now holds consumed gradients
+    return m->use_bf16 ? backward_impl<bf16>(m) : backward_impl<float>(m);
+}
+
+int gpt2_step(gpt2_model* m, float lr, float beta1, float beta2, float eps, float weight_decay,
+              float clip, float* h_grad_norm) {
+    if (!m) return GPT2_EINVAL;
+    cudaStream_t s = m->stream;
+    const double n = (double)m->n_arena;
+    RUN(m, "grad_norm", 1, 0, 4.0 * n,
+        k::grad_norm(m->grads, m->n_arena, m->norm_partial, m->norm_parts, s));
+    RUN(m, "step_finalize", 1, 0, 8.0 * m->norm_parts,
+        k::step_finalize(m->norm_partial, m->norm_parts, clip, beta1, beta2, m->st, s));
+    RUN(m, "adamw", 1, 0, 28.0 * n + (m->use_bf16 ? 2.0 * m->decay_end : 0.0),
+        k::adamw(m->params, m->grads, m->adam_m, m->adam_v, m->pbf, m->n_arena, m->decay_end,
+                 m->decay_end, lr, beta1, beta2, eps, weight_decay, m->st, s));
+    if (h_grad_norm) {
+        int r = check_device_status(m);
+        if (r) return r;
+        DevState st;
+        CK(m, cudaMemcpy(&st, m->st, sizeof(DevState), cudaMemcpyDeviceToHost));
+        *h_grad_norm = st.grad_norm;
+        if (st.skip) return fail(m, GPT2_ENONFINITE, "non-finite gradient norm: update skipped");
+    }
+    return GPT2_OK;
+}
+
+int gpt2_zero_grad(gpt2_model* m) {
+    if (!m) return GPT2_EINVAL;
+    RUN(m, "zero_grad", 0, 0, 4.0 * m->n_arena,
+        cudaMemsetAsync(m->grads, 0, (size_t)m->n_arena * sizeof(float), m->stream));
+    return GPT2_OK;
+}
+
+double gpt2_lr_schedule(int64_t it, int64_t warmup, int64_t horizon, double lr_max, double lr_min) {
+    if (it < warmup) return lr_max * (double)(it + 1) / (double)warmup;
+    if (it > horizon) return lr_min;
+    double ratio = (double)(it - warmup) / (double)(horizon - warmup);
+    return lr_min + 0.5 * (1.0 + std::cos(PI_D * ratio)) * (lr_max - lr_min);
+}
+
+int gpt2_sync(gpt2_model* m) {
+    if (!m) return GPT2_EINVAL;
+    return check_device_status(m);
+}
+
+int gpt2_get_loss(gpt2_model* m, float* h_loss) {
+    if (!m || !h_loss) return GPT2_EINVAL;
+    int r = check_device_status(m);
+    if (r) return r;
+    DevState st;
+    CK(m, cudaMemcpy(&st, m->st, sizeof(DevState), cudaMemcpyDeviceToHost));
+    *h_loss = st.loss;
+    return GPT2_OK;
+}
+
+int gpt2_num_tensors(const gpt2_model* m) { return m ? (int)m->tensors.size() : GPT2_EINVAL; }
+
+int gpt2_tensor_info(const gpt2_model* m, int i, const char** name, int* ndim, int64_t shape[2],
+                     int* decays) {
+    if (!m || i < 0 || i >= (int)m->tensors.size()) return GPT2_EINVAL;
+    const TensorRec& r = m->tensors[i];
+    if (name) *name = r.name.c_str();
+    if (ndim) *ndim = r.ndim;
+    if (shape) { shape[0] = r.shape[0]; shape[1] = r.shape[1]; }
+    if (decays) *decays = r.decays ? 1 : 0;
+    return GPT2_OK;
+}
+
+static float* buffer_of(gpt2_model* m, int which) {
+    switch (which) {
+        case GPT2_PARAM: return m->params;
+        case GPT2_GRAD: return m->grads;
+        case GPT2_ADAM_M: return m->adam_m;
+        case GPT2_ADAM_V: return m->adam_v;
+    }
+    return nullptr;
+}
+
+int gpt2_copy_tensor(gpt2_model* m, int i, int which, float* dst) {
+    if (!m || !dst || i < 0 || i >= (int)m->tensors.size()) return GPT2_EINVAL;
+    float* buf = buffer_of(m, which);
+    if (!buf) return fail(m, GPT2_EINVAL, "unknown buffer selector");
+    CK(m, cudaStreamSynchronize(m->stream));
+    const TensorRec& r = m->tensors[i];
+    CK(m, cudaMemcpy(dst, buf + r.offset, r.numel * sizeof(float), cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+
+int gpt2_set_tensor(gpt2_model* m, int i, int which, const float* src) {
+    if (!m || !src || i < 0 || i >= (int)m->tensors.size()) return GPT2_EINVAL;
+    float* buf = buffer_of(m, which);
+    if (!buf) return fail(m, GPT2_EINVAL, "unknown buffer selector");
+    CK(m, cudaStreamSynchronize(m->stream));
+    const TensorRec& r = m->tensors[i];
+    CK(m, cudaMemcpy(buf + r.offset, src, r.numel * sizeof(float), cudaMemcpyHostToDevice));
+    if (which == GPT2_PARAM && m->use_bf16 && r.offset < m->decay_end) {
+        int64_t n = (r.numel + 63) / 64 * 64;
+        CK(m, k::f32_to_bf16(m->params + r.offset, m->pbf + r.offset, n, nullptr));
+    }
+    CK(m, cudaDeviceSynchronize());
+    return GPT2_OK;
+}
+
+int gpt2_copy_logits(gpt2_model* m, int64_t row0, int64_t nrows, float* dst) {
+    if (!m || !dst || row0 < 0 || nrows < 0 || row0 + nrows > m->M) return GPT2_EINVAL;
+    CK(m, cudaStreamSynchronize(m->stream));
+    const int Vp = m->Vp, V = m->V;
+    if (!m->use_bf16) {
+        CK(m, cudaMemcpy2D(dst, (size_t)V * 4, (const float*)m->logits + row0 * Vp, (size_t)Vp * 4,
+                           (size_t)V * 4, (size_t)nrows, cudaMemcpyDeviceToHost));
+        return GPT2_OK;
+    }
+    std::vector<uint16_t> tmp((size_t)nrows * V);
+    CK(m, cudaMemcpy2D(tmp.data(), (size_t)V * 2, (const bf16*)m->logits + row0 * Vp, (size_t)Vp * 2,
+                       (size_t)V * 2, (size_t)nrows, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < tmp.size(); i++) {
+        uint32_t u = (uint32_t)tmp[i] << 16;
+        std::memcpy(&dst[i], &u, 4);
+    }
+    return GPT2_OK;
+}
+
+int gpt2_copy_row_losses(gpt2_model* m, int64_t row0, int64_t nrows, float* dst) {
+    if (!m || !dst || row0 < 0 || nrows < 0 || row0 + nrows > m->M) return GPT2_EINVAL;
+    CK(m, cudaStreamSynchronize(m->stream));
+    CK(m, cudaMemcpy(dst, m->row_loss + row0, nrows * sizeof(float), cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+
+int64_t gpt2_num_params(const gpt2_model* m, int include_wpe, int padded) {
+    if (!m) return GPT2_EINVAL;
+    int64_t n = 0;
+    for (const auto& r : m->tensors) {
+        if (r.name == "wpe" && !include_wpe) continue;
+        if (r.name == "wte" && !padded) { n += (int64_t)m->V * m->C; continue; }
+        n += r.numel;
+    }
+    return n;
+}
+
+int gpt2_host_init_tensor(const gpt2_config* cfg, uint64_t seed, int kidx, float* dst) {
+    std::string why;
+    int r = validate_cfg(cfg, why);
+    if (r) return fail(nullptr, r, why);
+    Plan p = make_plan(cfg);
+    if (!dst || kidx < 0 || kidx >= (int)p.t.size()) return fail(nullptr, GPT2_EINVAL, "bad tensor index");
+    host_init_tensor(cfg, p.t[kidx], kidx, seed, dst);
+    return GPT2_OK;
+}
+
+int gpt2_profile(gpt2_model* m, int on) {
+    if (!m) return GPT2_EINVAL;
+    int r = prof_collect(m);
+    if (r) return r;
+    m->sites.clear();
+    m->prof_on = on != 0;
+    return GPT2_OK;
+}
+
+int gpt2_profile_count(gpt2_model* m) {
+    if (!m) return GPT2_EINVAL;
+    int r = prof_collect(m);
+    if (r) return r;
+    return (int)m->sites.size();
+}
+
+int gpt2_profile_entry(gpt2_model* m, int i, const char** name, int64_t* calls, int64_t* kernels,
+                       double* ms, double* flops, double* bytes) {
+    if (!m || i < 0 || i >= (int)m->sites.size()) return GPT2_EINVAL;
+    const auto& a = m->sites[i];
+    if (name) *name = a.name;
+    if (calls) *calls = a.calls;
+    if (kernels) *kernels = a.kernels;
+    if (ms) *ms = a.ms;
+    if (flops) *flops = a.flops;
+    if (bytes) *bytes = a.bytes;
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ op-level
+static DevState* op_state() {
+    static DevState* st = nullptr;
+    if (!st) {
+        if (cudaMalloc(&st, sizeof(DevState)) != cudaSuccess) return nullptr;
+        cudaMemset(st, 0, sizeof(DevState));
+    }
+    return st;
+}
+
+int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
+                      int64_t ldb, int b_kmajor, const float* bias, void* out_bf16, float* out_f32,
+                      int64_t ldd, int accumulate, void* stream) {
+    if (!A || !B || (!out_bf16 && !out_f32)) return fail(nullptr, GPT2_EINVAL, "NULL operand");
+    GemmEpi e{};
+    if (out_bf16) {
+        e = GemmEpi{EPI_STORE_ACT, bias, out_bf16, ldd, nullptr, 0, nullptr, 0};
+    } else if (accumulate) {
+        if (bias) return fail(nullptr, GPT2_EINVAL, "bias with accumulate is not supported");
+        e = GemmEpi{EPI_ACCUM_F32, nullptr, out_f32, ldd, nullptr, 0, nullptr, 0};
+    } else {
+        e = GemmEpi{EPI_STORE_F32, bias, out_f32, ldd, nullptr, 0, nullptr, 0};
+    }
+    GemmOperand a{A, lda, a_kmajor != 0}, b{B, ldb, b_kmajor != 0};
+    if (!k::gemm_bf16_tc_supported(M, N, K, a, b, e))
+        return fail(nullptr, GPT2_EINVAL, "unsupported GEMM shape/alignment");
+    DevState* st = op_state();
+    if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
+    cudaError_t r = k::gemm_bf16_tc(M, N, K, a, b, e, 1, st, (cudaStream_t)stream);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "gemm_bf16_tc", r);
+    return GPT2_OK;
+}
+
+int gpt2_op_attention_fwd(int precision, int B, int T, int H, int hs, const void* qkv, void* out,
+                          float* lse, void* stream) {
+    if (!qkv || !out || !lse || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
+        return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
+    cudaError_t r;
+    if (precision == GPT2_BF16)
+        r = k::attention_fwd_bf16((const bf16*)qkv, (bf16*)out, lse, B, T, H, hs, (cudaStream_t)stream);
+    else
+        r = k::attention_fwd_f32((const float*)qkv, (float*)out, lse, B, T, H, hs, (cudaStream_t)stream);
+    if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");
+    if (r != cudaSuccess) return fail_cuda(nullptr, "attention_fwd", r);
+    return GPT2_OK;
+}
+
+int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void* qkv,
+                          const void* out, const float* lse, const void* dout, void* dqkv,
+                          float* scratch, void* stream) {
+    if (!qkv || !out || !lse || !dout || !dqkv || !scratch || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
+        return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
+    cudaError_t r;
+    if (precision == GPT2_BF16)
+        r = k::attention_bwd_bf16((const bf16*)qkv, (const bf16*)out, lse, (const bf16*)dout,
+                                  (bf16*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+    else
+        r = k::attention_bwd_f32((const float*)qkv, (const float*)out, lse, (const float*)dout,
+                                 (float*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+    if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");
+    if (r != cudaSuccess) return fail_cuda(nullptr, "attention_bwd", r);
+    return GPT2_OK;
+}
+
+}  // extern "C"

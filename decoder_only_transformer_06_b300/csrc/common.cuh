@@ -1,0 +1,175 @@
+// Shared definitions for the GPT-2 training-step kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+// Device status word bits (DevState::err).
+#define ERR_TOKEN_RANGE   1u
+#define ERR_TARGET_RANGE  2u
+#define ERR_TIMEOUT       4u
+
+// Scalars that live on the device so a whole step can run without host syncs.
+struct DevState {
+    double loss_sum;     // sum of per-row losses of the last forward
+    float loss;          // loss_sum / n_valid
+    int n_valid;         // targets != -1 in the last forward
+    float inv_count;     // 1 / (n_valid * grad_accum_steps): d loss / d logits scale
+    float grad_norm;     // pre-clip global norm of the last step
+    float clip_coef;     // min(1, clip / (norm + 1e-6))
+    int skip;            // 1 if the last step was skipped (non-finite norm)
+    int step_t;          // AdamW step counter t
+    float bc1, bc2;      // 1 - beta1^t, 1 - beta2^t for the current step
+    unsigned int err;    // ERR_* bits, sticky until read by the host
+    unsigned int timeout_site;
+};
+
+// A GEMM operand: element (row r, reduction index k) of the logical [R, K]
+// matrix sits at ptr[r*ld + k] when kmajor, else at ptr[k*ld + r].
+struct GemmOperand {
+    const void* ptr;
+    int64_t ld;
+    bool kmajor;
+};
+
+// GEMM epilogues. D[m,n] = acc[m,n] = sum_k A(m,k) B(n,k).
+enum EpiKind : int {
+    EPI_STORE_ACT = 0,   // out_act[m,n]  = acc + bias[n]
+    EPI_GELU = 1,        // out_act[m,n]  = pre = acc + bias[n]; out2_act[m,n] = gelu(pre)
+    EPI_RESID = 2,       // out_f32[m,n]  = resid_f32[m,n] + acc + bias[n]
+    EPI_GELU_BWD = 3,    // out_act[m,n]  = acc * gelu'(pre_act[m,n])
+    EPI_ACCUM_F32 = 4,   // out_f32[m,n] += acc
+    EPI_STORE_F32 = 5,   // out_f32[m,n]  = acc + bias[n]
+};
+
+struct GemmEpi {
+    int kind;
+    const float* bias;     // [N] or nullptr
+    void* out;             // act or f32 per kind
+    int64_t ldo;
+    void* out2;            // EPI_GELU post-activation output (act)
+    int64_t ldo2;
+    const void* aux;       // EPI_RESID: f32 residual input; EPI_GELU_BWD: act pre-activation
+    int64_t ld_aux;
+};
+
+#define CUDA_OK(expr) do { cudaError_t e__ = (expr); if (e__ != cudaSuccess) return e__; } while (0)
+
+// tanh-form GELU (Hendrycks & Gimpel) and its derivative, fp32.
+__device__ __forceinline__ float gelu_f(float x) {
+    const float a = 0.7978845608028654f, c = 0.044715f;
+    float t = tanhf(a * (x + c * x * x * x));
+    return 0.5f * x * (1.0f + t);
+}
+__device__ __forceinline__ float gelu_grad_f(float x) {
+    const float a = 0.7978845608028654f, c = 0.044715f;
+    float t = tanhf(a * (x + c * x * x * x));
+    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * a * (1.0f + 3.0f * c * x * x);
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Nanoseconds since an arbitrary epoch (for bounded waits).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded device-side waits give up after this long and report ERR_TIMEOUT.
+#define WAIT_LIMIT_NS 2000000000ull
+
+// ------------------------------------------------------------------ launchers
+// All launchers return cudaSuccess or the launch error; `st` may be null.
+namespace k {
+
+cudaError_t validate_inputs(const int32_t* tok, const int32_t* tgt, int M, int V, DevState* st,
+                            int accum, cudaStream_t s);
+cudaError_t embed_fwd(const int32_t* tok, const float* wte, const float* wpe, float* x, int M,
+                      int T, int C, int V, cudaStream_t s);
+// dwte[tok[m]] += dx[m]; dwpe[t] += sum_b dx[b*T+t]; deterministic.
+size_t embed_bwd_workspace(int M, int C);
+cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
+                      int C, int V, void* workspace, cudaStream_t s);
+
+template <typename Act>
+cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u, float* mu,
+                          float* rstd, int M, int C, cudaStream_t s);
+// dres (+)= LN backward of du; dres_act = Act copy of the new dres;
+// dg, db += parameter gradients (two-stage, fixed order).
+template <typename Act>
+cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const float* mu,
+                          const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
+                          float* db, int M, int C, float* partial, cudaStream_t s);
+size_t layernorm_bwd_partial_floats(int M, int C);
+
+// db[n] += sum_m dy[m, n]; fixed-order two-stage reduction.
+template <typename T>
+cudaError_t colsum_add(const T* dy, int64_t ld, int M, int N, float* db, float* partial,
+                       cudaStream_t s);
+size_t colsum_partial_floats(int M, int N);
+
+template <typename Act>
+cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int M, int V, int Vp,
+                          const DevState* st, cudaStream_t s);
+cudaError_t loss_reduce(const float* row_loss, int M, DevState* st, cudaStream_t s);
+
+cudaError_t grad_norm(const float* g, int64_t n, double* partial, int nparts, cudaStream_t s);
+cudaError_t step_finalize(const double* partial, int nparts, float clip, float beta1, float beta2,
+                          DevState* st, cudaStream_t s);
+cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* p_bf16, int64_t n,
+                  int64_t decay_end, int64_t bf16_end, float lr, float beta1, float beta2, float eps,
+                  float wd, const DevState* st, cudaStream_t s);
+cudaError_t f32_to_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s);
+cudaError_t splitk_reduce_add(const float* partial, int splits, int64_t n, float* out,
+                              cudaStream_t s);
+
+// attention on a fused qkv [B*T, 3C]
+cudaError_t attention_fwd_f32(const float* qkv, float* out, float* lse, int B, int T, int H, int hs,
+                              cudaStream_t s);
+cudaError_t attention_bwd_f32(const float* qkv, const float* out, const float* lse,
+                              const float* dout, float* dqkv, float* Dbuf, int B, int T, int H,
+                              int hs, cudaStream_t s);
+cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
+                               cudaStream_t s);
+cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* lse,
+                               const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,
+                               int hs, cudaStream_t s);
+bool attention_bf16_supported(int T, int hs);
+
+// GEMMs
+cudaError_t gemm_f32(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                     cudaStream_t s);
+// tcgen05 GEMM; splits > 1 writes fp32 partials [splits][M][N] to epi.out
+// (kind EPI_STORE_F32, no bias) for a later splitk_reduce_add.
+cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                         int splits, DevState* st, cudaStream_t s);
+bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi);
+
+int num_sms();
+
+}  // namespace k

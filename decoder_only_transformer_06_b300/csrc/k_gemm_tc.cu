@@ -1,0 +1,565 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   D[m,n] = sum_k A(m,k) B(n,k), fp32 accumulation in tensor memory (TMEM),
+//   followed by a fused epilogue (bias, tanh-GELU, residual add, GELU
+//   backward, fp32 gradient accumulation).
+//
+// Every Linear of the step maps onto this one routine (PyTorch layout
+// W[out,in], nanoGPT guide Deep dive 1):
+//   forward   y  = x W^T  : A = x  (K-major),  B = W (K-major)
+//   backward  dx = dy W   : A = dy (K-major),  B = W viewed [in, out] (MN-major)
+//   backward  dW += dy^T x: A = dy^T (MN-major), B = x^T (MN-major)
+// so operands are consumed in either major order straight from memory.
+//
+// Structure: persistent CTAs (one per SM), 192 threads.
+//   warp 0      TMA producer: 128B-swizzled tiles into a STAGES-deep ring
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
+//               and tcgen05.commit to free ring slots / publish accumulators
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, fused math, stores
+// Two TMEM accumulators (2*BN columns) let the epilogue of one tile overlap
+// the main loop of the next. Every mbarrier wait is bounded: on expiry the
+// CTA records ERR_TIMEOUT in the device status word, drains its in-flight
+// copies and MMAs (again bounded), frees TMEM and returns.
+#include "common.cuh"
+#include <cuda.h>
+
+namespace k {
+
+static constexpr int TC_BM = 128, TC_BK = 64;
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity. Returns false when the
+// CTA is aborting (another role timed out) or when this wait timed out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 "shared memory descriptor"):
+// start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
+// byte offset >> 4 in 32-45, descriptor version 1 in 46-47, base offset 0,
+// swizzle mode 2 (128-byte) in 61-63.
+//   K-major, 128B swizzle: rows of 64 bf16 (128 B), 8-row atoms 1024 B apart
+//     (SBO); LBO unused. Advancing K by 16 elements adds 32 B to the start.
+//   MN-major, 128B swizzle: each k row holds 64 MN elements (128 B); 8-row
+//     k groups are 1024 B apart (SBO) and 64-wide MN chunks are one TMA box
+//     (64 rows * 128 B = 8192 B) apart (LBO). Advancing K by 16 adds 2048 B.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bit 4), A and B bf16 (bits 7,
+// 10), A/B major in bits 15/16 (1 = MN-major), N>>3 in bits 17-22, M>>4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Grouped tile order: 16 m-tiles per group, m fastest inside a group, so a
+// wave of CTAs shares A and B tiles through L2.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mt, int& nt) {
+    const int G = 16;
+    int group = t / (G * num_n);
+    int first = group * G;
+    int gm = min(num_m - first, G);
+    int r = t - group * G * num_n;
+    mt = first + r % gm;
+    nt = r / gm;
+}
+
+// ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *(uint32_t*)&h;
+}
+
+__device__ __forceinline__ void store_bf16_32(bf16* dst, const float* v) {
+    uint4* d = (uint4*)dst;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        d[q] = w;
+    }
+}
+
+// Apply the epilogue to 32 consecutive columns n0..n0+31 of row m.
+__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, int64_t m, int n0, int N, float* v,
+                                               int64_t split_off) {
+    const bool full = (n0 + 32 <= N);
+    if (e.bias && e.kind != EPI_ACCUM_F32 && e.kind != EPI_GELU_BWD) {
+        if (full) {
+            const float4* b4 = (const float4*)(e.bias + n0);
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                float4 b = __ldg(b4 + q);
+                v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
+            }
+        } else {
+            for (int j = 0; j < 32 && n0 + j < N; j++) v[j] += e.bias[n0 + j];
+        }
+    }
+    switch (e.kind) {
+        case EPI_STORE_ACT: {
+            bf16* o = (bf16*)e.out + m * e.ldo + n0;
+            if (full) store_bf16_32(o, v);
+            else for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = __float2bfloat16_rn(v[j]);
+            break;
+        }
+        case EPI_GELU: {
+            bf16* o = (bf16*)e.out + m * e.ldo + n0;
+            bf16* o2 = (bf16*)e.out2 + m * e.ldo2 + n0;
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) g[j] = gelu_f(v[j]);
+            if (full) {
+                store_bf16_32(o, v);
+                store_bf16_32(o2, g);
+            } else {
+                for (int j = 0; j < 32 && n0 + j < N; j++) {
+                    o[j] = __float2bfloat16_rn(v[j]);
+                    o2[j] = __float2bfloat16_rn(g[j]);
+                }
+            }
+            break;
+        }
+        case EPI_RESID: {
+            float* o = (float*)e.out + m * e.ldo + n0;
+            const float* r = (const float*)e.aux + m * e.ld_aux + n0;
+            if (full) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float4 a = ((const float4*)r)[q];
+                    ((float4*)o)[q] = make_float4(a.x + v[4 * q], a.y + v[4 * q + 1],
+                                                  a.z + v[4 * q + 2], a.w + v[4 * q + 3]);
+                }
+            } else {
+                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = r[j] + v[j];
+            }
+            break;
+        }
+        case EPI_GELU_BWD: {
+            bf16* o = (bf16*)e.out + m * e.ldo + n0;
+            const bf16* p = (const bf16*)e.aux + m * e.ld_aux + n0;
+            if (full) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    uint4 w = ((const uint4*)p)[q];
+                    const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+#pragma unroll
+                    for (int t = 0; t < 4; t++) {
+                        float2 f = __bfloat1622float2(h[t]);
+                        v[8 * q + 2 * t] *= gelu_grad_f(f.x);
+                        v[8 * q + 2 * t + 1] *= gelu_grad_f(f.y);
+                    }
+                }
+                store_bf16_32(o, v);
+            } else {
+                for (int j = 0; j < 32 && n0 + j < N; j++)
+                    o[j] = __float2bfloat16_rn(v[j] * gelu_grad_f(__bfloat162float(p[j])));
+            }
+            break;
+        }
+        case EPI_ACCUM_F32: {
+            float* o = (float*)e.out + m * e.ldo + n0;
+            if (full) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float4 a = ((float4*)o)[q];
+                    ((float4*)o)[q] = make_float4(a.x + v[4 * q], a.y + v[4 * q + 1],
+                                                  a.z + v[4 * q + 2], a.w + v[4 * q + 3]);
+                }
+            } else {
+                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] += v[j];
+            }
+            break;
+        }
+        case EPI_STORE_F32: {
+            float* o = (float*)e.out + split_off + m * e.ldo + n0;
+            if (full) {
+#pragma unroll
+                for (int q = 0; q < 8; q++)
+                    ((float4*)o)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = v[j];
+            }
+            break;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN, bool A_MN, bool B_MN>
+struct TcCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int A_BYTES = TC_BM * TC_BK * 2;
+    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(192, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               int M, int N, int K, int splits, GemmEpi epi, DevState* st) {
+    using Cfg = TcCfg<BN, A_MN, B_MN>;
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
+    uint64_t* full = (uint64_t*)(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_m = (M + TC_BM - 1) / TC_BM;
+    const int num_n = (N + BN - 1) / BN;
+    const int tiles = num_m * num_n;
+    const int kblocks = (K + TC_BK - 1) / TC_BK;
+    const int kpb = (kblocks + splits - 1) / splits;
+    const int total = tiles * splits;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                int split = w / tiles, mt, nt;
+                tile_coords(w - split * tiles, num_m, num_n, mt, nt);
+                int kb0 = split * kpb, kb1 = min(kb0 + kpb, kblocks);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    uint8_t* a = sA + stage * Cfg::A_BYTES;
+                    uint8_t* b = sB + stage * Cfg::B_BYTES;
+                    const int k0 = kb * TC_BK;
+                    if (!A_MN) {
+                        tma_load_2d(a, &tmA, &full[stage], k0, mt * TC_BM);
+                    } else {
+                        tma_load_2d(a, &tmA, &full[stage], mt * TC_BM, k0);
+                        tma_load_2d(a + 8192, &tmA, &full[stage], mt * TC_BM + 64, k0);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(b, &tmB, &full[stage], k0, nt * BN);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; j++)
+                            tma_load_2d(b + j * 8192, &tmB, &full[stage], nt * BN + 64 * j, k0);
+                    }
+                    issued++;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok || *abort_flag) {
+                // drain: wait (bounded, ignoring the abort flag) for our last copies
+                long first = issued > STAGES ? issued - STAGES : 0;
+                for (long i = first; i < issued; i++) {
+                    int s = (int)(i % STAGES);
+                    uint32_t par = (uint32_t)((i / STAGES) & 1);
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(&full[s], par) && global_ns() - t0 < WAIT_LIMIT_NS) {}
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = make_idesc(TC_BM, BN, A_MN, B_MN);
+            constexpr uint32_t A_LBO = A_MN ? 8192 : 16, B_LBO = B_MN ? 8192 : 16;
+            constexpr uint32_t KSTEP_A = A_MN ? 2048 : 32, KSTEP_B = B_MN ? 2048 : 32;
+            const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            bool any = false;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                int split = w / tiles;
+                int kb0 = split * kpb, kb1 = min(kb0 + kpb, kblocks);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = sA0 + stage * Cfg::A_BYTES;
+                    const uint32_t b_addr = sB0 + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / 16; kk++) {
+                        uint64_t ad = smem_desc(a_addr + kk * KSTEP_A, A_LBO, 1024);
+                        uint64_t bd = smem_desc(b_addr + kk * KSTEP_B, B_LBO, 1024);
+                        mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    any = true;
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            if (any) {
+                // all MMAs of this CTA complete before TMEM is released
+                mma_commit(drain);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(drain, 0) && global_ns() - t0 < WAIT_LIMIT_NS) {}
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5: TMEM lanes 32*(warp%4) ...
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            int split = w / tiles, mt, nt;
+            tile_coords(w - split * tiles, num_m, num_n, mt, nt);
+            bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int64_t m = (int64_t)mt * TC_BM + row_in_tile;
+            const int64_t split_off = (int64_t)split * M * N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                const int n0 = nt * BN + c * 32;
+                if (m < M && n0 < N) epilogue_chunk(epi, m, n0, N, (float*)r, split_off);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        atomicOr(&st->err, ERR_TIMEOUT);
+        st->timeout_site = 1;
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per line, `outer` lines
+// `ld` elements apart; boxes of box_inner x box_outer with 128B swizzle.
+static bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, int64_t ld,
+                     uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi) {
+    if (M <= 0 || N <= 0 || K <= 0) return false;
+    if ((A.ld % 8) || (B.ld % 8)) return false;
+    if (((uintptr_t)A.ptr | (uintptr_t)B.ptr) & 15) return false;
+    if (epi.ldo % 8) return false;
+    if (!get_encode()) return false;
+    return true;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                             int splits, DevState* st, cudaStream_t s) {
+    using Cfg = TcCfg<BN, A_MN, B_MN>;
+    CUtensorMap ta, tb;
+    bool ok = A_MN ? make_map(&ta, A.ptr, (uint64_t)M, (uint64_t)K, A.ld, 64, 64)
+                   : make_map(&ta, A.ptr, (uint64_t)K, (uint64_t)M, A.ld, 64, TC_BM);
+    ok = ok && (B_MN ? make_map(&tb, B.ptr, (uint64_t)N, (uint64_t)K, B.ld, 64, 64)
+                     : make_map(&tb, B.ptr, (uint64_t)K, (uint64_t)N, B.ld, 64, BN));
+    if (!ok) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        CUDA_OK(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM));
+        attr_set = true;
+    }
+    const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN);
+    const int total = tiles * splits;
+    const int grid = total < num_sms() ? total : num_sms();
+    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, M, N, K, splits, epi, st);
+    return cudaGetLastError();
+}
+
+cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                         int splits, DevState* st, cudaStream_t s) {
+    if (!gemm_bf16_tc_supported(M, N, K, A, B, epi)) return cudaErrorInvalidValue;
+    const int kblocks = (K + TC_BK - 1) / TC_BK;
+    if (splits < 1) splits = 1;
+    if (splits > kblocks) splits = kblocks;
+    if (splits > 1) {
+        // every split must own at least one k-block
+        int kpb = (kblocks + splits - 1) / splits;
+        splits = (kblocks + kpb - 1) / kpb;
+        if (epi.kind != EPI_STORE_F32 || epi.bias) return cudaErrorInvalidValue;
+        if (epi.ldo != N) return cudaErrorInvalidValue;
+    }
+    const bool a_mn = !A.kmajor, b_mn = !B.kmajor;
+    const bool wide = (N % 256 == 0) || N > 2048;
+#define TC_CASE(BNV, AM, BM_)                                                   \
+    if (a_mn == AM && b_mn == BM_)                                              \
+        return launch_tc<BNV, AM, BM_>(M, N, K, A, B, epi, splits, st, s);
+    if (wide) {
+        TC_CASE(256, false, false)
+        TC_CASE(256, false, true)
+        TC_CASE(256, true, false)
+        TC_CASE(256, true, true)
+    } else {
+        TC_CASE(128, false, false)
+        TC_CASE(128, false, true)
+        TC_CASE(128, true, false)
+        TC_CASE(128, true, true)
+    }
+#undef TC_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace k

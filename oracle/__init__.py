@@ -12,7 +12,7 @@ see tests/test_oracle_pins.py. Every function here is pinned; none is marked
 """
 from .gpt2_oracle import (  # noqa: F401
     Config, Trainer, adamw_update, attention_bwd, attention_fwd, backward,
-    causal_softmax, clip_grads, decays, forward, gelu_tanh, gelu_tanh_grad,
+    causal_lse, causal_softmax, clip_grads, decays, forward, gelu_tanh, gelu_tanh_grad,
     global_grad_norm, init_normals, init_params, layernorm_bwd, layernorm_fwd,
     lr_schedule, num_params, param_shapes, zero_grads,
 )

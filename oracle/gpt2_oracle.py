@@ -220,6 +220,18 @@ def causal_softmax(q, k):
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def causal_lse(q, k):
+    """Natural-log normaliser of each causal softmax row,
+    lse_i = log sum_{j<=i} exp(q_i . k_j / sqrt(hs)); flash-style kernels keep
+    it from the forward to rebuild P in the backward."""
+    T, hs = q.shape[-2], q.shape[-1]
+    s = (q @ np.swapaxes(k, -1, -2)) / math.sqrt(hs)
+    future = np.triu(np.ones((T, T), dtype=bool), k=1)
+    s = np.where(future, -np.inf, s)
+    mx = s.max(axis=-1, keepdims=True)
+    return (mx + np.log(np.exp(s - mx).sum(axis=-1, keepdims=True)))[..., 0]
+
+
 def attention_fwd(q, k, v):
     """o = P v for P = causal_softmax(q, k). Shapes [B, H, T, hs]."""
     return causal_softmax(q, k) @ v

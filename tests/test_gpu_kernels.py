@@ -1,0 +1,119 @@
+"""Op-level parity: each tensor-core / attention kernel against the oracle's
+definition (fp64 on the same bf16-rounded inputs), through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from decoder_only_transformer_06_b300 import gpt2
+from oracle import gpt2_oracle as O
+
+from gpu_helpers import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemm_case(M, N, K, ak, bk, seed):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(M, K, generator=g).bfloat16()
+    B = torch.randn(N, K, generator=g).bfloat16()
+    a_mem = A if ak else A.t().contiguous()
+    b_mem = B if bk else B.t().contiguous()
+    lda = K if ak else M
+    ldb = K if bk else N
+    ref = A.double().numpy() @ B.double().numpy().T
+    return a_mem.cuda(), lda, b_mem.cuda(), ldb, ref
+
+
+SHAPES = [(128, 128, 64), (256, 512, 128), (384, 768, 768), (200, 96, 80), (136, 264, 200),
+          (128, 2304, 64), (1024, 3072, 192), (256, 50304, 64)]
+
+
+@pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 1), (0, 0)])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_bf16_fp32_out(M, N, K, ak, bk):
+    a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, M * 7 + N * 3 + K + 10 * ak + bk)
+    out = torch.full((M, N), float("nan"), device="cuda")
+    gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, out_f32=out)
+    torch.cuda.synchronize()
+    got = out.cpu().double().numpy()
+    # fp32 accumulation of exact bf16 products: error ~ sqrt(K) * 2^-24 * |terms|
+    assert np.abs(got - ref).max() <= 1e-4 * math.sqrt(K) * 4, (M, N, K, ak, bk)
+
+
+@pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 0)])
+def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk):
+    M, N, K = 320, 384, 256
+    a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, 5)
+    bias = torch.randn(N).cuda()
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, bias=bias, out_bf16=out)
+    acc = torch.ones(M, N, device="cuda")
+    gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, out_f32=acc, accumulate=True)
+    torch.cuda.synchronize()
+    r = ref + bias.cpu().double().numpy()[None, :]
+    got = out.cpu().double().numpy()
+    assert np.all(np.abs(got - r) <= 2 ** -8 * np.abs(r) + 1e-3 * math.sqrt(K))
+    assert np.abs(acc.cpu().double().numpy() - (ref + 1.0)).max() <= 4e-4 * math.sqrt(K)
+
+
+def _attn_inputs(B, T, H, hs, seed, dtype):
+    g = torch.Generator().manual_seed(seed)
+    qkv = torch.randn(B * T, 3 * H * hs, generator=g)
+    dout = torch.randn(B * T, H * hs, generator=g)
+    if dtype == torch.bfloat16:
+        qkv, dout = qkv.bfloat16(), dout.bfloat16()
+    return qkv, dout
+
+
+def _oracle_attn(qkv, dout, B, T, H, hs):
+    C = H * hs
+    x = qkv.double().numpy().reshape(B, T, 3 * C)
+    f = lambda t: t.reshape(B, T, H, hs).transpose(0, 2, 1, 3)
+    q, k, v = f(x[..., :C]), f(x[..., C:2 * C]), f(x[..., 2 * C:])
+    o = O.attention_fwd(q, k, v)
+    lse = O.causal_lse(q, k)
+    do = f(dout.double().numpy().reshape(B, T, C))
+    dq, dk, dv = O.attention_bwd(do, q, k, v)
+    m = lambda t: t.transpose(0, 2, 1, 3).reshape(B * T, C)
+    return m(o), lse.reshape(B * H * T), np.concatenate([m(dq), m(dk), m(dv)], axis=1)
+
+
+@pytest.mark.parametrize("precision", [gpt2.GPT2_BF16, gpt2.GPT2_FP32])
+@pytest.mark.parametrize("B,T,H", [(2, 256, 2), (1, 200, 3), (3, 64, 1), (2, 1, 2), (1, 1024, 2)])
+def test_attention_fwd_bwd(precision, B, T, H):
+    hs = 64
+    dt = torch.bfloat16 if precision == gpt2.GPT2_BF16 else torch.float32
+    qkv, dout = _attn_inputs(B, T, H, hs, B * 1000 + T + H, dt)
+    o_ref, lse_ref, d_ref = _oracle_attn(qkv, dout, B, T, H, hs)
+    C = H * hs
+    q_d, do_d = qkv.cuda(), dout.cuda()
+    out = torch.empty(B * T, C, dtype=dt, device="cuda")
+    lse = torch.empty(B * H * T, device="cuda")
+    dqkv = torch.empty(B * T, 3 * C, dtype=dt, device="cuda")
+    scratch = torch.empty(B * H * T, device="cuda")
+    gpt2.op_attention_fwd(precision, B, T, H, hs, q_d, out, lse)
+    gpt2.op_attention_bwd(precision, B, T, H, hs, q_d, out, lse, do_d, dqkv, scratch)
+    torch.cuda.synchronize()
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    d = dqkv.float().cpu().double().numpy()
+    if precision == gpt2.GPT2_FP32:
+        assert np.abs(o - o_ref).max() < 1e-5
+        assert np.abs(l - lse_ref).max() < 1e-5
+        assert rel_l2(d, d_ref) < 1e-5
+    else:
+        assert np.abs(o - o_ref).max() < 3e-2
+        assert np.abs(l - lse_ref).max() < 2e-3
+        for part in range(3):
+            sl = slice(part * C, (part + 1) * C)
+            assert rel_l2(d[:, sl], d_ref[:, sl]) < 2e-2, part
+
+
+def test_attention_rejects_unsupported_head_size():
+    qkv = torch.zeros(64, 3 * 96, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(64, 96, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(64, device="cuda")
+    with pytest.raises(gpt2.GPT2Error):
+        gpt2.op_attention_fwd(gpt2.GPT2_BF16, 1, 64, 1, 96, qkv, out, lse)

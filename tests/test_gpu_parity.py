@@ -1,0 +1,264 @@
+"""Model-level parity: the library's forward / backward / step against the
+oracle on the same seeded inputs, through the C ABI.
+
+Tolerances:
+  fp32-math mode: loss and every gradient within 1e-4 relative (per-tensor L2).
+  bf16 mode: loss within 5e-3 relative; per-tensor gradient relative L2 <= 2e-2
+  and cosine >= 0.999; after AdamW, parameters within 1e-3 absolute on every
+  element whose gradient sign agrees with the oracle's (the sign-flip count is
+  reported and must stay a tiny fraction).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synthdata
+from decoder_only_transformer_06_b300 import gpt2
+from oracle import CONFIGS
+from oracle import gpt2_oracle as O
+
+from gpu_helpers import adamw_param_diff, cosine, dev, gpu_cfg, oracle_cfg, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare_step(ocfg, precision, kind, seed=1337, data_seed=42, lr=1e-3, ignore=None):
+    m = gpt2.GPT2(gpu_cfg(ocfg, precision), seed=seed)
+    tr = O.Trainer(ocfg, seed)
+    # independent inits agree (bit-exact up to a rare fp32 ulp, see test_abi)
+    for name in m.names:
+        assert np.allclose(m.get(name), tr.params[name], rtol=2 ** -23, atol=0), name
+    x, y = synthdata.batch_for(kind, ocfg.vocab_size, ocfg.batch_size, ocfg.seq_len, data_seed)
+    if ignore is not None:
+        y = y.copy()
+        y[ignore] = -1
+    loss = m.forward(dev(x), dev(y))
+    lo, _ = tr.forward(x, y)
+    m.backward()
+    tr.backward()
+    g_gpu = m.state(gpt2.GPT2_GRAD)
+    norm = m.step(lr=lr)
+    p_gpu = m.state(gpt2.GPT2_PARAM)
+    g_orc = {n: a.copy() for n, a in tr.grads.items()}
+    tn = tr.step(lr=lr)
+    out = dict(loss=(loss, lo), norm=(norm, tn), g_gpu=g_gpu, g_orc=g_orc, p_gpu=p_gpu,
+               p_orc=tr.params, m=m, tr=tr, V=ocfg.vocab_size)
+    return out
+
+
+def _check_fp32(r):
+    loss, lo = r["loss"]
+    assert abs(loss - lo) / abs(lo) < 1e-4
+    for n, g in r["g_orc"].items():
+        e = rel_l2(r["g_gpu"][n], g)
+        assert e < 1e-4, (n, e)
+    assert abs(r["norm"][0] - r["norm"][1]) / r["norm"][1] < 1e-4
+    for n in r["p_orc"]:
+        d, flips = adamw_param_diff(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n], r["g_orc"][n])
+        assert d < 1e-6, (n, d)
+        assert flips <= max(2, r["p_orc"][n].size // 10000), (n, flips)
+
+
+def _check_bf16(r):
+    loss, lo = r["loss"]
+    assert abs(loss - lo) / abs(lo) < 5e-3, (loss, lo)
+    for n, g in r["g_orc"].items():
+        if not np.any(g):
+            assert not np.any(r["g_gpu"][n]), n
+            continue
+        e, c = rel_l2(r["g_gpu"][n], g), cosine(r["g_gpu"][n], g)
+        assert e <= 2e-2 and c >= 0.999, (n, e, c)
+    assert abs(r["norm"][0] - r["norm"][1]) / r["norm"][1] < 2e-2
+    total_flips = 0
+    for n in r["p_orc"]:
+        d, flips = adamw_param_diff(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n], r["g_orc"][n])
+        assert d <= 1e-3, (n, d)
+        total_flips += flips
+    total = sum(a.size for a in r["p_orc"].values())
+    assert total_flips <= 0.01 * total, total_flips
+
+
+def _pad_rows_zero(r):
+    V = r["V"]
+    assert np.all(r["g_gpu"]["wte"][V:] == 0.0)
+    assert np.all(r["g_orc"]["wte"][V:] == 0.0)
+
+
+def test_tiny_fp32_one_full_step():
+    """Tiny GPT (2 layers, 4 heads, d=64, V=65, T=64, B=4), fp32-math mode."""
+    r = _compare_step(CONFIGS["tiny"], gpt2.GPT2_FP32, "uniform")
+    _check_fp32(r)
+    _pad_rows_zero(r)
+
+
+def test_tiny_fp32_ignore_index():
+    r = _compare_step(CONFIGS["tiny"], gpt2.GPT2_FP32, "uniform",
+                      ignore=(np.array([0, 1, 3, 3]), np.array([5, 63, 0, 1])))
+    _check_fp32(r)
+
+
+def test_char_bf16_one_step_reduced_batch():
+    """Character model (6 layers, d=384, T=256) at B=8, bf16 mode."""
+    r = _compare_step(oracle_cfg(CONFIGS["char"], batch_size=8), gpt2.GPT2_BF16, "markov")
+    _check_bf16(r)
+    _pad_rows_zero(r)
+
+
+def test_char_fp32_one_step_reduced_batch():
+    r = _compare_step(oracle_cfg(CONFIGS["char"], batch_size=4), gpt2.GPT2_FP32, "markov")
+    _check_fp32(r)
+
+
+def test_bf16_ragged_sequence_and_small_width():
+    """T not a multiple of the 64-row tiles, d=128 (2 heads of 64), V=65."""
+    c = O.Config(n_layer=2, n_head=2, d_model=128, vocab_size=65, block_size=100, batch_size=3,
+                 seq_len=100)
+    r = _compare_step(c, gpt2.GPT2_BF16, "uniform",
+                      ignore=(np.array([0, 2]), np.array([99, 17])))
+    _check_bf16(r)
+
+
+def test_bf16_single_token_sequences():
+    c = O.Config(n_layer=1, n_head=1, d_model=64, vocab_size=65, block_size=8, batch_size=5,
+                 seq_len=1)
+    r = _compare_step(c, gpt2.GPT2_BF16, "uniform")
+    _check_bf16(r)
+
+
+@pytest.mark.slow
+def test_gpt2_124m_bf16_one_step_batch2():
+    """GPT-2 124M at B=2, T=1024 (the full-width model; oracle in fp64)."""
+    r = _compare_step(oracle_cfg(CONFIGS["gpt2_124m"], batch_size=2), gpt2.GPT2_BF16, "zipf",
+                      lr=6e-4)
+    _check_bf16(r)
+    _pad_rows_zero(r)
+
+
+def test_char_bf16_loss_trajectory():
+    """Several AdamW steps at lr 1e-3 on fresh batches: the loss curve tracks
+    the oracle's."""
+    c = oracle_cfg(CONFIGS["char"], batch_size=4, n_layer=2)
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_BF16), seed=3)
+    tr = O.Trainer(c, 3)
+    for step in range(6):
+        x, y = synthdata.markov_batch(65, c.batch_size, c.seq_len, 100 + step)
+        m.zero_grad()
+        tr.zero_grad()
+        loss = m.forward(dev(x), dev(y))
+        lo, _ = tr.forward(x, y)
+        assert abs(loss - lo) / lo < 5e-3 * (1 + step), (step, loss, lo)
+        m.backward()
+        tr.backward()
+        m.step(lr=1e-3)
+        tr.step(lr=1e-3)
+
+
+def test_grad_accumulation_matches_one_big_batch():
+    base = CONFIGS["tiny"]
+    x, y = synthdata.uniform_batch(65, 8, base.seq_len, 9)
+    big = gpt2.GPT2(gpu_cfg(oracle_cfg(base, batch_size=8), gpt2.GPT2_FP32), seed=5)
+    big.forward(dev(x), dev(y))
+    big.backward()
+    acc = gpt2.GPT2(gpu_cfg(oracle_cfg(base, batch_size=2, grad_accum_steps=4), gpt2.GPT2_FP32),
+                    seed=5)
+    for i in range(4):
+        acc.forward(dev(x[2 * i:2 * i + 2]), dev(y[2 * i:2 * i + 2]))
+        acc.backward()
+    gb, ga = big.state(gpt2.GPT2_GRAD), acc.state(gpt2.GPT2_GRAD)
+    for n in gb:
+        assert rel_l2(ga[n], gb[n]) < 1e-5, n
+
+
+def test_runs_are_bit_reproducible():
+    c = oracle_cfg(CONFIGS["char"], batch_size=4, n_layer=2)
+    x, y = synthdata.markov_batch(65, c.batch_size, c.seq_len, 1)
+    outs = []
+    for _ in range(2):
+        m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_BF16), seed=1)
+        loss = m.forward(dev(x), dev(y))
+        m.backward()
+        outs.append((loss, m.state(gpt2.GPT2_GRAD)))
+        m.close()
+    assert outs[0][0] == outs[1][0]
+    for n in outs[0][1]:
+        assert np.array_equal(outs[0][1][n], outs[1][1][n]), n
+
+
+def test_errors_are_reported_and_recoverable():
+    c = CONFIGS["tiny"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=1)
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.backward()
+    assert e.value.code == gpt2.GPT2_ESTATE
+    x, y = synthdata.uniform_batch(65, c.batch_size, c.seq_len, 2)
+    bad = x.copy()
+    bad[0, 3] = 70000
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.forward(dev(bad), dev(y))
+    assert e.value.code == gpt2.GPT2_ERANGE
+    bady = y.copy()
+    bady[1, 1] = -5
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.forward(dev(x), dev(bady))
+    assert e.value.code == gpt2.GPT2_ERANGE
+    loss = m.forward(dev(x), dev(y))          # the model stays usable
+    assert math.isfinite(loss)
+    m.backward()
+    m.step(lr=1e-3)
+
+
+def test_nonfinite_gradient_skips_the_update():
+    c = CONFIGS["tiny"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=1)
+    x, y = synthdata.uniform_batch(65, c.batch_size, c.seq_len, 2)
+    m.forward(dev(x), dev(y))
+    m.backward()
+    g = m.get("lnf.b", gpt2.GPT2_GRAD)
+    g[0] = np.nan
+    m.set("lnf.b", g, gpt2.GPT2_GRAD)
+    before = m.state()
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.step(lr=1e-3)
+    assert e.value.code == gpt2.GPT2_ENONFINITE
+    after = m.state()
+    for n in before:
+        assert np.array_equal(before[n], after[n], equal_nan=True), n
+    m.zero_grad()
+    m.forward(dev(x), dev(y))
+    m.backward()
+    assert math.isfinite(m.step(lr=1e-3))
+
+
+def test_num_params_matches_pages_through_the_library():
+    m = gpt2.GPT2(gpu_cfg(CONFIGS["gpt2_124m"], gpt2.GPT2_BF16, batch_size=1, seq_len=64), seed=1)
+    assert m.num_params(include_wpe=False) == 123_653_376
+    assert m.num_params() == 124_439_808
+    assert m.num_params(padded=True) == 124_475_904
+
+
+@pytest.mark.slow
+def test_gpt2_124m_full_size_sampled_rows():
+    """The benchmark's workload (B=16, T=1024, bf16): per-row losses of two
+    sampled sequences against the oracle run on those sequences alone, the
+    mean loss against the sampled mean, and a finite clipped step."""
+    c = CONFIGS["gpt2_124m"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_BF16), seed=1337)
+    x, y = synthdata.zipf_batch(c.vocab_size, c.batch_size, c.seq_len, 1337)
+    loss = m.forward(dev(x), dev(y))
+    rows = m.row_losses().reshape(c.batch_size, c.seq_len)
+    params = O.init_params(c, 1337)
+    one = oracle_cfg(c, batch_size=1)
+    for b in (0, 11):
+        lo, _, cache = O.forward(params, one, x[b:b + 1], y[b:b + 1])
+        ref_rows = cache["row_loss"][0]
+        assert np.abs(rows[b] - ref_rows).max() < 0.05
+        assert abs(rows[b].mean() - lo) / lo < 5e-3
+    assert abs(loss - rows.mean()) < 1e-4
+    assert abs(loss - (math.log(50257) + 0.0002 * 768)) < 0.15
+    m.backward()
+    norm = m.step(lr=6e-4)
+    assert math.isfinite(norm) and norm > 0
+    loss2 = m.forward(dev(x), dev(y))
+    assert loss2 < loss

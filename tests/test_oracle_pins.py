@@ -200,6 +200,13 @@ def test_attention_closed_forms():
     o = O.attention_fwd(np.zeros((1, 1, T, 4)), k, v)
     prefix_mean = np.cumsum(v, axis=2) / np.arange(1, T + 1)[None, None, :, None]
     assert np.allclose(o, prefix_mean, atol=1e-14)
+    # lse: q = 0 gives log(i + 1); otherwise torch.logsumexp of the masked scores
+    lse0 = O.causal_lse(np.zeros((1, 1, T, 4)), k)
+    assert np.allclose(lse0[0, 0], np.log(np.arange(1, T + 1)), atol=1e-14)
+    qq = rng.normal(size=(1, 1, T, 4))
+    s = torch.tensor(qq[0, 0] @ k[0, 0].T / 2.0)
+    s = s.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), float("-inf"))
+    assert np.allclose(O.causal_lse(qq, k)[0, 0], torch.logsumexp(s, -1).numpy(), atol=1e-13)
     # rows of P sum to one and are zero above the diagonal
     P = O.causal_softmax(rng.normal(size=(1, 1, T, 4)), k)
     assert np.allclose(P.sum(-1), 1.0, atol=1e-14)
