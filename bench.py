@@ -226,6 +226,8 @@ def run_ours(args):
     from decoder_only_transformer_06_b300 import gpt2
 
     L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    if args.batch:
+        B = args.batch
     cfg = gpt2.Config(n_layer=L, n_head=H, d_model=C, vocab_size=V, padded_vocab=Vp,
                       block_size=T, batch_size=B, seq_len=T, precision=gpt2.GPT2_BF16)
     stream = torch.cuda.Stream()
@@ -382,6 +384,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2_124m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (small profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

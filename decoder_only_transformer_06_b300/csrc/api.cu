@@ -351,7 +351,7 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
         for (auto& d : dims) {
             int tiles = ((d[0] + 127) / 128) * ((d[1] + (d[1] % 256 == 0 ? 255 : 127)) /
                                                 (d[1] % 256 == 0 ? 256 : 128));
-            int splits = (k::num_sms() + tiles - 1) / tiles;
+            int splits = k::num_sms() / tiles;
             if (splits > 16) splits = 16;
             if (splits > 1) need = std::max(need, (size_t)splits * d[0] * d[1]);
         }
@@ -470,8 +470,9 @@ struct Op {
             return GPT2_OK;
         }
         const int bn = (k_in % 256 == 0 || k_in > 2048) ? 256 : 128;
+        // one wave: as many K splits as fit the SMs beside the tiles (floor)
         int tiles = ((n_out + 127) / 128) * ((k_in + bn - 1) / bn);
-        int splits = (k::num_sms() + tiles - 1) / tiles;
+        int splits = k::num_sms() / tiles;
         if (splits > 16) splits = 16;
         if (splits > 1 && (size_t)splits * n_out * k_in <= m->splitk_ws_floats) {
             GemmEpi e{EPI_STORE_F32, nullptr, m->splitk_ws, k_in, nullptr, 0, nullptr, 0};
@@ -579,10 +580,12 @@ static int backward_impl(gpt2_model* m) {
         OPR(op.gemm("gemm_lmhead_dx", M, C, Vp, {m->logits, Vp, true}, {m->W(0), C, false}, e));
         OPR(op.gemm_dw("gemm_lmhead_dw", Vp, C, m->logits, Vp, m->uf, C, m->G(0)));
     }
+    // the new dres is the output gradient of the last MLP projection: its
+    // column sums (that projection's bias gradient) come out of the same pass
     RUN(m, "layernorm_bwd", 2, 0, ln_bytes(false),
         k::layernorm_bwd<Act>((const Act*)m->du, m->x_final, m->P(m->lnf_g()), m->muf, m->rsf, m->dres,
-                              (Act*)m->dres_act, false, m->G(m->lnf_g()), m->G(m->lnf_g() + 1), M, C,
-                              m->ln_partial, s));
+                              (Act*)m->dres_act, false, m->G(m->lnf_g()), m->G(m->lnf_g() + 1),
+                              m->G(m->lt(L - 1, T_MPB)), M, C, m->ln_partial, s));
     for (int l = L - 1; l >= 0; l--) {
         LayerActs& a = m->la[l];
         // MLP projection: x_out = x_mid + hgel W_mp^T + b_mp
@@ -591,8 +594,6 @@ static int backward_impl(gpt2_model* m) {
             OPR(op.gemm("gemm_mlpproj_dx", M, 4 * C, C, {m->dres_act, C, true},
                         {m->W(m->lt(l, T_MPW)), 4 * C, false}, e));
             OPR(op.gemm_dw("gemm_mlpproj_dw", C, 4 * C, m->dres_act, C, a.hgel, 4 * C, m->G(m->lt(l, T_MPW))));
-            RUN(m, "bias_colsum", 2, 0, 4.0 * MC,
-                k::colsum_add<float>(m->dres, C, M, C, m->G(m->lt(l, T_MPB)), m->cs_partial, s));
         }
         // fc: hpre = u2 W_fc^T + b_fc
         {
@@ -606,14 +607,13 @@ static int backward_impl(gpt2_model* m) {
         RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
             k::layernorm_bwd<Act>((const Act*)m->du, a.x_mid, m->P(m->lt(l, T_LN2G)), a.mu2, a.rs2,
                                   m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN2G)),
-                                  m->G(m->lt(l, T_LN2B)), M, C, m->ln_partial, s));
+                                  m->G(m->lt(l, T_LN2B)), m->G(m->lt(l, T_APB)), M, C,
+                                  m->ln_partial, s));
         // attention projection: x_mid = x_in + att W_ap^T + b_ap
         {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->datt, C, nullptr, 0, nullptr, 0};
             OPR(op.gemm("gemm_attproj_dx", M, C, C, {m->dres_act, C, true}, {m->W(m->lt(l, T_APW)), C, false}, e));
             OPR(op.gemm_dw("gemm_attproj_dw", C, C, m->dres_act, C, a.att, C, m->G(m->lt(l, T_APW))));
-            RUN(m, "bias_colsum", 2, 0, 4.0 * MC,
-                k::colsum_add<float>(m->dres, C, M, C, m->G(m->lt(l, T_APB)), m->cs_partial, s));
         }
         if (m->use_bf16)
             RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
@@ -635,7 +635,9 @@ static int backward_impl(gpt2_model* m) {
         RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
             k::layernorm_bwd<Act>((const Act*)m->du, a.x_in, m->P(m->lt(l, T_LN1G)), a.mu1, a.rs1,
                                   m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN1G)),
-                                  m->G(m->lt(l, T_LN1B)), M, C, m->ln_partial, s));
+                                  m->G(m->lt(l, T_LN1B)),
+                                  l > 0 ? m->G(m->lt(l - 1, T_MPB)) : nullptr, M, C,
+                                  m->ln_partial, s));
     }
     RUN(m, "embed_bwd", 4, 0, 4.0 * M + 8.0 * MC,
         k::embed_bwd(m->last_tok, m->dres, m->G(0), m->G(1), M, T, C, m->V, m->emb_ws, s));

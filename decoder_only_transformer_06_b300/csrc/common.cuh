@@ -120,11 +120,13 @@ template <typename Act>
 cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u, float* mu,
                           float* rstd, int M, int C, cudaStream_t s);
 // dres (+)= LN backward of du; dres_act = Act copy of the new dres;
-// dg, db += parameter gradients (two-stage, fixed order).
+// dg, db += parameter gradients; dsum (optional) += column sums of the new
+// dres (the bias gradient of the Linear whose output gradient it is). All
+// two-stage, fixed order.
 template <typename Act>
 cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const float* mu,
                           const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
-                          float* db, int M, int C, float* partial, cudaStream_t s);
+                          float* db, float* dsum, int M, int C, float* partial, cudaStream_t s);
 size_t layernorm_bwd_partial_floats(int M, int C);
 
 // db[n] += sum_m dy[m, n]; fixed-order two-stage reduction.
@@ -135,7 +137,7 @@ size_t colsum_partial_floats(int M, int N);
 
 template <typename Act>
 cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int M, int V, int Vp,
-                          const DevState* st, cudaStream_t s);
+                          DevState* st, cudaStream_t s);
 cudaError_t loss_reduce(const float* row_loss, int M, DevState* st, cudaStream_t s);
 
 cudaError_t grad_norm(const float* g, int64_t n, double* partial, int nparts, cudaStream_t s);

@@ -9,6 +9,7 @@
 // place (0 on pad columns and on ignored rows). HBM traffic: one read and one
 // write of the logits. Math in fp32.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace k {
 
@@ -137,11 +138,176 @@ ce_kernel(Act* __restrict__ logits, const int32_t* __restrict__ tgt, float* __re
     if (threadIdx.x == 0) row_loss[row] = ignore ? 0.f : (lse - zy);
 }
 
+
+// ------------------------------------------------------------------ bf16 rows
+// Persistent variant for bf16 logits whose row fits twice in shared memory
+// (Vp <= 55296): one CTA per SM walks rows blockIdx.x, +gridDim.x, ...; row
+// i+1 is fetched by one TMA bulk copy while row i is processed, and the
+// gradient row is written back by one TMA bulk store. Per row:
+//   pass 1  max over j < V (packed bf16x2 max);
+//   pass 2  e_j = exp(z_j - max) in fp32, sum in fp32, e_j kept as bf16 in place;
+//   pass 3  dz_j = (e_j / sum - [j == y]) * scale, 0 on pad columns.
+// Storing e_j in bf16 rounds it once more at the precision the gradient is
+// written in anyway.
+static constexpr int CEB_THREADS = 512;
+
+__device__ __forceinline__ float block_reduce_n(float v, bool is_max, float* sm) {
+    v = is_max ? warp_max(v) : warp_sum(v);
+    const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+    __syncthreads();
+    if (l == 0) sm[w] = v;
+    __syncthreads();
+    float r = sm[0];
+    for (int i = 1; i < CEB_THREADS / 32; i++) r = is_max ? fmaxf(r, sm[i]) : r + sm[i];
+    return r;
+}
+
+__global__ void __launch_bounds__(CEB_THREADS, 1)
+ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
+               float* __restrict__ row_loss, int M, int V, int Vp, DevState* st) {
+    extern __shared__ __align__(128) uint8_t ce_smem[];
+    const uint32_t rowbytes = (uint32_t)Vp * 2;
+    const uint32_t padbytes = (rowbytes + 127) & ~127u;
+    bf16* bufs[2] = {(bf16*)ce_smem, (bf16*)(ce_smem + padbytes)};
+    uint64_t* bar = (uint64_t*)(ce_smem + 2 * padbytes);
+    float* red = (float*)(bar + 2);
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        ptx::mbar_init(&bar[0], 1);
+        ptx::mbar_init(&bar[1], 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && (int)blockIdx.x < M) {
+        ptx::mbar_arrive_expect_tx(&bar[0], rowbytes);
+        ptx::bulk_g2s(bufs[0], logits + (int64_t)blockIdx.x * Vp, rowbytes, &bar[0]);
+    }
+    const int nvec = Vp / 8;          // 16-byte chunks per row
+    const int nfull = V / 8;          // chunks entirely below V
+    const float L2E = 1.4426950408889634f;
+    const float scale_valid = st->inv_count;
+    int i = 0;
+    for (int row = blockIdx.x; row < M; row += gridDim.x, i++) {
+        const int b = i & 1;
+        const uint32_t par = (uint32_t)((i >> 1) & 1);
+        bf16* cur = bufs[b];
+        const int next = row + gridDim.x;
+        if (tid == 0 && next < M) {
+            ptx::bulk_wait_read_all();            // previous store out of bufs[b^1] has read it
+            ptx::mbar_arrive_expect_tx(&bar[b ^ 1], rowbytes);
+            ptx::bulk_g2s(bufs[b ^ 1], logits + (int64_t)next * Vp, rowbytes, &bar[b ^ 1]);
+        }
+        const bool ok = ptx::mbar_wait_bounded(&bar[b], par);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(&st->err, ERR_TIMEOUT);
+                st->timeout_site = 2;
+                // drain (bounded) the prefetch this thread may have issued
+                if (next < M) ptx::mbar_wait_bounded(&bar[b ^ 1], (uint32_t)(((i + 1) >> 1) & 1));
+            }
+            break;
+        }
+        int y = tgt[row];
+        const bool ignore = (y == -1);
+        y = (y < 0 || y >= V) ? 0 : y;
+        const float zy = __bfloat162float(cur[y]);
+        const uint4* cv = (const uint4*)cur;
+        // pass 1: max
+        __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+        for (int vi = tid; vi < nfull; vi += CEB_THREADS) {
+            uint4 w = cv[vi];
+            const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+            mx2 = __hmax2(mx2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
+        }
+        float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+        if (tid == 0) {
+            for (int j = nfull * 8; j < V; j++) mx = fmaxf(mx, __bfloat162float(cur[j]));
+        }
+        mx = block_reduce_n(mx, true, red);
+        const float mxl = mx * L2E;
+        // pass 2: e = exp(z - max), sum; e kept in place as bf16
+        float sum = 0.f;
+        for (int vi = tid; vi < nfull; vi += CEB_THREADS) {
+            uint4 w = cv[vi];
+            const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+            uint4 o;
+            uint32_t* op = (uint32_t*)&o;
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                float2 f = __bfloat1622float2(h[t]);
+                float e0 = ptx::ex2(fmaf(f.x, L2E, -mxl)), e1 = ptx::ex2(fmaf(f.y, L2E, -mxl));
+                sum += e0 + e1;
+                __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
+                op[t] = *(uint32_t*)&p;
+            }
+            ((uint4*)cur)[vi] = o;
+        }
+        if (tid == 0) {
+            for (int j = nfull * 8; j < V; j++) {
+                float e = ptx::ex2(fmaf(__bfloat162float(cur[j]), L2E, -mxl));
+                sum += e;
+                cur[j] = __float2bfloat16_rn(e);
+            }
+        }
+        sum = block_reduce_n(sum, false, red);
+        const float inv = 1.0f / sum;
+        const float scale = ignore ? 0.f : scale_valid;
+        // pass 3: gradient in place
+        for (int vi = tid; vi < nvec; vi += CEB_THREADS) {
+            uint4 o;
+            uint32_t* op = (uint32_t*)&o;
+            if (vi < nfull) {
+                uint4 w = cv[vi];
+                const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    float2 f = __bfloat1622float2(h[t]);
+                    const int j = vi * 8 + 2 * t;
+                    float d0 = (f.x * inv - (j == y ? 1.f : 0.f)) * scale;
+                    float d1 = (f.y * inv - (j + 1 == y ? 1.f : 0.f)) * scale;
+                    __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
+                    op[t] = *(uint32_t*)&p;
+                }
+            } else {
+                const bf16* e = cur + vi * 8;
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    const int j = vi * 8 + 2 * t;
+                    float d0 = j < V ? (__bfloat162float(e[2 * t]) * inv - (j == y ? 1.f : 0.f)) * scale : 0.f;
+                    float d1 = j + 1 < V ? (__bfloat162float(e[2 * t + 1]) * inv - (j + 1 == y ? 1.f : 0.f)) * scale : 0.f;
+                    __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
+                    op[t] = *(uint32_t*)&p;
+                }
+            }
+            ((uint4*)cur)[vi] = o;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::bulk_s2g(logits + (int64_t)row * Vp, cur, rowbytes);
+            ptx::bulk_commit();
+            row_loss[row] = ignore ? 0.f : (mx + logf(sum) - zy);
+        }
+    }
+    if (tid == 0) ptx::bulk_wait_all();
+}
+
 template <typename Act>
 cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int M, int V, int Vp,
-                          const DevState* st, cudaStream_t s) {
+                          DevState* st, cudaStream_t s) {
     constexpr int VEC = Vec16<Act>::N;
     if (Vp % VEC) return cudaErrorInvalidValue;
+    if constexpr (sizeof(Act) == 2) {
+        const size_t pad = ((size_t)Vp * 2 + 127) & ~(size_t)127;
+        const size_t smem = 2 * pad + 16 + CEB_THREADS / 32 * sizeof(float);
+        if (Vp >= 1024 && smem <= 227 * 1024) {
+            CUDA_OK(cudaFuncSetAttribute(ce_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem));
+            int grid = M < num_sms() ? M : num_sms();
+            ce_bulk_kernel<<<grid, CEB_THREADS, smem, s>>>((bf16*)logits, tgt, row_loss, M, V, Vp, st);
+            return cudaGetLastError();
+        }
+    }
     int nch = (Vp / VEC + CE_THREADS - 1) / CE_THREADS;
 #define CE_CASE(NC)                                                                     \
     if (nch <= NC) {                                                                    \
@@ -160,9 +326,9 @@ cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int 
     return cudaErrorInvalidValue;
 }
 
-template cudaError_t cross_entropy<float>(float*, const int32_t*, float*, int, int, int,
-                                          const DevState*, cudaStream_t);
-template cudaError_t cross_entropy<bf16>(bf16*, const int32_t*, float*, int, int, int,
-                                         const DevState*, cudaStream_t);
+template cudaError_t cross_entropy<float>(float*, const int32_t*, float*, int, int, int, DevState*,
+                                          cudaStream_t);
+template cudaError_t cross_entropy<bf16>(bf16*, const int32_t*, float*, int, int, int, DevState*,
+                                         cudaStream_t);
 
 }  // namespace k

@@ -11,11 +11,12 @@
 //   backward  dW += dy^T x: A = dy^T (MN-major), B = x^T (MN-major)
 // so operands are consumed in either major order straight from memory.
 //
-// Structure: persistent CTAs (one per SM), 192 threads.
+// Structure: persistent CTAs (one per SM), 320 threads.
 //   warp 0      TMA producer: 128B-swizzled tiles into a STAGES-deep ring
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
 //               and tcgen05.commit to free ring slots / publish accumulators
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, fused math, stores
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half
+//               the columns: tcgen05.ld 32 at a time, fused math, stores
 // Two TMEM accumulators (2*BN columns) let the epilogue of one tile overlap
 // the main loop of the next. Every mbarrier wait is bounded: on expiry the
 // CTA records ERR_TIMEOUT in the device status word, drains its in-flight
@@ -160,7 +161,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *(uint32_t*)&h;
 }
 
-__device__ __forceinline__ void store_bf16_32(bf16* dst, const float* v) {
+// Hardware tanh (MUFU, max relative error about 2^-11): ample for values that
+// are rounded to bf16 right after.
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float gelu_hw(float x) {
+    const float a = 0.7978845608028654f, c = 0.044715f;
+    return 0.5f * x * (1.0f + tanh_hw(a * (x + c * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_hw(float x) {
+    const float a = 0.7978845608028654f, c = 0.044715f;
+    float t = tanh_hw(a * (x + c * x * x * x));
+    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * a * (1.0f + 3.0f * c * x * x);
+}
+
+__device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32]) {
     uint4* d = (uint4*)dst;
 #pragma unroll
     for (int q = 0; q < 4; q++) {
@@ -173,107 +191,99 @@ __device__ __forceinline__ void store_bf16_32(bf16* dst, const float* v) {
     }
 }
 
-// Apply the epilogue to 32 consecutive columns n0..n0+31 of row m.
-__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, int64_t m, int n0, int N, float* v,
-                                               int64_t split_off) {
-    const bool full = (n0 + 32 <= N);
-    if (e.bias && e.kind != EPI_ACCUM_F32 && e.kind != EPI_GELU_BWD) {
-        if (full) {
-            const float4* b4 = (const float4*)(e.bias + n0);
+// The epilogue works on 32 x 32 chunks per warp (32 TMEM lanes = rows, 32
+// fp32 columns). The chunk is staged through a 4 KB per-warp shared-memory
+// tile (16-byte groups XOR-swizzled by row, conflict-free both ways) so that
+// the fused math and every global load/store run in a coalesced layout: lane
+// l handles columns 4*(l%8)..+3 of rows l/8, l/8+4, ..., i.e. each warp
+// instruction covers 4 rows x 32 columns.
+__device__ __forceinline__ void stage_write(float* st, int lane, const uint32_t (&r)[32]) {
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                float4 b = __ldg(b4 + q);
-                v[4 * q] += b.x; v[4 * q + 1] += b.y; v[4 * q + 2] += b.z; v[4 * q + 3] += b.w;
-            }
-        } else {
-            for (int j = 0; j < 32 && n0 + j < N; j++) v[j] += e.bias[n0 + j];
+    for (int c = 0; c < 8; c++)
+        *(uint4*)&st[lane * 32 + ((c ^ (lane & 7)) << 2)] =
+            make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+}
+__device__ __forceinline__ float4 stage_read(const float* st, int row, int q) {
+    return *(const float4*)&st[row * 32 + ((q ^ (row & 7)) << 2)];
+}
+
+__device__ __forceinline__ uint2 pack4_bf16(float4 v) {
+    return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// Operand the epilogue reads besides the accumulator (residual fp32, GELU
+// pre-activation bf16, or the fp32 gradient it accumulates into): for one
+// chunk, lane l's 8 groups of 4 columns. Loaded one chunk ahead of its use.
+struct AuxBuf {
+    float4 f[8];
+};
+
+__device__ __forceinline__ void aux_load(const GemmEpi& e, int64_t m_base, int M, int n, int N,
+                                         int rsub, AuxBuf& a) {
+    const bool ncol = n < N;
+    if (e.kind == EPI_RESID || e.kind == EPI_ACCUM_F32) {
+        const float* src = (e.kind == EPI_RESID) ? (const float*)e.aux : (const float*)e.out;
+        const int64_t ld = (e.kind == EPI_RESID) ? e.ld_aux : e.ldo;
+#pragma unroll
+        for (int it = 0; it < 8; it++) {
+            const int64_t m = m_base + it * 4 + rsub;
+            a.f[it] = (ncol && m < M) ? *(const float4*)(src + m * ld + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else if (e.kind == EPI_GELU_BWD) {
+        const bf16* src = (const bf16*)e.aux;
+#pragma unroll
+        for (int it = 0; it < 8; it++) {
+            const int64_t m = m_base + it * 4 + rsub;
+            uint2 w = (ncol && m < M) ? *(const uint2*)(src + m * e.ld_aux + n) : make_uint2(0u, 0u);
+            a.f[it] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), 0.f, 0.f);
         }
     }
-    switch (e.kind) {
-        case EPI_STORE_ACT: {
-            bf16* o = (bf16*)e.out + m * e.ldo + n0;
-            if (full) store_bf16_32(o, v);
-            else for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = __float2bfloat16_rn(v[j]);
-            break;
-        }
-        case EPI_GELU: {
-            bf16* o = (bf16*)e.out + m * e.ldo + n0;
-            bf16* o2 = (bf16*)e.out2 + m * e.ldo2 + n0;
-            float g[32];
+}
+
+// Apply the epilogue to one staged chunk: rows m_base..m_base+31, columns
+// n..n+3 for this lane (n = chunk start + 4*(lane%8)); N % 4 == 0.
+__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const float* st, int64_t m_base,
+                                               int M, int n, int N, int rsub, int q,
+                                               const AuxBuf& a, int64_t split_off) {
+    if (n >= N) return;
+    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e.bias && e.kind != EPI_ACCUM_F32 && e.kind != EPI_GELU_BWD) bias = __ldg((const float4*)(e.bias + n));
 #pragma unroll
-            for (int j = 0; j < 32; j++) g[j] = gelu_f(v[j]);
-            if (full) {
-                store_bf16_32(o, v);
-                store_bf16_32(o2, g);
-            } else {
-                for (int j = 0; j < 32 && n0 + j < N; j++) {
-                    o[j] = __float2bfloat16_rn(v[j]);
-                    o2[j] = __float2bfloat16_rn(g[j]);
-                }
+    for (int it = 0; it < 8; it++) {
+        const int row = it * 4 + rsub;
+        const int64_t m = m_base + row;
+        if (m >= M) continue;
+        float4 v = stage_read(st, row, q);
+        v.x += bias.x; v.y += bias.y; v.z += bias.z; v.w += bias.w;
+        switch (e.kind) {
+            case EPI_STORE_ACT:
+                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
+                break;
+            case EPI_GELU: {
+                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
+                float4 g = make_float4(gelu_hw(v.x), gelu_hw(v.y), gelu_hw(v.z), gelu_hw(v.w));
+                *(uint2*)((bf16*)e.out2 + m * e.ldo2 + n) = pack4_bf16(g);
+                break;
             }
-            break;
-        }
-        case EPI_RESID: {
-            float* o = (float*)e.out + m * e.ldo + n0;
-            const float* r = (const float*)e.aux + m * e.ld_aux + n0;
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    float4 a = ((const float4*)r)[q];
-                    ((float4*)o)[q] = make_float4(a.x + v[4 * q], a.y + v[4 * q + 1],
-                                                  a.z + v[4 * q + 2], a.w + v[4 * q + 3]);
-                }
-            } else {
-                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = r[j] + v[j];
+            case EPI_RESID:
+            case EPI_ACCUM_F32: {
+                const float4 r = a.f[it];
+                v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+                *(float4*)((float*)e.out + m * e.ldo + n) = v;
+                break;
             }
-            break;
-        }
-        case EPI_GELU_BWD: {
-            bf16* o = (bf16*)e.out + m * e.ldo + n0;
-            const bf16* p = (const bf16*)e.aux + m * e.ld_aux + n0;
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    uint4 w = ((const uint4*)p)[q];
-                    const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
-#pragma unroll
-                    for (int t = 0; t < 4; t++) {
-                        float2 f = __bfloat1622float2(h[t]);
-                        v[8 * q + 2 * t] *= gelu_grad_f(f.x);
-                        v[8 * q + 2 * t + 1] *= gelu_grad_f(f.y);
-                    }
-                }
-                store_bf16_32(o, v);
-            } else {
-                for (int j = 0; j < 32 && n0 + j < N; j++)
-                    o[j] = __float2bfloat16_rn(v[j] * gelu_grad_f(__bfloat162float(p[j])));
+            case EPI_GELU_BWD: {
+                const uint32_t w0 = __float_as_uint(a.f[it].x), w1 = __float_as_uint(a.f[it].y);
+                float2 p0 = __bfloat1622float2(*(const __nv_bfloat162*)&w0);
+                float2 p1 = __bfloat1622float2(*(const __nv_bfloat162*)&w1);
+                v.x *= gelu_grad_hw(p0.x); v.y *= gelu_grad_hw(p0.y);
+                v.z *= gelu_grad_hw(p1.x); v.w *= gelu_grad_hw(p1.y);
+                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
+                break;
             }
-            break;
-        }
-        case EPI_ACCUM_F32: {
-            float* o = (float*)e.out + m * e.ldo + n0;
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    float4 a = ((float4*)o)[q];
-                    ((float4*)o)[q] = make_float4(a.x + v[4 * q], a.y + v[4 * q + 1],
-                                                  a.z + v[4 * q + 2], a.w + v[4 * q + 3]);
-                }
-            } else {
-                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] += v[j];
-            }
-            break;
-        }
-        case EPI_STORE_F32: {
-            float* o = (float*)e.out + split_off + m * e.ldo + n0;
-            if (full) {
-#pragma unroll
-                for (int q = 0; q < 8; q++)
-                    ((float4*)o)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            } else {
-                for (int j = 0; j < 32 && n0 + j < N; j++) o[j] = v[j];
-            }
-            break;
+            case EPI_STORE_F32:
+                *(float4*)((float*)e.out + split_off + m * e.ldo + n) = v;
+                break;
         }
     }
 }
@@ -286,11 +296,12 @@ struct TcCfg {
     static constexpr int B_BYTES = BN * TC_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int STAGING_BYTES = 8 * 32 * 32 * 4;   // 4 KB per epilogue warp
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
 };
 
 template <int BN, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                int M, int N, int K, int splits, GemmEpi epi, DevState* st) {
     using Cfg = TcCfg<BN, A_MN, B_MN>;
@@ -299,7 +310,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-    uint64_t* full = (uint64_t*)(smem + STAGES * Cfg::STAGE_BYTES);
+    float* staging = (float*)(smem + STAGES * Cfg::STAGE_BYTES);
+    uint64_t* full = (uint64_t*)(smem + STAGES * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
@@ -315,7 +327,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], 8);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -425,25 +437,39 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5: TMEM lanes 32*(warp%4) ...
-        const int q = warp & 3;
-        const int row_in_tile = q * 32 + lane;
+        // ---------------- epilogue warps 2..9. TMEM lane quarter = warp % 4 (the
+        // hardware's access rule); the two warps of a quarter split the columns.
+        const int q4 = warp & 3;
+        const int half = (warp - 2) >> 2;
+        constexpr int HCH = BN / 64;                 // 32-column chunks per half
+        float* st_w = staging + (warp - 2) * 32 * 32;
+        const int rsub = lane >> 3, qc = lane & 7;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
             int split = w / tiles, mt, nt;
             tile_coords(w - split * tiles, num_m, num_n, mt, nt);
+            const int64_t m_base = (int64_t)mt * TC_BM + q4 * 32;
+            const int64_t split_off = (int64_t)split * M * N;
+            const int nbase = nt * BN + half * HCH * 32;
+            AuxBuf cur;
+            aux_load(epi, m_base, M, nbase + 4 * qc, N, rsub, cur);   // overlaps the main loop
             bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int64_t m = (int64_t)mt * TC_BM + row_in_tile;
-            const int64_t split_off = (int64_t)split * M * N;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; c++) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+#pragma unroll
+            for (int cc = 0; cc < HCH; cc++) {
+                const int c = half * HCH + cc;
                 const int n0 = nt * BN + c * 32;
-                if (m < M && n0 < N) epilogue_chunk(epi, m, n0, N, (float*)r, split_off);
+                AuxBuf nxt;
+                if (cc + 1 < HCH) aux_load(epi, m_base, M, n0 + 32 + 4 * qc, N, rsub, nxt);
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                stage_write(st_w, lane, r);
+                __syncwarp();
+                epilogue_chunk(epi, st_w, m_base, M, n0 + 4 * qc, N, rsub, qc, cur, split_off);
+                __syncwarp();
+                if (cc + 1 < HCH) cur = nxt;
             }
             tc_fence_before();
             __syncwarp();
@@ -502,6 +528,7 @@ bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, c
     if ((A.ld % 8) || (B.ld % 8)) return false;
     if (((uintptr_t)A.ptr | (uintptr_t)B.ptr) & 15) return false;
     if (epi.ldo % 8) return false;
+    if (N % 4) return false;
     if (!get_encode()) return false;
     return true;
 }
@@ -525,7 +552,7 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN);
     const int total = tiles * splits;
     const int grid = total < num_sms() ? total : num_sms();
-    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, M, N, K, splits, epi, st);
+    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 320, Cfg::SMEM, s>>>(ta, tb, M, N, K, splits, epi, st);
     return cudaGetLastError();
 }
 

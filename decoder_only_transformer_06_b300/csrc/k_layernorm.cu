@@ -59,16 +59,17 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 ln_bwd_kernel(const Act* __restrict__ du, const float* __restrict__ x,
               const float* __restrict__ g, const float* __restrict__ mu,
               const float* __restrict__ rstd_in, float* __restrict__ dres,
-              Act* __restrict__ dres_act, int accumulate, float* __restrict__ partial, int M,
-              int C) {
-    extern __shared__ float sm[];   // [LN_WARPS][2][C]
+              Act* __restrict__ dres_act, int accumulate, int want_sum,
+              float* __restrict__ partial, int M, int C) {
+    extern __shared__ float sm[];   // [LN_WARPS][3][C]
     int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    float pg[EPL], pb[EPL], gv[EPL];
+    float pg[EPL], pb[EPL], ps[EPL], gv[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; j++) {
         int c = lane + 32 * j;
         pg[j] = 0.f;
         pb[j] = 0.f;
+        ps[j] = 0.f;
         gv[j] = c < C ? g[c] : 0.f;
     }
     int stride = gridDim.x * LN_WARPS;
@@ -106,6 +107,7 @@ ln_bwd_kernel(const Act* __restrict__ du, const float* __restrict__ x,
                 float o = accumulate ? dr[c] + dx : dx;
                 dr[c] = o;
                 da[c] = from_f<Act>(o);
+                ps[j] += o;
             }
         }
     }
@@ -113,42 +115,194 @@ ln_bwd_kernel(const Act* __restrict__ du, const float* __restrict__ x,
     for (int j = 0; j < EPL; j++) {
         int c = lane + 32 * j;
         if (c < C) {
-            sm[(warp * 2 + 0) * C + c] = pg[j];
-            sm[(warp * 2 + 1) * C + c] = pb[j];
+            sm[(warp * 3 + 0) * C + c] = pg[j];
+            sm[(warp * 3 + 1) * C + c] = pb[j];
+            sm[(warp * 3 + 2) * C + c] = ps[j];
         }
     }
     __syncthreads();
+    const int np = want_sum ? 3 : 2;
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        float a = 0.f, bb = 0.f;
-        for (int w = 0; w < LN_WARPS; w++) {
-            a += sm[(w * 2 + 0) * C + c];
-            bb += sm[(w * 2 + 1) * C + c];
+        for (int k = 0; k < np; k++) {
+            float a = 0.f;
+            for (int w = 0; w < LN_WARPS; w++) a += sm[(w * 3 + k) * C + c];
+            partial[((int64_t)blockIdx.x * 3 + k) * C + c] = a;
         }
-        partial[(int64_t)blockIdx.x * 2 * C + c] = a;
-        partial[(int64_t)blockIdx.x * 2 * C + C + c] = bb;
+    }
+}
+
+
+// ---------------------------------------------------------------- vector path
+// C a multiple of 128: lane l owns float4 columns l, l+32, ... (each warp load
+// is 512 contiguous bytes); the activation is written 4 values at a time.
+template <typename Act>
+__device__ __forceinline__ void store4(Act* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) { *(float4*)dst = v; }
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* dst, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *(uint32_t*)&lo;
+    o.y = *(uint32_t*)&hi;
+    *(uint2*)dst = o;
+}
+template <typename Act>
+__device__ __forceinline__ float4 load4(const Act* src);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* src) { return *(const float4*)src; }
+template <>
+__device__ __forceinline__ float4 load4<bf16>(const bf16* src) {
+    uint2 w = *(const uint2*)src;
+    float2 a = __bfloat1622float2(*(const __nv_bfloat162*)&w.x);
+    float2 b = __bfloat1622float2(*(const __nv_bfloat162*)&w.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename Act, int V4>
+__global__ void __launch_bounds__(LN_WARPS * 32)
+ln_fwd_vec(const float* __restrict__ x, const float* __restrict__ g, const float* __restrict__ b,
+           Act* __restrict__ u, float* __restrict__ mu_out, float* __restrict__ rstd_out, int M,
+           int C) {
+    const int row = blockIdx.x * LN_WARPS + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= M) return;
+    const float4* xr = (const float4*)(x + (int64_t)row * C);
+    float4 v[V4];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < V4; j++) {
+        v[j] = xr[lane + 32 * j];
+        s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+    }
+    const float mean = warp_sum(s) / (float)C;
+    float q = 0.f;
+#pragma unroll
+    for (int j = 0; j < V4; j++) {
+        float a = v[j].x - mean, bq = v[j].y - mean, c = v[j].z - mean, d = v[j].w - mean;
+        q += (a * a + bq * bq) + (c * c + d * d);
+    }
+    const float rstd = 1.0f / sqrtf(warp_sum(q) / (float)C + LN_EPS);
+    Act* ur = u + (int64_t)row * C;
+#pragma unroll
+    for (int j = 0; j < V4; j++) {
+        const int c4 = lane + 32 * j;
+        const float4 gg = __ldg((const float4*)g + c4), bb = __ldg((const float4*)b + c4);
+        float4 y = make_float4((v[j].x - mean) * rstd * gg.x + bb.x, (v[j].y - mean) * rstd * gg.y + bb.y,
+                               (v[j].z - mean) * rstd * gg.z + bb.z, (v[j].w - mean) * rstd * gg.w + bb.w);
+        store4<Act>(ur + 4 * c4, y);
+    }
+    if (lane == 0) {
+        mu_out[row] = mean;
+        rstd_out[row] = rstd;
+    }
+}
+
+template <typename Act, int V4>
+__global__ void __launch_bounds__(LN_WARPS * 32, 2)
+ln_bwd_vec(const Act* __restrict__ du, const float* __restrict__ x, const float* __restrict__ g,
+           const float* __restrict__ mu, const float* __restrict__ rstd_in,
+           float* __restrict__ dres, Act* __restrict__ dres_act, int accumulate, int want_sum,
+           float* __restrict__ partial, int M, int C) {
+    // each warp accumulates its partials (dg, db and, if asked, the column sum
+    // of the new dres) in its own slice of shared memory ([LN_WARPS][3][C]);
+    // slices are combined in warp order at the end
+    extern __shared__ float sm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float4* pgs = (float4*)&sm[(warp * 3 + 0) * C];
+    float4* pbs = (float4*)&sm[(warp * 3 + 1) * C];
+    float4* pss = (float4*)&sm[(warp * 3 + 2) * C];
+#pragma unroll
+    for (int j = 0; j < V4; j++) {
+        pgs[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        pbs[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        pss[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float invC = 1.0f / (float)C;
+    const int stride = gridDim.x * LN_WARPS;
+    for (int row = blockIdx.x * LN_WARPS + warp; row < M; row += stride) {
+        const Act* dur = du + (int64_t)row * C;
+        const float4* xr = (const float4*)(x + (int64_t)row * C);
+        float4* dr = (float4*)(dres + (int64_t)row * C);
+        const float m = mu[row], rs = rstd_in[row];
+        float4 dy[V4], xh[V4], prev[V4];
+#pragma unroll
+        for (int j = 0; j < V4; j++) {
+            const int c4 = lane + 32 * j;
+            dy[j] = load4<Act>(dur + 4 * c4);
+            xh[j] = xr[c4];
+            prev[j] = accumulate ? dr[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < V4; j++) {
+            const int c4 = lane + 32 * j;
+            xh[j] = make_float4((xh[j].x - m) * rs, (xh[j].y - m) * rs, (xh[j].z - m) * rs, (xh[j].w - m) * rs);
+            const float4 gg = __ldg((const float4*)g + c4);
+            float a = dy[j].x * gg.x, bq = dy[j].y * gg.y, c = dy[j].z * gg.z, d = dy[j].w * gg.w;
+            s1 += (a + bq) + (c + d);
+            s2 += (a * xh[j].x + bq * xh[j].y) + (c * xh[j].z + d * xh[j].w);
+        }
+        s1 = warp_sum(s1) * invC;
+        s2 = warp_sum(s2) * invC;
+        Act* da = dres_act + (int64_t)row * C;
+#pragma unroll
+        for (int j = 0; j < V4; j++) {
+            const int c4 = lane + 32 * j;
+            const float4 gg = __ldg((const float4*)g + c4);
+            float4 o = make_float4(prev[j].x + rs * (dy[j].x * gg.x - s1 - xh[j].x * s2),
+                                   prev[j].y + rs * (dy[j].y * gg.y - s1 - xh[j].y * s2),
+                                   prev[j].z + rs * (dy[j].z * gg.z - s1 - xh[j].z * s2),
+                                   prev[j].w + rs * (dy[j].w * gg.w - s1 - xh[j].w * s2));
+            dr[c4] = o;
+            if ((const void*)da != (const void*)dr) store4<Act>(da + 4 * c4, o);
+            float4 pg = pgs[c4], pb = pbs[c4];
+            pg.x += dy[j].x * xh[j].x; pg.y += dy[j].y * xh[j].y;
+            pg.z += dy[j].z * xh[j].z; pg.w += dy[j].w * xh[j].w;
+            pb.x += dy[j].x; pb.y += dy[j].y; pb.z += dy[j].z; pb.w += dy[j].w;
+            pgs[c4] = pg;
+            pbs[c4] = pb;
+            if (want_sum) {
+                float4 ps = pss[c4];
+                ps.x += o.x; ps.y += o.y; ps.z += o.z; ps.w += o.w;
+                pss[c4] = ps;
+            }
+        }
+    }
+    __syncthreads();
+    const int np = want_sum ? 3 : 2;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        for (int k = 0; k < np; k++) {
+            float a = 0.f;
+            for (int w = 0; w < LN_WARPS; w++) a += sm[(w * 3 + k) * C + c];
+            partial[((int64_t)blockIdx.x * 3 + k) * C + c] = a;
+        }
     }
 }
 
 __global__ void ln_param_reduce(const float* __restrict__ partial, int nblocks, int C,
-                                float* __restrict__ dg, float* __restrict__ db) {
+                                float* __restrict__ dg, float* __restrict__ db,
+                                float* __restrict__ dsum) {
     int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= C) return;
-    float a = 0.f, b = 0.f;
+    float a = 0.f, b = 0.f, t = 0.f;
     for (int k = 0; k < nblocks; k++) {
-        a += partial[(int64_t)k * 2 * C + c];
-        b += partial[(int64_t)k * 2 * C + C + c];
+        a += partial[((int64_t)k * 3 + 0) * C + c];
+        b += partial[((int64_t)k * 3 + 1) * C + c];
+        if (dsum) t += partial[((int64_t)k * 3 + 2) * C + c];
     }
     dg[c] += a;
     db[c] += b;
+    if (dsum) dsum[c] += t;
 }
 
 static int ln_bwd_blocks(int M) {
     int want = (M + LN_WARPS - 1) / LN_WARPS;
-    int cap = num_sms() * 4;
+    int cap = num_sms() * 2;
     return want < cap ? want : cap;
 }
 
-size_t layernorm_bwd_partial_floats(int M, int C) { return (size_t)ln_bwd_blocks(M) * 2 * C; }
+size_t layernorm_bwd_partial_floats(int M, int C) { return (size_t)ln_bwd_blocks(M) * 3 * C; }
 
 #define LN_DISPATCH(EPLV, CALL)                       \
     if (epl <= EPLV) { CALL(EPLV); return cudaGetLastError(); }
@@ -158,6 +312,17 @@ cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u
                           float* rstd, int M, int C, cudaStream_t s) {
     int epl = (C + 31) / 32;
     int blocks = (M + LN_WARPS - 1) / LN_WARPS;
+    if (C % 128 == 0 && C <= 2048) {
+        switch (C / 128) {
+#define LNV(V)                                                                                      \
+    case V:                                                                                         \
+        ln_fwd_vec<Act, V><<<blocks, LN_WARPS * 32, 0, s>>>(x, g, b, u, mu, rstd, M, C);            \
+        return cudaGetLastError();
+            LNV(1) LNV(2) LNV(3) LNV(4) LNV(5) LNV(6) LNV(7) LNV(8)
+            LNV(9) LNV(10) LNV(11) LNV(12) LNV(13) LNV(14) LNV(15) LNV(16)
+#undef LNV
+        }
+    }
 #define LNF(E) ln_fwd_kernel<Act, E><<<blocks, LN_WARPS * 32, 0, s>>>(x, g, b, u, mu, rstd, M, C)
     LN_DISPATCH(2, LNF)
     LN_DISPATCH(4, LNF)
@@ -175,17 +340,36 @@ cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u
 template <typename Act>
 cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const float* mu,
                           const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
-                          float* db, int M, int C, float* partial, cudaStream_t s) {
+                          float* db, float* dsum, int M, int C, float* partial, cudaStream_t s) {
     int epl = (C + 31) / 32;
     int blocks = ln_bwd_blocks(M);
-    size_t smem = (size_t)LN_WARPS * 2 * C * sizeof(float);
+    size_t smem = (size_t)LN_WARPS * 3 * C * sizeof(float);
+    const int want_sum = dsum ? 1 : 0;
     cudaError_t e = cudaErrorInvalidValue;
+    if (C % 128 == 0 && C <= 1024) {
+        switch (C / 128) {
+#define LBV(V)                                                                                     \
+    case V:                                                                                        \
+        cudaFuncSetAttribute(ln_bwd_vec<Act, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
+                             (int)smem);                                                           \
+        ln_bwd_vec<Act, V><<<blocks, LN_WARPS * 32, smem, s>>>(du, x, g, mu, rstd, dres, dres_act, \
+                                                               accumulate ? 1 : 0, want_sum,       \
+                                                               partial, M, C);                     \
+        e = cudaGetLastError();                                                                    \
+        break;
+            LBV(1) LBV(2) LBV(3) LBV(4) LBV(5) LBV(6) LBV(7) LBV(8)
+#undef LBV
+        }
+        if (e != cudaSuccess) return e;
+        ln_param_reduce<<<(C + 255) / 256, 256, 0, s>>>(partial, blocks, C, dg, db, dsum);
+        return cudaGetLastError();
+    }
 #define LNB(E)                                                                                  \
     do {                                                                                        \
         cudaFuncSetAttribute(ln_bwd_kernel<Act, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              (int)smem);                                                        \
         ln_bwd_kernel<Act, E><<<blocks, LN_WARPS * 32, smem, s>>>(                              \
-            du, x, g, mu, rstd, dres, dres_act, accumulate ? 1 : 0, partial, M, C);             \
+            du, x, g, mu, rstd, dres, dres_act, accumulate ? 1 : 0, want_sum, partial, M, C);   \
         e = cudaGetLastError();                                                                 \
     } while (0)
     if (epl <= 2) LNB(2);
@@ -199,7 +383,7 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
     else if (epl <= 64) LNB(64);
 #undef LNB
     if (e != cudaSuccess) return e;
-    ln_param_reduce<<<(C + 255) / 256, 256, 0, s>>>(partial, blocks, C, dg, db);
+    ln_param_reduce<<<(C + 255) / 256, 256, 0, s>>>(partial, blocks, C, dg, db, dsum);
     return cudaGetLastError();
 }
 
@@ -208,10 +392,10 @@ template cudaError_t layernorm_fwd<float>(const float*, const float*, const floa
 template cudaError_t layernorm_fwd<bf16>(const float*, const float*, const float*, bf16*, float*,
                                          float*, int, int, cudaStream_t);
 template cudaError_t layernorm_bwd<float>(const float*, const float*, const float*, const float*,
-                                          const float*, float*, float*, bool, float*, float*, int,
-                                          int, float*, cudaStream_t);
+                                          const float*, float*, float*, bool, float*, float*,
+                                          float*, int, int, float*, cudaStream_t);
 template cudaError_t layernorm_bwd<bf16>(const bf16*, const float*, const float*, const float*,
-                                         const float*, float*, bf16*, bool, float*, float*, int,
-                                         int, float*, cudaStream_t);
+                                         const float*, float*, bf16*, bool, float*, float*, float*,
+                                         int, int, float*, cudaStream_t);
 
 }  // namespace k

@@ -230,35 +230,53 @@ cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* d
 }
 
 // ---------------------------------------------------------------- column sums
-// db[n] += sum_m dy[m, n], as a fixed-order two-stage reduction: stage 1 sums
-// row splits of 2 columns per thread (8 row phases per CTA, combined in order);
-// stage 2 adds the split partials in split order.
+// db[n] += sum_m dy[m, n], as a fixed-order two-stage reduction. Stage 1: a
+// CTA of 32 x 8 threads covers 32 16-byte column vectors and one split of
+// CS_ROWS_PER_SPLIT rows; threadIdx.y takes every 8th row, the 8 row phases
+// are combined in order through shared memory. Stage 2 adds the split
+// partials in split order.
 static constexpr int CS_ROWS_PER_SPLIT = 256;
 
 template <typename T>
-__global__ void colsum_stage1(const T* __restrict__ dy, int64_t ld, int M, int N,
-                              float* __restrict__ partial) {
-    __shared__ float sm[8][64];
-    int n = blockIdx.x * 64 + threadIdx.x * 2;
-    int r0 = blockIdx.y * CS_ROWS_PER_SPLIT;
-    int r1 = min(r0 + CS_ROWS_PER_SPLIT, M);
-    float a0 = 0.f, a1 = 0.f;
+__global__ void __launch_bounds__(256)
+colsum_stage1(const T* __restrict__ dy, int64_t ld, int M, int N, float* __restrict__ partial) {
+    constexpr int VEC = 16 / sizeof(T);
+    __shared__ float sm[8][32 * VEC + 1];
+    const int n = (blockIdx.x * 32 + threadIdx.x) * VEC;
+    const int r0 = blockIdx.y * CS_ROWS_PER_SPLIT;
+    const int r1 = min(r0 + CS_ROWS_PER_SPLIT, M);
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; e++) acc[e] = 0.f;
     if (n < N) {
+#pragma unroll 4
         for (int r = r0 + threadIdx.y; r < r1; r += 8) {
-            const T* p = dy + (int64_t)r * ld + n;
-            a0 += to_f(p[0]);
-            if (n + 1 < N) a1 += to_f(p[1]);
+            uint4 w = *(const uint4*)(dy + (int64_t)r * ld + n);
+            if constexpr (sizeof(T) == 2) {
+                const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    float2 f = __bfloat1622float2(h[t]);
+                    acc[2 * t] += f.x;
+                    acc[2 * t + 1] += f.y;
+                }
+            } else {
+                const float* f = (const float*)&w;
+#pragma unroll
+                for (int t = 0; t < 4; t++) acc[t] += f[t];
+            }
         }
     }
-    sm[threadIdx.y][threadIdx.x * 2] = a0;
-    sm[threadIdx.y][threadIdx.x * 2 + 1] = a1;
+#pragma unroll
+    for (int e = 0; e < VEC; e++) sm[threadIdx.y][threadIdx.x * VEC + e] = acc[e];
     __syncthreads();
-    if (threadIdx.y == 0) {
-        for (int j = 0; j < 2; j++) {
-            int c = threadIdx.x * 2 + j;
+    for (int c = threadIdx.y * 32 + threadIdx.x; c < 32 * VEC; c += 256) {
+        const int col = blockIdx.x * 32 * VEC + c;
+        if (col < N) {
             float s = 0.f;
+#pragma unroll
             for (int y = 0; y < 8; y++) s += sm[y][c];
-            if (blockIdx.x * 64 + c < N) partial[(int64_t)blockIdx.y * N + blockIdx.x * 64 + c] = s;
+            partial[(int64_t)blockIdx.y * N + col] = s;
         }
     }
 }
@@ -279,8 +297,10 @@ size_t colsum_partial_floats(int M, int N) {
 template <typename T>
 cudaError_t colsum_add(const T* dy, int64_t ld, int M, int N, float* db, float* partial,
                        cudaStream_t s) {
+    constexpr int VEC = 16 / sizeof(T);
+    if ((N % VEC) || (ld % VEC) || ((uintptr_t)dy & 15)) return cudaErrorInvalidValue;
     int splits = (M + CS_ROWS_PER_SPLIT - 1) / CS_ROWS_PER_SPLIT;
-    dim3 grid((N + 63) / 64, splits);
+    dim3 grid((N / VEC + 31) / 32, splits);
     colsum_stage1<T><<<grid, dim3(32, 8), 0, s>>>(dy, ld, M, N, partial);
     CUDA_OK(cudaGetLastError());
     colsum_stage2<<<(N + 255) / 256, 256, 0, s>>>(partial, splits, N, db);

@@ -39,12 +39,42 @@ def cosine(a, b) -> float:
     return float(a @ b / (na * nb))
 
 
-def adamw_param_diff(p_gpu, p_orc, g_gpu, g_orc):
-    """Max |p_gpu - p_orc| over elements whose gradients agree in sign, and the
-    number of elements whose signs differ (a first AdamW step moves every
-    element by about lr whatever |g|, so a sign flip at the noise floor moves
-    it by 2 lr)."""
+def adamw_param_check(p_gpu, p_orc, g_gpu, g_orc, fp32: bool):
+    """Post-AdamW parameter comparison (first step, lr ~1e-3).
+
+    A first AdamW step moves an element by lr * g / (|g| + eps) (plus the
+    identical decay), i.e. by about lr whatever |g|, so:
+      * where the GPU and oracle gradients agree in sign, |p_gpu - p_orc| is
+        returned as `agree_max` (bf16 bound 1e-3; for fp32 only elements with
+        |g| >= 100*eps are taken, because the step is ill-conditioned near
+        |g| = eps and an fp32 gradient there carries relative error);
+      * a sign flip moves an element by up to 2 lr; `big_flips` counts flips
+        among elements whose oracle gradient is large (> 0.1 * the tensor's RMS
+        and > eps), where none should occur.
+    Returns (agree_max, big_flips, all_max)."""
     p_gpu, p_orc = np.asarray(p_gpu, np.float64), np.asarray(p_orc, np.float64)
-    agree = np.sign(g_gpu) == np.sign(g_orc)
+    g_gpu, g_orc = np.asarray(g_gpu, np.float64), np.asarray(g_orc, np.float64)
     d = np.abs(p_gpu - p_orc)
-    return float(d[agree].max()) if agree.any() else 0.0, int((~agree).sum())
+    agree = np.sign(g_gpu) == np.sign(g_orc)
+    sel = agree & (np.abs(g_orc) >= 1e-6) if fp32 else agree
+    agree_max = float(d[sel].max()) if sel.any() else 0.0
+    rms = float(np.sqrt(np.mean(g_orc ** 2))) if g_orc.size else 0.0
+    big = (np.abs(g_orc) > 0.1 * rms) & (np.abs(g_orc) > 1e-8)
+    big_flips = int(np.count_nonzero(big & ~agree))
+    return agree_max, big_flips, float(d.max())
+
+
+def oracle_adamw_on(params0, grads, lr, t=1, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, clip=1.0):
+    """The oracle's clip + AdamW applied to given gradients (the optimizer in
+    isolation: fed the GPU's own gradients it must reproduce the GPU's update)."""
+    from oracle import gpt2_oracle as O
+    g = {n: np.asarray(a, np.float64).copy() for n, a in grads.items()}
+    O.clip_grads(g, clip)
+    out = {}
+    for n, p0 in params0.items():
+        p = np.asarray(p0, np.float64).copy()
+        m = np.zeros_like(p)
+        v = np.zeros_like(p)
+        O.adamw_update(p, g[n], m, v, t, lr, beta1, beta2, eps, wd, p.ndim >= 2)
+        out[n] = p
+    return out

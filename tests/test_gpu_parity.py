@@ -4,9 +4,14 @@ oracle on the same seeded inputs, through the C ABI.
 Tolerances:
   fp32-math mode: loss and every gradient within 1e-4 relative (per-tensor L2).
   bf16 mode: loss within 5e-3 relative; per-tensor gradient relative L2 <= 2e-2
-  and cosine >= 0.999; after AdamW, parameters within 1e-3 absolute on every
-  element whose gradient sign agrees with the oracle's (the sign-flip count is
-  reported and must stay a tiny fraction).
+  and cosine >= 0.999; after AdamW, parameters within 1e-3 absolute.
+Post-AdamW parameters are checked two ways. (1) The optimizer in isolation:
+the oracle's clip + AdamW fed the GPU's own gradients reproduces the GPU's
+parameters within 1e-6 absolute. (2) End to end (see adamw_param_check): a
+first Adam step moves every element by ~lr whatever |g|, so the 1e-3 bound
+applies where the two gradients agree in sign (fp32: 1e-6 where also
+|g| >= 100 eps); no element with a large gradient may flip sign; every
+element stays within 2 lr (plus decay) of the oracle.
 """
 import math
 
@@ -19,7 +24,7 @@ from decoder_only_transformer_06_b300 import gpt2
 from oracle import CONFIGS
 from oracle import gpt2_oracle as O
 
-from gpu_helpers import adamw_param_diff, cosine, dev, gpu_cfg, oracle_cfg, rel_l2
+from gpu_helpers import adamw_param_check, cosine, dev, gpu_cfg, oracle_adamw_on, oracle_cfg, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -39,13 +44,21 @@ def _compare_step(ocfg, precision, kind, seed=1337, data_seed=42, lr=1e-3, ignor
     m.backward()
     tr.backward()
     g_gpu = m.state(gpt2.GPT2_GRAD)
+    p0 = {n: a.copy() for n, a in tr.params.items()}
     norm = m.step(lr=lr)
     p_gpu = m.state(gpt2.GPT2_PARAM)
     g_orc = {n: a.copy() for n, a in tr.grads.items()}
     tn = tr.step(lr=lr)
     out = dict(loss=(loss, lo), norm=(norm, tn), g_gpu=g_gpu, g_orc=g_orc, p_gpu=p_gpu,
-               p_orc=tr.params, m=m, tr=tr, V=ocfg.vocab_size)
+               p_orc=tr.params, m=m, tr=tr, V=ocfg.vocab_size,
+               p_iso=oracle_adamw_on(p0, g_gpu, lr))
     return out
+
+
+def _check_isolated_adamw(r):
+    for n, p in r["p_iso"].items():
+        d = float(np.abs(r["p_gpu"][n] - p).max())
+        assert d < 1e-6, (n, d)
 
 
 def _check_fp32(r):
@@ -55,10 +68,12 @@ def _check_fp32(r):
         e = rel_l2(r["g_gpu"][n], g)
         assert e < 1e-4, (n, e)
     assert abs(r["norm"][0] - r["norm"][1]) / r["norm"][1] < 1e-4
+    _check_isolated_adamw(r)
     for n in r["p_orc"]:
-        d, flips = adamw_param_diff(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n], r["g_orc"][n])
+        d, flips, _ = adamw_param_check(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n],
+                                        r["g_orc"][n], fp32=True)
         assert d < 1e-6, (n, d)
-        assert flips <= max(2, r["p_orc"][n].size // 10000), (n, flips)
+        assert flips == 0, (n, flips)
 
 
 def _check_bf16(r):
@@ -71,13 +86,13 @@ def _check_bf16(r):
         e, c = rel_l2(r["g_gpu"][n], g), cosine(r["g_gpu"][n], g)
         assert e <= 2e-2 and c >= 0.999, (n, e, c)
     assert abs(r["norm"][0] - r["norm"][1]) / r["norm"][1] < 2e-2
-    total_flips = 0
+    _check_isolated_adamw(r)
     for n in r["p_orc"]:
-        d, flips = adamw_param_diff(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n], r["g_orc"][n])
+        d, flips, dmax = adamw_param_check(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n],
+                                           r["g_orc"][n], fp32=False)
         assert d <= 1e-3, (n, d)
-        total_flips += flips
-    total = sum(a.size for a in r["p_orc"].values())
-    assert total_flips <= 0.01 * total, total_flips
+        assert flips <= max(2, r["p_orc"][n].size // 100000), (n, flips)
+        assert dmax <= 2.2e-3, (n, dmax)      # 2 lr (+ decay) for any element
 
 
 def _pad_rows_zero(r):
