@@ -39,15 +39,17 @@ def cosine(a, b) -> float:
     return float(a @ b / (na * nb))
 
 
-def adamw_param_check(p_gpu, p_orc, g_gpu, g_orc, fp32: bool):
+def adamw_param_check(p_gpu, p_orc, g_gpu, g_orc, fp32: bool, coef: float = 1.0):
     """Post-AdamW parameter comparison (first step, lr ~1e-3).
 
     A first AdamW step moves an element by lr * g / (|g| + eps) (plus the
     identical decay), i.e. by about lr whatever |g|, so:
       * where the GPU and oracle gradients agree in sign, |p_gpu - p_orc| is
-        returned as `agree_max` (bf16 bound 1e-3; for fp32 only elements with
-        |g| >= 100*eps are taken, because the step is ill-conditioned near
-        |g| = eps and an fp32 gradient there carries relative error);
+        returned as `agree_max` (bf16 bound 1e-3; for fp32 only elements whose
+        clipped gradient coef*|g| (the gradient AdamW sees; coef = the clip
+        coefficient) is >= 100*eps are taken, because the step's sensitivity
+        lr*eps/(|g|+eps)^2 grows without bound as |g| nears eps and an fp32
+        gradient there carries relative error);
       * a sign flip moves an element by up to 2 lr; `big_flips` counts flips
         among elements whose oracle gradient is large (> 0.1 * the tensor's RMS
         and > eps), where none should occur.
@@ -56,7 +58,7 @@ def adamw_param_check(p_gpu, p_orc, g_gpu, g_orc, fp32: bool):
     g_gpu, g_orc = np.asarray(g_gpu, np.float64), np.asarray(g_orc, np.float64)
     d = np.abs(p_gpu - p_orc)
     agree = np.sign(g_gpu) == np.sign(g_orc)
-    sel = agree & (np.abs(g_orc) >= 1e-6) if fp32 else agree
+    sel = agree & (coef * np.abs(g_orc) >= 1e-6) if fp32 else agree
     agree_max = float(d[sel].max()) if sel.any() else 0.0
     rms = float(np.sqrt(np.mean(g_orc ** 2))) if g_orc.size else 0.0
     big = (np.abs(g_orc) > 0.1 * rms) & (np.abs(g_orc) > 1e-8)

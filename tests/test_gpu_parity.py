@@ -69,9 +69,10 @@ def _check_fp32(r):
         assert e < 1e-4, (n, e)
     assert abs(r["norm"][0] - r["norm"][1]) / r["norm"][1] < 1e-4
     _check_isolated_adamw(r)
+    coef = min(1.0, 1.0 / (r["norm"][1] + 1e-6))       # clip 1.0
     for n in r["p_orc"]:
         d, flips, _ = adamw_param_check(r["p_gpu"][n], r["p_orc"][n], r["g_gpu"][n],
-                                        r["g_orc"][n], fp32=True)
+                                        r["g_orc"][n], fp32=True, coef=coef)
         assert d < 1e-6, (n, d)
         assert flips == 0, (n, flips)
 
