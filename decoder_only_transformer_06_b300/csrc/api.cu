@@ -931,6 +931,25 @@ int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kma
     return GPT2_OK;
 }
 
+int gpt2_op_sync(void* stream) {
+    cudaError_t r = cudaStreamSynchronize((cudaStream_t)stream);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "cudaStreamSynchronize", r);
+    DevState* st = op_state();
+    if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
+    DevState h;
+    r = cudaMemcpy(&h, st, sizeof h, cudaMemcpyDeviceToHost);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "status read", r);
+    if (h.err) {
+        const unsigned int err = h.err, site = h.timeout_site;
+        cudaMemset(st, 0, sizeof(DevState));
+        if (err & ERR_TIMEOUT)
+            return fail(nullptr, GPT2_ETIMEOUT,
+                        "a bounded device wait expired in an op-level call (site " +
+                            std::to_string(site) + ")");
+    }
+    return GPT2_OK;
+}
+
 int gpt2_op_attention_fwd(int precision, int B, int T, int H, int hs, const void* qkv, void* out,
                           float* lse, void* stream) {
     if (!qkv || !out || !lse || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
@@ -963,3 +982,4 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
 }
 
 }  // extern "C"
+

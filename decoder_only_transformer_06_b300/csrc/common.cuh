@@ -93,15 +93,13 @@ __device__ __forceinline__ double warp_sum_d(double v) {
     return v;
 }
 
-// Nanoseconds since an arbitrary epoch (for bounded waits).
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded device-side waits give up after this long and report ERR_TIMEOUT.
-#define WAIT_LIMIT_NS 2000000000ull
+// Bounded device-side waits measure elapsed time on the SM's own cycle
+// counter (monotonic for the warp that reads it) and give up after
+// WAIT_LIMIT_CYCLES, about two seconds at B300 clocks; they then report
+// ERR_TIMEOUT. The global nanosecond timer is not used: the driver may adjust
+// it while a kernel runs, which would end a wait early.
+__device__ __forceinline__ long long wait_clock() { return clock64(); }
+#define WAIT_LIMIT_CYCLES 4000000000ll
 
 // ------------------------------------------------------------------ launchers
 // All launchers return cudaSuccess or the launch error; `st` may be null.

@@ -280,20 +280,35 @@ ln_bwd_vec(const Act* __restrict__ du, const float* __restrict__ x, const float*
     }
 }
 
-__global__ void ln_param_reduce(const float* __restrict__ partial, int nblocks, int C,
-                                float* __restrict__ dg, float* __restrict__ db,
-                                float* __restrict__ dsum) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
+// Second stage of the parameter-gradient reduction: block = 32 columns x 32
+// slices of the partial rows; slice s sums partial rows s, s+32, ... and the
+// slice sums are combined in slice order (fixed order: deterministic).
+static constexpr int LNR_SLICES = 32;
+__global__ void __launch_bounds__(32 * LNR_SLICES)
+ln_param_reduce(const float* __restrict__ partial, int nblocks, int C, float* __restrict__ dg,
+                float* __restrict__ db, float* __restrict__ dsum) {
+    __shared__ float sm[3][LNR_SLICES][33];
+    const int cx = threadIdx.x & 31, sl = threadIdx.x >> 5;
+    const int c = blockIdx.x * 32 + cx;
     float a = 0.f, b = 0.f, t = 0.f;
-    for (int k = 0; k < nblocks; k++) {
-        a += partial[((int64_t)k * 3 + 0) * C + c];
-        b += partial[((int64_t)k * 3 + 1) * C + c];
-        if (dsum) t += partial[((int64_t)k * 3 + 2) * C + c];
+    if (c < C) {
+#pragma unroll 4
+        for (int k = sl; k < nblocks; k += LNR_SLICES) {
+            a += partial[((int64_t)k * 3 + 0) * C + c];
+            b += partial[((int64_t)k * 3 + 1) * C + c];
+            if (dsum) t += partial[((int64_t)k * 3 + 2) * C + c];
+        }
     }
-    dg[c] += a;
-    db[c] += b;
-    if (dsum) dsum[c] += t;
+    sm[0][sl][cx] = a;
+    sm[1][sl][cx] = b;
+    sm[2][sl][cx] = t;
+    __syncthreads();
+    if (sl < 3 && c < C) {
+        float acc = 0.f;
+        for (int k = 0; k < LNR_SLICES; k++) acc += sm[sl][k][cx];
+        float* dst = sl == 0 ? dg : (sl == 1 ? db : dsum);
+        if (dst) dst[c] += acc;
+    }
 }
 
 static int ln_bwd_blocks(int M) {
@@ -361,7 +376,7 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
 #undef LBV
         }
         if (e != cudaSuccess) return e;
-        ln_param_reduce<<<(C + 255) / 256, 256, 0, s>>>(partial, blocks, C, dg, db, dsum);
+        ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, blocks, C, dg, db, dsum);
         return cudaGetLastError();
     }
 #define LNB(E)                                                                                  \
@@ -383,7 +398,7 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
     else if (epl <= 64) LNB(64);
 #undef LNB
     if (e != cudaSuccess) return e;
-    ln_param_reduce<<<(C + 255) / 256, 256, 0, s>>>(partial, blocks, C, dg, db, dsum);
+    ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, blocks, C, dg, db, dsum);
     return cudaGetLastError();
 }
 

@@ -281,13 +281,24 @@ colsum_stage1(const T* __restrict__ dy, int64_t ld, int M, int N, float* __restr
     }
 }
 
-__global__ void colsum_stage2(const float* __restrict__ partial, int splits, int N,
-                              float* __restrict__ db) {
-    int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
+// Second stage: block = 32 columns x 8 slices of the partial rows, slices
+// combined in slice order (deterministic).
+__global__ void __launch_bounds__(256)
+colsum_stage2(const float* __restrict__ partial, int splits, int N, float* __restrict__ db) {
+    __shared__ float sm[8][33];
+    const int cx = threadIdx.x & 31, sl = threadIdx.x >> 5;
+    const int n = blockIdx.x * 32 + cx;
     float s = 0.f;
-    for (int k = 0; k < splits; k++) s += partial[(int64_t)k * N + n];
-    db[n] += s;
+    if (n < N)
+        for (int k = sl; k < splits; k += 8) s += partial[(int64_t)k * N + n];
+    sm[sl][cx] = s;
+    __syncthreads();
+    if (sl == 0 && n < N) {
+        float t = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) t += sm[k][cx];
+        db[n] += t;
+    }
 }
 
 size_t colsum_partial_floats(int M, int N) {
@@ -303,7 +314,7 @@ cudaError_t colsum_add(const T* dy, int64_t ld, int M, int N, float* db, float* 
     dim3 grid((N / VEC + 31) / 32, splits);
     colsum_stage1<T><<<grid, dim3(32, 8), 0, s>>>(dy, ld, M, N, partial);
     CUDA_OK(cudaGetLastError());
-    colsum_stage2<<<(N + 255) / 256, 256, 0, s>>>(partial, splits, N, db);
+    colsum_stage2<<<(N + 31) / 32, 256, 0, s>>>(partial, splits, N, db);
     return cudaGetLastError();
 }
 template cudaError_t colsum_add<float>(const float*, int64_t, int, int, float*, float*,

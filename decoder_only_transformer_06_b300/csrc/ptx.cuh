@@ -32,13 +32,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity, giving up after WAIT_LIMIT_NS.
+// Wait for the phase with the given parity, giving up after WAIT_LIMIT_CYCLES.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
+    const long long t0 = wait_clock();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (wait_clock() - t0 > WAIT_LIMIT_CYCLES) return false;
     }
 }
 // 1-D bulk copy global -> shared; completion counted on `bar` (bytes % 16 == 0,

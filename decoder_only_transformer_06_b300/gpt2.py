@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_last_error": (ctypes.c_char_p, [P]),
         "gpt2_version": (ctypes.c_char_p, []),
         "gpt2_op_gemm_bf16": (I, [I, I, I, P, I64, I, P, I64, I, P, P, P, I64, I, P]),
+        "gpt2_op_sync": (I, [P]),
         "gpt2_op_attention_fwd": (I, [I, I, I, I, I, P, P, P, P]),
         "gpt2_op_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
     }
@@ -294,6 +295,12 @@ def op_gemm_bf16(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, bias=None, out_bf1
                                   _stream_ptr(stream)))
 
 
+def op_sync(stream=None):
+    """Synchronise the stream; raise GPT2Error(ETIMEOUT) if a bounded device
+    wait expired in an op-level call since the last op_sync."""
+    _check(_lib.gpt2_op_sync(_stream_ptr(stream)))
+
+
 def op_attention_fwd(precision, B, T, H, hs, qkv, out, lse, stream=None):
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
     _check(_lib.gpt2_op_attention_fwd(precision, B, T, H, hs, ptr(qkv), ptr(out), ptr(lse),
@@ -304,3 +311,4 @@ def op_attention_bwd(precision, B, T, H, hs, qkv, out, lse, dout, dqkv, scratch,
     ptr = lambda t: ctypes.c_void_p(t.data_ptr())
     _check(_lib.gpt2_op_attention_bwd(precision, B, T, H, hs, ptr(qkv), ptr(out), ptr(lse),
                                       ptr(dout), ptr(dqkv), ptr(scratch), _stream_ptr(stream)))
+

@@ -240,6 +240,12 @@ int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kma
                       void* out_bf16, float* out_f32, int64_t ldd, int accumulate,
                       void* stream);
 
+/* Synchronise `stream` and report device-side conditions raised by the
+ * op-level calls above since the previous gpt2_op_sync: GPT2_ETIMEOUT if a
+ * bounded wait inside a kernel expired (the kernel then skipped its remaining
+ * work, so its outputs are incomplete). Clears the recorded conditions. */
+int gpt2_op_sync(void* stream);
+
 /* Causal attention forward on a fused qkv buffer [B*T, 3C] (bf16 when
  * precision == GPT2_BF16, else fp32): out [B*T, C], lse fp32 [B, H, T]
  * (natural log of each softmax row's normaliser, scores scaled by 1/sqrt(hs)). */

@@ -16,8 +16,8 @@ pytestmark = pytest.mark.gpu
 
 def _gemm_case(M, N, K, ak, bk, seed):
     g = torch.Generator().manual_seed(seed)
-    A = torch.randn(M, K, generator=g).bfloat16()
-    B = torch.randn(N, K, generator=g).bfloat16()
+    A = torch.randn(M, K, generator=g, dtype=torch.float32).bfloat16()
+    B = torch.randn(N, K, generator=g, dtype=torch.float32).bfloat16()
     a_mem = A if ak else A.t().contiguous()
     b_mem = B if bk else B.t().contiguous()
     lda = K if ak else M
@@ -34,9 +34,9 @@ SHAPES = [(128, 128, 64), (256, 512, 128), (384, 768, 768), (200, 96, 80), (136,
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_gemm_bf16_fp32_out(M, N, K, ak, bk):
     a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, M * 7 + N * 3 + K + 10 * ak + bk)
-    out = torch.full((M, N), float("nan"), device="cuda")
+    out = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, out_f32=out)
-    torch.cuda.synchronize()
+    gpt2.op_sync()
     got = out.cpu().double().numpy()
     # fp32 accumulation of exact bf16 products: error ~ sqrt(K) * 2^-24 * |terms|
     assert np.abs(got - ref).max() <= 1e-4 * math.sqrt(K) * 4, (M, N, K, ak, bk)
@@ -46,12 +46,12 @@ def test_gemm_bf16_fp32_out(M, N, K, ak, bk):
 def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk):
     M, N, K = 320, 384, 256
     a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, 5)
-    bias = torch.randn(N).cuda()
+    bias = torch.randn(N, dtype=torch.float32).cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, bias=bias, out_bf16=out)
-    acc = torch.ones(M, N, device="cuda")
+    acc = torch.ones(M, N, dtype=torch.float32, device="cuda")
     gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, out_f32=acc, accumulate=True)
-    torch.cuda.synchronize()
+    gpt2.op_sync()
     r = ref + bias.cpu().double().numpy()[None, :]
     got = out.cpu().double().numpy()
     assert np.all(np.abs(got - r) <= 2 ** -8 * np.abs(r) + 1e-3 * math.sqrt(K))
@@ -60,8 +60,8 @@ def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk):
 
 def _attn_inputs(B, T, H, hs, seed, dtype):
     g = torch.Generator().manual_seed(seed)
-    qkv = torch.randn(B * T, 3 * H * hs, generator=g)
-    dout = torch.randn(B * T, H * hs, generator=g)
+    qkv = torch.randn(B * T, 3 * H * hs, generator=g, dtype=torch.float32)
+    dout = torch.randn(B * T, H * hs, generator=g, dtype=torch.float32)
     if dtype == torch.bfloat16:
         qkv, dout = qkv.bfloat16(), dout.bfloat16()
     return qkv, dout
@@ -90,12 +90,12 @@ def test_attention_fwd_bwd(precision, B, T, H):
     C = H * hs
     q_d, do_d = qkv.cuda(), dout.cuda()
     out = torch.empty(B * T, C, dtype=dt, device="cuda")
-    lse = torch.empty(B * H * T, device="cuda")
+    lse = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
     dqkv = torch.empty(B * T, 3 * C, dtype=dt, device="cuda")
-    scratch = torch.empty(B * H * T, device="cuda")
+    scratch = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
     gpt2.op_attention_fwd(precision, B, T, H, hs, q_d, out, lse)
     gpt2.op_attention_bwd(precision, B, T, H, hs, q_d, out, lse, do_d, dqkv, scratch)
-    torch.cuda.synchronize()
+    gpt2.op_sync()
     o = out.float().cpu().double().numpy()
     l = lse.cpu().double().numpy()
     d = dqkv.float().cpu().double().numpy()
@@ -114,6 +114,6 @@ def test_attention_fwd_bwd(precision, B, T, H):
 def test_attention_rejects_unsupported_head_size():
     qkv = torch.zeros(64, 3 * 96, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(64, 96, dtype=torch.bfloat16, device="cuda")
-    lse = torch.zeros(64, device="cuda")
+    lse = torch.zeros(64, dtype=torch.float32, device="cuda")
     with pytest.raises(gpt2.GPT2Error):
         gpt2.op_attention_fwd(gpt2.GPT2_BF16, 1, 64, 1, 96, qkv, out, lse)

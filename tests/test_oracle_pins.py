@@ -25,7 +25,17 @@ import synthdata
 from oracle import gpt2_oracle as O
 from oracle import CONFIGS
 
-torch.set_default_dtype(torch.float64)
+
+
+@pytest.fixture(autouse=True)
+def _fp64_default():
+    """The library-routine pins below build fp64 torch tensors with default
+    dtypes; the default is set for each test of this module only and restored
+    afterwards, so other test modules keep torch's fp32 default."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def tiny(**kw):
