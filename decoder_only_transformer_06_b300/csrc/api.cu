@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -983,3 +984,67 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
 
 }  // extern "C"
 
+// ------------------------------------------------------- allocation-free variant
+// gpt2_op_attention_bwd_noalloc: the attention backward with its rowsum
+// scratch in a fixed, file-scope device array instead of a caller buffer, for
+// callers that cannot allocate device memory (a plugin inside a host that owns
+// the allocator and forbids cudaMalloc, code that runs while an allocator is
+// locked, or a host with a hard no-allocation policy after start-up).
+//
+// The array lives in every device that loads this library until the process
+// exits. Host code must not use its name as an address (on the host it is a
+// stand-in symbol), so each device's address is looked up once, with that
+// device current, by cudaGetSymbolAddress on the first call made on it.
+namespace {
+
+constexpr int64_t NOALLOC_ROWS_MAX = int64_t(1) << 20;   // B*H*T rows, 4 MiB of fp32
+__device__ __align__(256) float g_noalloc_rowsum[NOALLOC_ROWS_MAX];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of g_noalloc_rowsum on the current device (looked up once).
+cudaError_t noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_rowsum);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = (float*)p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int gpt2_op_attention_bwd_noalloc(int precision, int B, int T, int H, int hs,
+                                             const void* qkv, const void* out, const float* lse,
+                                             const void* dout, void* dqkv, void* stream) {
+    if (!qkv || !out || !lse || !dout || !dqkv || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
+        return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
+    if ((int64_t)B * H * T > NOALLOC_ROWS_MAX)
+        return fail(nullptr, GPT2_EINVAL,
+                    "B*H*T = " + std::to_string((int64_t)B * H * T) +
+                        " exceeds the fixed scratch of the allocation-free attention backward (" +
+                        std::to_string(NOALLOC_ROWS_MAX) + " rows)");
+    float* scratch = nullptr;
+    cudaError_t r = noalloc_scratch(&scratch);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "cudaGetSymbolAddress", r);
+    // every row of the scratch is written by the rowsum pass before any read,
+    // so stale contents from an earlier call need no clearing
+    if (precision == GPT2_BF16)
+        r = k::attention_bwd_bf16((const bf16*)qkv, (const bf16*)out, lse, (const bf16*)dout,
+                                  (bf16*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+    else
+        r = k::attention_bwd_f32((const float*)qkv, (const float*)out, lse, (const float*)dout,
+                                 (float*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+    if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");
+    if (r != cudaSuccess) return fail_cuda(nullptr, "attention_bwd_noalloc", r);
+    return GPT2_OK;
+}

@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_op_sync": (I, [P]),
         "gpt2_op_attention_fwd": (I, [I, I, I, I, I, P, P, P, P]),
         "gpt2_op_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
+        "gpt2_op_attention_bwd_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -312,3 +313,12 @@ def op_attention_bwd(precision, B, T, H, hs, qkv, out, lse, dout, dqkv, scratch,
     _check(_lib.gpt2_op_attention_bwd(precision, B, T, H, hs, ptr(qkv), ptr(out), ptr(lse),
                                       ptr(dout), ptr(dqkv), ptr(scratch), _stream_ptr(stream)))
 
+
+def op_attention_bwd_noalloc(precision, B, T, H, hs, qkv, out, lse, dout, dqkv, stream=None):
+    """gpt2_op_attention_bwd without a scratch argument: the library keeps the
+    rowsum scratch in a fixed device array of its own (B*H*T <= 2**20), for
+    callers that must not allocate device memory."""
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    _check(_lib.gpt2_op_attention_bwd_noalloc(precision, B, T, H, hs, ptr(qkv), ptr(out),
+                                              ptr(lse), ptr(dout), ptr(dqkv),
+                                              _stream_ptr(stream)))

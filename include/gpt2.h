@@ -258,6 +258,30 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
                           const void* out, const float* lse, const void* dout, void* dqkv,
                           float* scratch, void* stream);
 
+/* Allocation-free variant of gpt2_op_attention_bwd (this entry point has no
+ * counterpart on the pages: it exists for callers that may not allocate device
+ * memory themselves, e.g. a plugin whose host application owns every device
+ * allocation, or code bound by a no-cudaMalloc-after-start-up policy).
+ * Arguments, layouts and results are those of gpt2_op_attention_bwd without
+ * `scratch`: the fp32 rowsum(dout*out) scratch instead lives in a fixed array
+ * of 2^20 floats (4 MiB) compiled into the library, which every device that
+ * loads the library holds until the process exits. The caller still owns and
+ * passes qkv, out, lse, dout and dqkv.
+ *  - B*H*T must be <= 2^20 (1,048,576): larger sizes return GPT2_EINVAL with a
+ *    message in gpt2_last_error(NULL), before any device work.
+ *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call outside any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents (each call rewrites every row it reads, so no clearing is
+ *    needed). Calls that may overlap on the GPU (different streams, no ordering
+ *    between them) race on it: order them on one stream or with events.
+ * Return codes as gpt2_op_attention_bwd. */
+int gpt2_op_attention_bwd_noalloc(int precision, int B, int T, int H, int hs, const void* qkv,
+                                  const void* out, const float* lse, const void* dout,
+                                  void* dqkv, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
