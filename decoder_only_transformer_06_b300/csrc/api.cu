@@ -37,7 +37,7 @@ struct LayerActs {
     void* u2;
     float* mu2;
     float* rs2;
-    void* hpre;       // fc output before GELU (act [M,4C])
+    void* hpre;       // gelu'(fc output), saved for the backward (act [M,4C])
     void* hgel;       // after GELU
 };
 
@@ -77,6 +77,7 @@ struct gpt2_model {
     void* du = nullptr;
     void* dqkv = nullptr;
     void* datt = nullptr;
+    void* yproj = nullptr;   // output of a residual-branch projection (act [M,C]), forward only
     void* dh = nullptr;
     float* Dbuf = nullptr;
     float* ln_partial = nullptr;
@@ -337,6 +338,7 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     ALLOC(m, m->du, M * C * A);
     ALLOC(m, m->dqkv, M * 3 * C * A);
     ALLOC(m, m->datt, M * C * A);
+    ALLOC(m, m->yproj, M * C * A);
     ALLOC(m, m->dh, M * 4 * C * A);
     ALLOC(m, m->Dbuf, M * m->H * 4);
     ALLOC(m, m->ln_partial, k::layernorm_bwd_partial_floats(m->M, m->C) * 4);
@@ -516,43 +518,54 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
     RUN(m, "validate", 1, 0, 8.0 * M, k::validate_inputs(tok, tgt, M, m->V, m->st, m->accum, s));
     RUN(m, "embed_fwd", 1, 0, 4.0 * M + 12.0 * MC,
         k::embed_fwd(tok, m->P(0), m->P(1), m->la[0].x_in, M, T, C, m->V, s));
+    // LayerNorm: read x, write u, mu, rstd; fused residual add: also read y, write x
     const double ln_bytes = MC * (4 + A) + 8.0 * M;
+    const double add_ln_bytes = ln_bytes + MC * (A + 4);
+    RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
+        k::layernorm_fwd<Act>(m->la[0].x_in, nullptr, nullptr, m->P(m->lt(0, T_LN1G)),
+                              m->P(m->lt(0, T_LN1B)), (Act*)m->la[0].u1, m->la[0].mu1, m->la[0].rs1,
+                              M, C, s));
     for (int l = 0; l < L; l++) {
         LayerActs& a = m->la[l];
-        float* x_next = (l + 1 < L) ? m->la[l + 1].x_in : m->x_final;
-        RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
-            k::layernorm_fwd<Act>(a.x_in, m->P(m->lt(l, T_LN1G)), m->P(m->lt(l, T_LN1B)), (Act*)a.u1,
-                                  a.mu1, a.rs1, M, C, s));
         {
             GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_ATTB)), a.qkv, 3 * C, nullptr, 0, nullptr, 0};
             OPR(op.gemm("gemm_qkv_fwd", M, 3 * C, C, {a.u1, C, true}, {m->W(m->lt(l, T_ATTW)), C, true}, e));
         }
         if (m->use_bf16)
             RUN(m, "attention_fwd", 1, attn_flops(m, 2), MC * A * 4,
-                k::attention_fwd_bf16((const bf16*)a.qkv, (bf16*)a.att, a.lse, B, T, H, m->hs, s));
+                k::attention_fwd_bf16((const bf16*)a.qkv, (bf16*)a.att, a.lse, B, T, H, m->hs, m->st, s));
         else
             RUN(m, "attention_fwd", 1, attn_flops(m, 2), MC * A * 4,
                 k::attention_fwd_f32((const float*)a.qkv, (float*)a.att, a.lse, B, T, H, m->hs, s));
         {
-            GemmEpi e{EPI_RESID, m->P(m->lt(l, T_APB)), a.x_mid, C, nullptr, 0, a.x_in, C};
+            // y = att W_ap^T + b_ap; x_mid = x_in + y fused into ln_2
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_APB)), m->yproj, C, nullptr, 0, nullptr, 0};
             OPR(op.gemm("gemm_attproj_fwd", M, C, C, {a.att, C, true}, {m->W(m->lt(l, T_APW)), C, true}, e));
         }
-        RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
-            k::layernorm_fwd<Act>(a.x_mid, m->P(m->lt(l, T_LN2G)), m->P(m->lt(l, T_LN2B)), (Act*)a.u2,
-                                  a.mu2, a.rs2, M, C, s));
+        RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
+            k::layernorm_fwd<Act>(a.x_in, (const Act*)m->yproj, a.x_mid, m->P(m->lt(l, T_LN2G)),
+                                  m->P(m->lt(l, T_LN2B)), (Act*)a.u2, a.mu2, a.rs2, M, C, s));
         {
             GemmEpi e{EPI_GELU, m->P(m->lt(l, T_FCB)), a.hpre, 4 * C, a.hgel, 4 * C, nullptr, 0};
             OPR(op.gemm("gemm_fc_fwd", M, 4 * C, C, {a.u2, C, true}, {m->W(m->lt(l, T_FCW)), C, true}, e));
         }
         {
-            GemmEpi e{EPI_RESID, m->P(m->lt(l, T_MPB)), x_next, C, nullptr, 0, a.x_mid, C};
+            // y = gelu(h) W_mp^T + b_mp; the next residual x_mid + y is fused into
+            // the next block's ln_1 (or ln_f)
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_MPB)), m->yproj, C, nullptr, 0, nullptr, 0};
             OPR(op.gemm("gemm_mlpproj_fwd", M, C, 4 * C, {a.hgel, 4 * C, true},
                         {m->W(m->lt(l, T_MPW)), 4 * C, true}, e));
         }
+        if (l + 1 < L) {
+            LayerActs& n = m->la[l + 1];
+            RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
+                k::layernorm_fwd<Act>(a.x_mid, (const Act*)m->yproj, n.x_in, m->P(m->lt(l + 1, T_LN1G)),
+                                      m->P(m->lt(l + 1, T_LN1B)), (Act*)n.u1, n.mu1, n.rs1, M, C, s));
+        }
     }
-    RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
-        k::layernorm_fwd<Act>(m->x_final, m->P(m->lnf_g()), m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf,
-                              m->rsf, M, C, s));
+    RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
+        k::layernorm_fwd<Act>(m->la[L - 1].x_mid, (const Act*)m->yproj, m->x_final, m->P(m->lnf_g()),
+                              m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf, m->rsf, M, C, s));
     {
         // tied LM head: logits = uf wte^T over all Vp rows of wte (pad columns
         // are masked by the cross-entropy)
@@ -957,7 +970,8 @@ int gpt2_op_attention_fwd(int precision, int B, int T, int H, int hs, const void
         return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
     cudaError_t r;
     if (precision == GPT2_BF16)
-        r = k::attention_fwd_bf16((const bf16*)qkv, (bf16*)out, lse, B, T, H, hs, (cudaStream_t)stream);
+        r = k::attention_fwd_bf16((const bf16*)qkv, (bf16*)out, lse, B, T, H, hs, op_state(),
+                                  (cudaStream_t)stream);
     else
         r = k::attention_fwd_f32((const float*)qkv, (float*)out, lse, B, T, H, hs, (cudaStream_t)stream);
     if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");

@@ -38,9 +38,9 @@ struct GemmOperand {
 // GEMM epilogues. D[m,n] = acc[m,n] = sum_k A(m,k) B(n,k).
 enum EpiKind : int {
     EPI_STORE_ACT = 0,   // out_act[m,n]  = acc + bias[n]
-    EPI_GELU = 1,        // out_act[m,n]  = pre = acc + bias[n]; out2_act[m,n] = gelu(pre)
-    EPI_RESID = 2,       // out_f32[m,n]  = resid_f32[m,n] + acc + bias[n]
-    EPI_GELU_BWD = 3,    // out_act[m,n]  = acc * gelu'(pre_act[m,n])
+    EPI_GELU = 1,        // pre = acc + bias[n]; out_act[m,n] = gelu'(pre); out2_act[m,n] = gelu(pre)
+    EPI_RESID = 2,       // out_f32[m,n]  = resid_f32[m,n] + acc + bias[n] (fp32 SIMT GEMM only)
+    EPI_GELU_BWD = 3,    // out_act[m,n]  = acc * aux_act[m,n] (aux: the gelu'(pre) saved by EPI_GELU)
     EPI_ACCUM_F32 = 4,   // out_f32[m,n] += acc
     EPI_STORE_F32 = 5,   // out_f32[m,n]  = acc + bias[n]
 };
@@ -52,13 +52,15 @@ struct GemmEpi {
     int64_t ldo;
     void* out2;            // EPI_GELU post-activation output (act)
     int64_t ldo2;
-    const void* aux;       // EPI_RESID: f32 residual input; EPI_GELU_BWD: act pre-activation
+    const void* aux;       // EPI_RESID: f32 residual input; EPI_GELU_BWD: act gelu'(pre)
     int64_t ld_aux;
 };
 
 #define CUDA_OK(expr) do { cudaError_t e__ = (expr); if (e__ != cudaSuccess) return e__; } while (0)
 
-// tanh-form GELU (Hendrycks & Gimpel) and its derivative, fp32.
+// tanh-form GELU (Hendrycks & Gimpel) and its derivative, fp32. The forward
+// Linear that applies GELU saves gelu'(pre) (not pre): the backward then only
+// multiplies by it.
 __device__ __forceinline__ float gelu_f(float x) {
     const float a = 0.7978845608028654f, c = 0.044715f;
     float t = tanhf(a * (x + c * x * x * x));
@@ -114,9 +116,12 @@ size_t embed_bwd_workspace(int M, int C);
 cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
                       int C, int V, void* workspace, cudaStream_t s);
 
+// u = LN(x') with x' = x, or x' = x + y written to x_out when y != nullptr
+// (the residual add of the preceding branch fused into the LayerNorm).
 template <typename Act>
-cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u, float* mu,
-                          float* rstd, int M, int C, cudaStream_t s);
+cudaError_t layernorm_fwd(const float* x, const Act* y, float* x_out, const float* g,
+                          const float* b, Act* u, float* mu, float* rstd, int M, int C,
+                          cudaStream_t s);
 // dres (+)= LN backward of du; dres_act = Act copy of the new dres;
 // dg, db += parameter gradients; dsum (optional) += column sums of the new
 // dres (the bias gradient of the Linear whose output gradient it is). All
@@ -154,8 +159,9 @@ cudaError_t attention_fwd_f32(const float* qkv, float* out, float* lse, int B, i
 cudaError_t attention_bwd_f32(const float* qkv, const float* out, const float* lse,
                               const float* dout, float* dqkv, float* Dbuf, int B, int T, int H,
                               int hs, cudaStream_t s);
+// tcgen05 flash attention (head size 64); bounded waits report into st
 cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
-                               cudaStream_t s);
+                               DevState* st, cudaStream_t s);
 cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* lse,
                                const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,
                                int hs, cudaStream_t s);

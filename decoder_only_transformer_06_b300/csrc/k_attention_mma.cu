@@ -1,15 +1,16 @@
-// Causal flash attention, bf16 operands / fp32 softmax and accumulation,
-// head size 64, on warp-level mma.sync (m16n8k16) tensor-core instructions.
+// Causal flash attention BACKWARD, bf16 operands / fp32 softmax and
+// accumulation, head size 64, on warp-level mma.sync (m16n8k16) tensor-core
+// instructions (the forward runs on tcgen05: k_attention_tc.cu).
 //
 // Semantics: the manual attention of nanoGPT's CausalSelfAttention (nanoGPT
 // guide Deep dive 1): S = q k^T / sqrt(hs), keys j > i masked to -inf before
-// the softmax, o = softmax(S) v. The T x T scores never leave the chip: an
-// online softmax runs over 64-key blocks ("Let's reproduce GPT-2" 02:00:18,
-// Flash Attention; nixfred "Flash attention").
+// the softmax, o = softmax(S) v. The probabilities are recomputed from the
+// forward's per-row lse ("Let's reproduce GPT-2" 02:00:18, Flash Attention;
+// nixfred "Flash attention"), so the T x T matrices never leave the chip.
 //
-// Forward: CTA = 64 queries of one (b, h), 4 warps x 16 query rows; K/V blocks
-// double-buffered through 128B-XOR-swizzled shared memory with cp.async.
-// Backward (deterministic, no atomics): rowsum(dO*O) pre-pass; one kernel
+// K/V and Q/dO blocks of 64 rows are double-buffered through 128B-XOR-swizzled
+// shared memory with cp.async; 4 warps x 16 rows per CTA.
+// Deterministic (no atomics): rowsum(dO*O) pre-pass; one kernel
 // accumulates dK/dV per 64-key block over the query blocks that see it;
 // another accumulates dQ per 64-query block over the key blocks it sees.
 // Layout as in the fp32 kernels: qkv [B*T, 3C], out [B*T, C], lse [B,H,T].
@@ -149,109 +150,6 @@ __device__ __forceinline__ void store_acc(const float (&acc)[8][4], bf16* g, int
             *(uint32_t*)(g + (int64_t)ra * ld + col) = pack2(acc[nt][0] * scale, acc[nt][1] * scale);
         if (rb < nvalid)
             *(uint32_t*)(g + (int64_t)rb * ld + col) = pack2(acc[nt][2] * scale, acc[nt][3] * scale);
-    }
-}
-
-// ------------------------------------------------------------------ forward
-__global__ void __launch_bounds__(FA_THREADS)
-fa_fwd_kernel(const bf16* __restrict__ qkv, bf16* __restrict__ out, float* __restrict__ lse, int T,
-              int H) {
-    __shared__ __align__(128) bf16 sQ[FA_BLK * FA_HS];
-    __shared__ __align__(128) bf16 sK[2][FA_BLK * FA_HS];
-    __shared__ __align__(128) bf16 sV[2][FA_BLK * FA_HS];
-    const int nqb = (T + FA_BLK - 1) / FA_BLK;
-    const int qb = nqb - 1 - blockIdx.x;        // heaviest blocks first
-    const int bh = blockIdx.y, h = bh % H, b = bh / H;
-    const int C = H * FA_HS;
-    const int64_t ld = 3 * C;
-    const bf16* base = qkv + (int64_t)b * T * ld;
-    const bf16* qg = base + h * FA_HS;
-    const bf16* kg = base + C + h * FA_HS;
-    const bf16* vg = base + 2 * C + h * FA_HS;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
-    const float sl2 = LOG2E / sqrtf((float)FA_HS);
-
-    load_tile(sQ, qg, ld, qb * FA_BLK, T);
-    load_tile(sK[0], kg, ld, 0, T);
-    load_tile(sV[0], vg, ld, 0, T);
-    cp_commit();
-
-    uint32_t qf[4][4];
-    float o[8][4];
-    zero8x4(o);
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    const int qrow0 = qb * FA_BLK + warp * 16 + gq;
-
-    for (int kb = 0; kb <= qb; kb++) {
-        const int buf = kb & 1;
-        if (kb + 1 <= qb) {
-            load_tile(sK[buf ^ 1], kg, ld, (kb + 1) * FA_BLK, T);
-            load_tile(sV[buf ^ 1], vg, ld, (kb + 1) * FA_BLK, T);
-        }
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        if (kb == 0) load_a_frags(sQ, warp * 16, qf);
-
-        float s[8][4];
-        zero8x4(s);
-        mma_a_xt(s, qf, sK[buf]);
-
-        const bool need_mask = (kb == qb) || ((kb + 1) * FA_BLK > T);
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float v = s[nt][e] * sl2;
-                if (need_mask) {
-                    int key = kb * FA_BLK + nt * 8 + 2 * t + (e & 1);
-                    int row = qrow0 + ((e >> 1) << 3);
-                    if (key > row || key >= T) v = -INFINITY;
-                }
-                s[nt][e] = v;
-                mx[e >> 1] = fmaxf(mx[e >> 1], v);
-            }
-        }
-        float corr[2];
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            float mn = fmaxf(mrow[r], mx[r]);
-            corr[r] = exp2f(mrow[r] - mn);
-            mrow[r] = mn;
-            lrow[r] *= corr[r];
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; nt++) {
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                float p = exp2f(s[nt][e] - mrow[e >> 1]);
-                s[nt][e] = p;
-                lrow[e >> 1] += p;
-                o[nt][e] *= corr[e >> 1];
-            }
-        }
-        mma_p_x(o, s, sV[buf]);
-        __syncthreads();
-    }
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-        lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-    const float inv0 = 1.f / lrow[0], inv1 = 1.f / lrow[1];
-#pragma unroll
-    for (int nt = 0; nt < 8; nt++) {
-        o[nt][0] *= inv0; o[nt][1] *= inv0;
-        o[nt][2] *= inv1; o[nt][3] *= inv1;
-    }
-    store_acc(o, out + (int64_t)b * T * C + h * FA_HS, C, qb * FA_BLK + warp * 16, T, 1.f);
-    if (t == 0) {
-        float* lr = lse + (int64_t)bh * T;
-        if (qrow0 < T) lr[qrow0] = (mrow[0] + log2f(lrow[0])) / LOG2E;
-        if (qrow0 + 8 < T) lr[qrow0 + 8] = (mrow[1] + log2f(lrow[1])) / LOG2E;
     }
 }
 
@@ -468,14 +366,6 @@ fa_bwd_dq_kernel(const bf16* __restrict__ qkv, const bf16* __restrict__ dout,
 }
 
 bool attention_bf16_supported(int T, int hs) { return hs == FA_HS && T >= 1; }
-
-cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
-                               cudaStream_t s) {
-    if (!attention_bf16_supported(T, hs)) return cudaErrorInvalidValue;
-    dim3 grid((T + FA_BLK - 1) / FA_BLK, B * H);
-    fa_fwd_kernel<<<grid, FA_THREADS, 0, s>>>(qkv, out, lse, T, H);
-    return cudaGetLastError();
-}
 
 cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* lse,
                                const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,

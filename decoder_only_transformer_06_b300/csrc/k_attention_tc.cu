@@ -1,0 +1,369 @@
+// Causal flash attention forward on the 5th-generation tensor cores (tcgen05,
+// sm_103a): bf16 q, k, v, fp32 scores and output accumulation in tensor memory.
+//
+// Semantics: the manual attention of nanoGPT's CausalSelfAttention (nanoGPT
+// guide Deep dive 1): S = q k^T / sqrt(hs), keys j > i masked to -inf before
+// the softmax, o = softmax(S) v; the T x T scores never leave the chip (online
+// softmax over key blocks: "Let's reproduce GPT-2" 02:00:18, Flash Attention).
+// Also writes lse = log sum_j exp(S_ij) per query for the backward.
+//
+// One CTA per (128-query block, b, h); 192 threads:
+//   warps 0..3  softmax: one thread per query row (= its TMEM lane). Reads the
+//               row of S from TMEM, masks, tracks the running max, writes
+//               P = exp(S - max) in bf16 to shared memory as the A operand of
+//               the P V product, rescales the O row in TMEM when the max grew
+//               by more than 2^8 (otherwise P may exceed 1 by up to 2^8, which
+//               the final division by the row sum absorbs exactly).
+//   warp 4      TMA producer: Q once, then K and V blocks of 128 keys into
+//               three-slot rings (separate K and V slots so a K slot frees as
+//               soon as its S product is done).
+//   warp 5      allocates 512 TMEM columns (S double buffer 2x128, O 64);
+//               lane 0 issues S_j = Q K_j^T (M=128, N=128, K=64) into S[j%2]
+//               and O += P_{j-1} V_{j-1} (M=128, N=64, K=128), so the tensor
+//               core computes S_{j+1} and P_{j-1} V_{j-1} while the softmax
+//               works on S_j.
+// Every mbarrier wait is bounded; on expiry the CTA records ERR_TIMEOUT,
+// drains its copies and MMAs (bounded), frees TMEM and returns.
+#include "common.cuh"
+#include "tc.cuh"
+#include <cuda.h>
+#include <cstring>
+
+namespace k {
+
+using namespace tc;
+
+namespace {
+
+constexpr int AT_BQ = 128;                     // queries per CTA
+constexpr int AT_BK = 128;                     // keys per block
+constexpr int AT_HS = 64;                      // head size
+constexpr int AT_SLOTS = 3;                    // K and V ring depth
+constexpr int AT_TILE = AT_BQ * AT_HS * 2;     // 16 KB: 128 rows x 128 B
+constexpr int AT_P_BYTES = AT_BQ * AT_BK * 2;  // 32 KB
+constexpr int AT_THREADS = 192;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + AT_TILE;
+constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
+constexpr int OFF_P = OFF_V + AT_SLOTS * AT_TILE;
+constexpr int OFF_BAR = OFF_P + 2 * AT_P_BYTES;
+constexpr size_t AT_SMEM = OFF_BAR + 256 + 1024;
+constexpr uint32_t TM_O = 256;                 // S[0] at 0, S[1] at 128
+constexpr uint32_t AT_TMEM_COLS = 512;
+constexpr float LN2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *(uint32_t*)&h;
+}
+__device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
+    const long long t0 = wait_clock();
+    while (!mbar_try_wait(bar, parity) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ out,
+                 float* __restrict__ lse, int T, int H, DevState* st) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem + OFF_Q;
+    uint8_t* sK = smem + OFF_K;
+    uint8_t* sV = smem + OFF_V;
+    uint8_t* sP = smem + OFF_P;
+    uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = bars + 4;
+    uint64_t* v_full = bars + 7;
+    uint64_t* v_empty = bars + 10;
+    uint64_t* s_full = bars + 13;
+    uint64_t* s_empty = bars + 15;
+    uint64_t* p_full = bars + 17;
+    uint64_t* pv_done = bars + 19;
+    uint64_t* drain = bars + 21;
+    uint32_t* tmem_slot = (uint32_t*)(bars + 22);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int nqb = (T + AT_BQ - 1) / AT_BQ;
+    const int qb = nqb - 1 - (int)blockIdx.x;     // heaviest query blocks first
+    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int C = H * AT_HS;
+    const int nkv = qb + 1;                       // causal: key blocks 0..qb
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < AT_SLOTS; s++) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            mbar_arrive_expect_tx(q_full, AT_TILE);
+            tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, qb * AT_BQ, b);
+            int nk = 0, nv = 0;
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; j++) {
+                const int s = j % AT_SLOTS;
+                const uint32_t ph = (uint32_t)((j / AT_SLOTS) & 1);
+                if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&k_full[s], AT_TILE);
+                tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
+                nk++;
+                if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&v_full[s], AT_TILE);
+                tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                nv++;
+            }
+            if (!ok || *abort_flag) {
+                // wait (bounded) for every copy still in flight before the CTA exits
+                wait_bounded(q_full, 0);
+                for (int j = (nk > AT_SLOTS ? nk - AT_SLOTS : 0); j < nk; j++)
+                    wait_bounded(&k_full[j % AT_SLOTS], (uint32_t)((j / AT_SLOTS) & 1));
+                for (int j = (nv > AT_SLOTS ? nv - AT_SLOTS : 0); j < nv; j++)
+                    wait_bounded(&v_full[j % AT_SLOTS], (uint32_t)((j / AT_SLOTS) & 1));
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
+            constexpr uint32_t id_o = make_idesc(AT_BQ, AT_HS, false, true);
+            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV),
+                           p_addr = smem_u32(sP);
+            bool ok = mbar_wait(q_full, 0, abort_flag);
+            bool any = false;
+            for (int j = 0; j <= nkv && ok; j++) {
+                if (j < nkv) {
+                    const int s = j % AT_SLOTS, sb = j & 1;
+                    if (!mbar_wait(&k_full[s], (uint32_t)((j / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&s_empty[sb], (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_HS / 16; kk++)
+                        mma_bf16(tmem_base + (uint32_t)(sb * AT_BK), smem_desc(q_addr + 32 * kk, 16, 1024),
+                                 smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                    mma_commit(&s_full[sb]);
+                    mma_commit(&k_empty[s]);
+                    any = true;
+                }
+                if (j >= 1) {
+                    const int i = j - 1, s = i % AT_SLOTS, pb = i & 1;
+                    if (!mbar_wait(&v_full[s], (uint32_t)((i / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&p_full[pb], (uint32_t)((i >> 1) & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_BK / 16; kk++) {
+                        const uint32_t a = p_addr + pb * AT_P_BYTES + (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t bb = v_addr + s * AT_TILE + kk * 2048;
+                        mma_bf16(tmem_base + TM_O, smem_desc(a, 16, 1024), smem_desc(bb, 8192, 1024), id_o,
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&pv_done[pb]);
+                    mma_commit(&v_empty[s]);
+                }
+            }
+            if (any) {
+                mma_commit(drain);
+                wait_bounded(drain, 0);
+            }
+        }
+    } else {
+        // ---------------- softmax warps 0..3: thread r owns query row r (TMEM lane r)
+        const int r = threadIdx.x;
+        const int q = qb * AT_BQ + r;
+        const float sl2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
+        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; j++) {
+            const int sb = j & 1;
+            ok = mbar_wait(&s_full[sb], (uint32_t)((j >> 1) & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[128];
+#pragma unroll
+            for (int c = 0; c < 4; c++) tmem_ld32_nowait(lane_base + (uint32_t)(sb * AT_BK + 32 * c), sr + 32 * c);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[sb]);
+            // mask (raw scores; the scale is applied in the exponent), row max
+            // as eight independent partial maxima
+            const int key0 = j * AT_BK;
+            const bool edge = (j == qb) || (key0 + AT_BK > T);
+            if (edge) {
+#pragma unroll
+                for (int i = 0; i < 128; i++)
+                    if (key0 + i > q || key0 + i >= T) sr[i] = __float_as_uint(-INFINITY);
+            }
+            float pm[8];
+#pragma unroll
+            for (int t = 0; t < 8; t++) pm[t] = __uint_as_float(sr[t]);
+#pragma unroll
+            for (int i = 8; i < 128; i++) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sr[i]));
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl2;
+            const float m_new = fmaxf(m_run, mx);
+            const bool resc = (j > 0) && (m_new > m_run + 8.f);
+            if (j == 0) m_run = m_new;
+            if (__any_sync(0xffffffffu, resc)) {
+                // rescale the O row once the previous P V product has landed
+                ok = mbar_wait(&pv_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const float f = resc ? ex2f(m_run - m_new) : 1.f;
+                uint32_t o[64];
+                tmem_ld32_nowait(lane_base + TM_O, o);
+                tmem_ld32_nowait(lane_base + TM_O + 32, o + 32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 64; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                tmem_st32(lane_base + TM_O, o);
+                tmem_st32(lane_base + TM_O + 32, o + 32);
+                if (resc) {
+                    l_run *= f;
+                    m_run = m_new;
+                }
+            }
+            // the P buffer is free once the product that read it (two blocks ago) is done
+            if (j >= 2) {
+                ok = mbar_wait(&pv_done[sb], (uint32_t)(((j - 2) >> 1) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            }
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint8_t* pbuf = sP + sb * AT_P_BYTES + r * 128;
+#pragma unroll
+            for (int kb2 = 0; kb2 < 2; kb2++) {
+#pragma unroll
+                for (int pq = 0; pq < 8; pq++) {
+                    float e[8];
+#pragma unroll
+                    for (int t = 0; t < 8; t++) {
+                        e[t] = ex2f(fmaf(__uint_as_float(sr[kb2 * 64 + pq * 8 + t]), sl2, -m_run));
+                        ps[t] += e[t];
+                    }
+                    uint4 w = make_uint4(pack2_bf16(e[0], e[1]), pack2_bf16(e[2], e[3]),
+                                         pack2_bf16(e[4], e[5]), pack2_bf16(e[6], e[7]));
+                    *(uint4*)(pbuf + kb2 * 16384 + ((pq ^ (r & 7)) << 4)) = w;
+                }
+            }
+            const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            l_run += sum;
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+        }
+        if (ok) {
+            ok = mbar_wait(&pv_done[(nkv - 1) & 1], (uint32_t)(((nkv - 1) >> 1) & 1), abort_flag);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                uint32_t o[64];
+                tmem_ld32_nowait(lane_base + TM_O, o);
+                tmem_ld32_nowait(lane_base + TM_O + 32, o + 32);
+                tmem_wait_ld();
+                if (q < T) {
+                    const float inv = 1.f / l_run;
+                    uint4* orow = (uint4*)(out + ((int64_t)b * T + q) * C + h * AT_HS);
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        const float* f = (const float*)&o[8 * c];
+                        orow[c] = make_uint4(pack2_bf16(f[0] * inv, f[1] * inv), pack2_bf16(f[2] * inv, f[3] * inv),
+                                             pack2_bf16(f[4] * inv, f[5] * inv), pack2_bf16(f[6] * inv, f[7] * inv));
+                    }
+                    lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        atomicOr(&st->err, ERR_TIMEOUT);
+        st->timeout_site = 3;
+    }
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, AT_TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFnA)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFnA encode_fn() {
+    static EncodeTiledFnA fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFnA)p;
+    }
+    return fn;
+}
+
+// qkv [B, T, 3C] bf16 as a 3-D map {3C, T, B}: rows beyond T of a sequence
+// read as zeros (never the next sequence's rows). Boxes of 64 x 128 x 1 with
+// 128B swizzle: the K-major operand layout of the tcgen05 descriptors.
+static bool make_qkv_map(CUtensorMap* map, const bf16* qkv, int B, int T, int C) {
+    EncodeTiledFnA enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)3 * C * 2 * T};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bf16*>(qkv), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
+                               DevState* st, cudaStream_t s) {
+    if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
+    if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
+    CUtensorMap map;
+    memset(&map, 0, sizeof map);
+    if (!make_qkv_map(&map, qkv, B, T, H * hs)) return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        CUDA_OK(cudaFuncSetAttribute(fa_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AT_SMEM));
+        attr = true;
+    }
+    dim3 grid((T + AT_BQ - 1) / AT_BQ, B * H);
+    fa_tc_fwd_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, st);
+    return cudaGetLastError();
+}
+
+}  // namespace k

@@ -62,7 +62,7 @@ gemm_f32_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda, b
                     break;
                 case EPI_GELU: {
                     float pre = v + bias;
-                    ((float*)epi.out)[(int64_t)m * epi.ldo + n] = pre;
+                    ((float*)epi.out)[(int64_t)m * epi.ldo + n] = gelu_grad_f(pre);
                     ((float*)epi.out2)[(int64_t)m * epi.ldo2 + n] = gelu_f(pre);
                     break;
                 }
@@ -72,7 +72,7 @@ gemm_f32_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda, b
                     break;
                 case EPI_GELU_BWD:
                     ((float*)epi.out)[(int64_t)m * epi.ldo + n] =
-                        v * gelu_grad_f(((const float*)epi.aux)[(int64_t)m * epi.ld_aux + n]);
+                        v * ((const float*)epi.aux)[(int64_t)m * epi.ld_aux + n];
                     break;
                 case EPI_ACCUM_F32:
                     ((float*)epi.out)[(int64_t)m * epi.ldo + n] += v;

@@ -1,8 +1,8 @@
 // bf16 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 //   D[m,n] = sum_k A(m,k) B(n,k), fp32 accumulation in tensor memory (TMEM),
-//   followed by a fused epilogue (bias, tanh-GELU, residual add, GELU
-//   backward, fp32 gradient accumulation).
+//   followed by a fused epilogue (bias, tanh-GELU, GELU backward, fp32
+//   gradient accumulation).
 //
 // Every Linear of the step maps onto this one routine (PyTorch layout
 // W[out,in], nanoGPT guide Deep dive 1):
@@ -15,8 +15,16 @@
 //   warp 0      TMA producer: 128B-swizzled tiles into a STAGES-deep ring
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16)
 //               and tcgen05.commit to free ring slots / publish accumulators
-//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half
-//               the columns: tcgen05.ld 32 at a time, fused math, stores
+//   warps 2..9  epilogue, two per TMEM lane quarter (32 rows of the tile, half
+//               the columns each): tcgen05.ld 32 columns at a time (one row
+//               per lane), fused math in registers, the result written to a
+//               swizzled shared-memory tile and sent out by one TMA store (or
+//               TMA reduce-add for the fp32 gradient). A second operand of the
+//               epilogue (the GELU derivative saved by the forward) arrives by
+//               TMA load, prefetched one chunk ahead.
+// Moving epilogue traffic through the TMA engine keeps the SM's load/store
+// and shared-memory pipes free for the operand stream of the main loop; with
+// per-lane global stores the epilogue, not the tensor pipe, set the pace.
 // Two TMEM accumulators (2*BN columns) let the epilogue of one tile overlap
 // the main loop of the next. Every mbarrier wait is bounded: on expiry the
 // CTA records ERR_TIMEOUT in the device status word, drains its in-flight
@@ -24,12 +32,16 @@
 #include "common.cuh"
 #include "tc.cuh"
 #include <cuda.h>
+#include <cstring>
 
 namespace k {
 
 using namespace tc;
 
 static constexpr int TC_BM = 128, TC_BK = 64;
+static constexpr int EPI_WARPS = 8;
+static constexpr int TC_THREADS = 32 * (2 + EPI_WARPS);
+static constexpr int EPI_WARP_BYTES = 4096;                 // one 32x32 fp32 tile per warp
 
 // Grouped tile order: 16 m-tiles per group, m fastest inside a group, so a
 // wave of CTAs shares A and B tiles through L2.
@@ -43,7 +55,7 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mt
     nt = r / gm;
 }
 
-// ------------------------------------------------------------------ epilogue
+// ------------------------------------------------------------------ epilogue math
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *(uint32_t*)&h;
@@ -56,18 +68,25 @@ __device__ __forceinline__ float tanh_hw(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float gelu_hw(float x) {
+// gelu(x) and gelu'(x) from one tanh
+__device__ __forceinline__ void gelu_and_grad_hw(float x, float& g, float& dg) {
     const float a = 0.7978845608028654f, c = 0.044715f;
-    return 0.5f * x * (1.0f + tanh_hw(a * (x + c * x * x * x)));
-}
-__device__ __forceinline__ float gelu_grad_hw(float x) {
-    const float a = 0.7978845608028654f, c = 0.044715f;
-    float t = tanh_hw(a * (x + c * x * x * x));
-    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * a * (1.0f + 3.0f * c * x * x);
+    const float t = tanh_hw(a * (x + c * x * x * x));
+    g = 0.5f * x * (1.0f + t);
+    dg = 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * a * (1.0f + 3.0f * c * x * x);
 }
 
-__device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32]) {
-    uint4* d = (uint4*)dst;
+// Staging tiles are laid out as the TMA expects them with swizzling, which
+// also makes the per-row writes (one row per lane) bank-conflict free:
+//   bf16 32x32 tile, 64 B rows, 64B swizzle: 16-byte piece q of row r sits at
+//     r*64 + ((q ^ ((r >> 1) & 3)) << 4)
+//   fp32 32x32 tile, 128 B rows, 128B swizzle: piece q of row r at
+//     r*128 + ((q ^ (r & 7)) << 4)
+__device__ __forceinline__ uint32_t sw64(int r, int q) { return r * 64 + ((q ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw128(int r, int q) { return r * 128 + ((q ^ (r & 7)) << 4); }
+
+// Row `lane` of a bf16 32x32 staging tile from 32 fp32 values.
+__device__ __forceinline__ void stage_bf16(uint8_t* tile, int lane, const float (&v)[32]) {
 #pragma unroll
     for (int q = 0; q < 4; q++) {
         uint4 w;
@@ -75,135 +94,64 @@ __device__ __forceinline__ void store_bf16_32(bf16* dst, const float (&v)[32]) {
         w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
         w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
         w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        d[q] = w;
+        *(uint4*)(tile + sw64(lane, q)) = w;
     }
 }
-
-// The epilogue works on 32 x 32 chunks per warp (32 TMEM lanes = rows, 32
-// fp32 columns). The chunk is staged through a 4 KB per-warp shared-memory
-// tile (16-byte groups XOR-swizzled by row, conflict-free both ways) so that
-// the fused math and every global load/store run in a coalesced layout: lane
-// l handles columns 4*(l%8)..+3 of rows l/8, l/8+4, ..., i.e. each warp
-// instruction covers 4 rows x 32 columns.
-__device__ __forceinline__ void stage_write(float* st, int lane, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void stage_f32(uint8_t* tile, int lane, const float (&v)[32]) {
 #pragma unroll
-    for (int c = 0; c < 8; c++)
-        *(uint4*)&st[lane * 32 + ((c ^ (lane & 7)) << 2)] =
-            make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+    for (int q = 0; q < 8; q++)
+        *(float4*)(tile + sw128(lane, q)) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
-__device__ __forceinline__ float4 stage_read(const float* st, int row, int q) {
-    return *(const float4*)&st[row * 32 + ((q ^ (row & 7)) << 2)];
-}
-
-__device__ __forceinline__ uint2 pack4_bf16(float4 v) {
-    return make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-}
-
-// Operand the epilogue reads besides the accumulator (residual fp32, GELU
-// pre-activation bf16, or the fp32 gradient it accumulates into): for one
-// chunk, lane l's 8 groups of 4 columns. Loaded one chunk ahead of its use.
-struct AuxBuf {
-    float4 f[8];
-};
-
-__device__ __forceinline__ void aux_load(const GemmEpi& e, int64_t m_base, int M, int n, int N,
-                                         int rsub, AuxBuf& a) {
-    const bool ncol = n < N;
-    if (e.kind == EPI_RESID || e.kind == EPI_ACCUM_F32) {
-        const float* src = (e.kind == EPI_RESID) ? (const float*)e.aux : (const float*)e.out;
-        const int64_t ld = (e.kind == EPI_RESID) ? e.ld_aux : e.ldo;
+__device__ __forceinline__ void unstage_bf16(const uint8_t* tile, int lane, float (&v)[32]) {
 #pragma unroll
-        for (int it = 0; it < 8; it++) {
-            const int64_t m = m_base + it * 4 + rsub;
-            a.f[it] = (ncol && m < M) ? *(const float4*)(src + m * ld + n) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    } else if (e.kind == EPI_GELU_BWD) {
-        const bf16* src = (const bf16*)e.aux;
+    for (int q = 0; q < 4; q++) {
+        uint4 w = *(const uint4*)(tile + sw64(lane, q));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int it = 0; it < 8; it++) {
-            const int64_t m = m_base + it * 4 + rsub;
-            uint2 w = (ncol && m < M) ? *(const uint2*)(src + m * e.ld_aux + n) : make_uint2(0u, 0u);
-            a.f[it] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), 0.f, 0.f);
-        }
-    }
-}
-
-// Apply the epilogue to one staged chunk: rows m_base..m_base+31, columns
-// n..n+3 for this lane (n = chunk start + 4*(lane%8)); N % 4 == 0.
-__device__ __forceinline__ void epilogue_chunk(const GemmEpi& e, const float* st, int64_t m_base,
-                                               int M, int n, int N, int rsub, int q,
-                                               const AuxBuf& a, int64_t split_off) {
-    if (n >= N) return;
-    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (e.bias && e.kind != EPI_ACCUM_F32 && e.kind != EPI_GELU_BWD) bias = __ldg((const float4*)(e.bias + n));
-#pragma unroll
-    for (int it = 0; it < 8; it++) {
-        const int row = it * 4 + rsub;
-        const int64_t m = m_base + row;
-        if (m >= M) continue;
-        float4 v = stage_read(st, row, q);
-        v.x += bias.x; v.y += bias.y; v.z += bias.z; v.w += bias.w;
-        switch (e.kind) {
-            case EPI_STORE_ACT:
-                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
-                break;
-            case EPI_GELU: {
-                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
-                float4 g = make_float4(gelu_hw(v.x), gelu_hw(v.y), gelu_hw(v.z), gelu_hw(v.w));
-                *(uint2*)((bf16*)e.out2 + m * e.ldo2 + n) = pack4_bf16(g);
-                break;
-            }
-            case EPI_RESID:
-            case EPI_ACCUM_F32: {
-                const float4 r = a.f[it];
-                v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
-                *(float4*)((float*)e.out + m * e.ldo + n) = v;
-                break;
-            }
-            case EPI_GELU_BWD: {
-                const uint32_t w0 = __float_as_uint(a.f[it].x), w1 = __float_as_uint(a.f[it].y);
-                float2 p0 = __bfloat1622float2(*(const __nv_bfloat162*)&w0);
-                float2 p1 = __bfloat1622float2(*(const __nv_bfloat162*)&w1);
-                v.x *= gelu_grad_hw(p0.x); v.y *= gelu_grad_hw(p0.y);
-                v.z *= gelu_grad_hw(p1.x); v.w *= gelu_grad_hw(p1.y);
-                *(uint2*)((bf16*)e.out + m * e.ldo + n) = pack4_bf16(v);
-                break;
-            }
-            case EPI_STORE_F32:
-                *(float4*)((float*)e.out + split_off + m * e.ldo + n) = v;
-                break;
+        for (int j = 0; j < 4; j++) {
+            float2 f = __bfloat1622float2(*(const __nv_bfloat162*)&u[j]);
+            v[8 * q + 2 * j] = f.x;
+            v[8 * q + 2 * j + 1] = f.y;
         }
     }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, bool A_MN, bool B_MN>
+template <int BN>
 struct TcCfg {
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
     static constexpr int B_BYTES = BN * TC_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int STAGING_BYTES = 8 * 32 * 32 * 4;   // 4 KB per epilogue warp
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + 256;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
 };
 
-template <int BN, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(320, 1)
+// Tensor maps of the epilogue: o1 (bf16 out / fp32 out / fp32 reduce target /
+// GELU derivative), o2 (GELU post-activation), aux (GELU derivative to read).
+struct EpiMaps {
+    CUtensorMap o1, o2, aux;
+};
+
+template <int BN, bool A_MN, bool B_MN, int KIND>
+__global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               int M, int N, int K, int splits, GemmEpi epi, DevState* st) {
-    using Cfg = TcCfg<BN, A_MN, B_MN>;
+               const __grid_constant__ EpiMaps maps, int M, int N, int K, int splits,
+               const float* __restrict__ bias, DevState* st) {
+    using Cfg = TcCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-    float* staging = (float*)(smem + STAGES * Cfg::STAGE_BYTES);
-    uint64_t* full = (uint64_t*)(smem + STAGES * Cfg::STAGE_BYTES + Cfg::STAGING_BYTES);
+    uint8_t* sEpi = smem + STAGES * Cfg::STAGE_BYTES;
+    uint64_t* full = (uint64_t*)(sEpi + Cfg::EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* auxbar = tempty + 2;              // [EPI_WARPS]
+    uint64_t* drain = auxbar + EPI_WARPS;
     uint32_t* tmem_slot = (uint32_t*)(drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -215,8 +163,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 8);
+            mbar_init(&tempty[a], EPI_WARPS);
         }
+        for (int i = 0; i < EPI_WARPS; i++) mbar_init(&auxbar[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -325,44 +274,126 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else {
-        // ---------------- epilogue warps 2..9. TMEM lane quarter = warp % 4 (the
-        // hardware's access rule); the two warps of a quarter split the columns.
+        // ---------------- epilogue warps 2..9: TMEM lane quarter q4 = warp % 4
+        // (the hardware's access rule), i.e. rows q4*32..q4*32+31 of the tile;
+        // the two warps of a quarter take the left and right half of the columns.
+        // Each warp stages through its own 4 KB: a bf16 result in one 2 KB half
+        // (alternating halves for a single output, so that one TMA store can
+        // still be reading while the next chunk is written), the GELU outputs or
+        // the GELU derivative operand in both halves, an fp32 result in all 4 KB.
+        const int ew = warp - 2;
         const int q4 = warp & 3;
-        const int half = (warp - 2) >> 2;
-        constexpr int HCH = BN / 64;                 // 32-column chunks per half
-        float* st_w = staging + (warp - 2) * 32 * 32;
-        const int rsub = lane >> 3, qc = lane & 7;
+        const int half = ew >> 2;
+        constexpr int NCH = BN / 64;                 // 32-column chunks per warp per tile
+        constexpr bool ALT = (KIND == EPI_STORE_ACT);
+        uint8_t* wbuf = sEpi + ew * EPI_WARP_BYTES;
+        uint64_t* abar = auxbar + ew;
+        uint32_t aphase = 0u;
+        bool aux_inflight = false;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        uint32_t seq = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
             int split = w / tiles, mt, nt;
             tile_coords(w - split * tiles, num_m, num_n, mt, nt);
-            const int64_t m_base = (int64_t)mt * TC_BM + q4 * 32;
-            const int64_t split_off = (int64_t)split * M * N;
-            const int nbase = nt * BN + half * HCH * 32;
-            AuxBuf cur;
-            aux_load(epi, m_base, M, nbase + 4 * qc, N, rsub, cur);   // overlaps the main loop
-            bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            const int m_base = mt * TC_BM + q4 * 32;
+            const int n_half = nt * BN + half * (BN / 2);
+            // lane j holds bias[n_half + 32c + j] for chunk c; broadcast by shuffle
+            float bz[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; c++) {
+                const int n = n_half + 32 * c + lane;
+                bz[c] = (bias != nullptr && n < N) ? __ldg(bias + n) : 0.f;
+            }
+            if (KIND == EPI_GELU_BWD && lane == 0) {
+                mbar_arrive_expect_tx(abar, 2048);
+                tma_load_2d(wbuf + 2048, &maps.aux, abar, n_half, m_base);
+                aux_inflight = true;
+            }
+            ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int cc = 0; cc < HCH; cc++) {
-                const int c = half * HCH + cc;
-                const int n0 = nt * BN + c * 32;
-                AuxBuf nxt;
-                if (cc + 1 < HCH) aux_load(epi, m_base, M, n0 + 32 + 4 * qc, N, rsub, nxt);
+            for (int c = 0; c < NCH; c++, seq++) {
+                const int n0 = n_half + 32 * c;
+                uint8_t* sbuf = wbuf + (ALT ? (seq & 1) * 2048 : 0);
                 uint32_t r[32];
-                tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
-                stage_write(st_w, lane, r);
+                tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) +
+                              (uint32_t)(acc * BN + half * (BN / 2) + c * 32), r);
+                if (c == NCH - 1) {
+                    // the accumulator is free for the MMA once its last chunk is in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                }
+                float v[32];
+                if (bias != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        v[j] = __uint_as_float(r[j]) + __shfl_sync(0xffffffffu, bz[c], j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                }
+                if (KIND == EPI_GELU_BWD) {
+                    ok = mbar_wait(abar, aphase, abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    aphase ^= 1u;
+                    aux_inflight = false;
+                    float dg[32];
+                    unstage_bf16(wbuf + 2048, lane, dg);
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] *= dg[j];
+                    __syncwarp();                        // every lane has read the operand
+                    if (lane == 0 && c + 1 < NCH) {      // prefetch the next chunk's operand
+                        mbar_arrive_expect_tx(abar, 2048);
+                        tma_load_2d(wbuf + 2048, &maps.aux, abar, n0 + 32, m_base);
+                        aux_inflight = true;
+                    }
+                }
+                // the TMA store that last read this staging area is done
+                if (lane == 0) {
+                    if (ALT) tma_wait_read<1>();
+                    else tma_wait_read<0>();
+                }
                 __syncwarp();
-                epilogue_chunk(epi, st_w, m_base, M, n0 + 4 * qc, N, rsub, qc, cur, split_off);
+                if (KIND == EPI_STORE_F32 || KIND == EPI_ACCUM_F32) {
+                    stage_f32(sbuf, lane, v);
+                } else if (KIND == EPI_GELU) {
+                    // o1 = gelu'(pre) (saved for the backward), o2 = gelu(pre)
+                    float g[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j++) gelu_and_grad_hw(v[j], g[j], v[j]);
+                    stage_bf16(sbuf, lane, v);
+                    stage_bf16(sbuf + 2048, lane, g);
+                } else {
+                    stage_bf16(sbuf, lane, v);
+                }
+                fence_async_smem();
                 __syncwarp();
-                if (cc + 1 < HCH) cur = nxt;
+                if (lane == 0 && n0 < N && m_base < M) {
+                    if (KIND == EPI_STORE_F32) {
+                        tma_store_3d(&maps.o1, sbuf, n0, m_base, split);
+                    } else if (KIND == EPI_ACCUM_F32) {
+                        tma_reduce_add_2d(&maps.o1, sbuf, n0, m_base);
+                    } else {
+                        tma_store_2d(&maps.o1, sbuf, n0, m_base);
+                        if (KIND == EPI_GELU) tma_store_2d(&maps.o2, sbuf + 2048, n0, m_base);
+                    }
+                }
+                if (lane == 0) tma_commit();
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+        if (lane == 0) {
+            tma_wait_all();
+            // after an abort a prefetch of the GELU derivative may still be in
+            // flight: wait for it (bounded) before the CTA exits
+            if (KIND == EPI_GELU_BWD && aux_inflight) {
+                const long long t0 = wait_clock();
+                while (!mbar_try_wait(abar, aphase) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
+            }
         }
     }
     __syncthreads();
@@ -395,53 +426,111 @@ static EncodeTiledFn get_encode() {
     return fn;
 }
 
-// 2-D bf16 tensor map: `inner` contiguous elements per line, `outer` lines
-// `ld` elements apart; boxes of box_inner x box_outer with 128B swizzle.
-static bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, int64_t ld,
-                     uint32_t box_inner, uint32_t box_outer) {
+// Tensor map of a row-major matrix of `outer` lines of `inner` elements, `ld`
+// elements between lines. rank 3 adds a third dimension of `splits` such
+// matrices stored back to back (the map's rank must match the dimensionality
+// of the TMA instructions that use it). Boxes of box_inner x box_outer (x 1).
+static bool make_map(CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int esize,
+                     uint64_t inner, uint64_t outer, int64_t ld, uint32_t box_inner,
+                     uint32_t box_outer, CUtensorMapSwizzle sw, int rank = 2, int splits = 1) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint64_t dims[3] = {inner, outer, (cuuint64_t)splits};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * esize, (cuuint64_t)ld * esize * outer};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (rank != 2 && rank != 3) return false;
+    CUresult r = enc(map, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+static bool make_operand_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                             int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    return make_map(map, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld, box_inner,
+                    box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi) {
     if (M <= 0 || N <= 0 || K <= 0) return false;
     if ((A.ld % 8) || (B.ld % 8)) return false;
-    if (((uintptr_t)A.ptr | (uintptr_t)B.ptr) & 15) return false;
-    if (epi.ldo % 8) return false;
-    if (N % 4) return false;
+    if (!aligned16(A.ptr) || !aligned16(B.ptr)) return false;
+    if (!epi.out || !aligned16(epi.out)) return false;
+    switch (epi.kind) {
+        case EPI_STORE_ACT:
+            if (epi.ldo % 8) return false;
+            break;
+        case EPI_GELU:
+            if (epi.ldo % 8 || !epi.out2 || !aligned16(epi.out2) || epi.ldo2 % 8) return false;
+            break;
+        case EPI_GELU_BWD:
+            if (epi.ldo % 8 || !epi.aux || !aligned16(epi.aux) || epi.ld_aux % 8 || epi.bias) return false;
+            break;
+        case EPI_STORE_F32:
+            if (epi.ldo % 4) return false;
+            break;
+        case EPI_ACCUM_F32:
+            if (epi.ldo % 4 || epi.bias) return false;
+            break;
+        default:
+            return false;   // the residual add is fused into the LayerNorm, not done here
+    }
     if (!get_encode()) return false;
     return true;
 }
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, int KIND>
 static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                              int splits, DevState* st, cudaStream_t s) {
-    using Cfg = TcCfg<BN, A_MN, B_MN>;
+    using Cfg = TcCfg<BN>;
     CUtensorMap ta, tb;
-    bool ok = A_MN ? make_map(&ta, A.ptr, (uint64_t)M, (uint64_t)K, A.ld, 64, 64)
-                   : make_map(&ta, A.ptr, (uint64_t)K, (uint64_t)M, A.ld, 64, TC_BM);
-    ok = ok && (B_MN ? make_map(&tb, B.ptr, (uint64_t)N, (uint64_t)K, B.ld, 64, 64)
-                     : make_map(&tb, B.ptr, (uint64_t)K, (uint64_t)N, B.ld, 64, BN));
+    bool ok = A_MN ? make_operand_map(&ta, A.ptr, (uint64_t)M, (uint64_t)K, A.ld, 64, 64)
+                   : make_operand_map(&ta, A.ptr, (uint64_t)K, (uint64_t)M, A.ld, 64, TC_BM);
+    ok = ok && (B_MN ? make_operand_map(&tb, B.ptr, (uint64_t)N, (uint64_t)K, B.ld, 64, 64)
+                     : make_operand_map(&tb, B.ptr, (uint64_t)K, (uint64_t)N, B.ld, 64, BN));
+    EpiMaps maps;
+    memset(&maps, 0, sizeof maps);
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (KIND == EPI_STORE_F32)          // 3-D store: {n, m, split}
+        ok = ok && make_map(&maps.o1, epi.out, F32, 4, N, M, epi.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                            3, splits);
+    else if (KIND == EPI_ACCUM_F32)     // 2-D reduce-add
+        ok = ok && make_map(&maps.o1, epi.out, F32, 4, N, M, epi.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && make_map(&maps.o1, epi.out, BF, 2, N, M, epi.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (KIND == EPI_GELU)
+        ok = ok && make_map(&maps.o2, epi.out2, BF, 2, N, M, epi.ldo2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (KIND == EPI_GELU_BWD)
+        ok = ok && make_map(&maps.aux, epi.aux, BF, 2, N, M, epi.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
-        CUDA_OK(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+        CUDA_OK(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, KIND>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM));
         attr_set = true;
     }
     const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN);
     const int total = tiles * splits;
     const int grid = total < num_sms() ? total : num_sms();
-    gemm_tc_kernel<BN, A_MN, B_MN><<<grid, 320, Cfg::SMEM, s>>>(ta, tb, M, N, K, splits, epi, st);
+    gemm_tc_kernel<BN, A_MN, B_MN, KIND><<<grid, TC_THREADS, Cfg::SMEM, s>>>(
+        ta, tb, maps, M, N, K, splits, epi.bias, st);
     return cudaGetLastError();
+}
+
+template <int BN, bool A_MN, bool B_MN>
+static cudaError_t launch_kind(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                               int splits, DevState* st, cudaStream_t s) {
+    switch (epi.kind) {
+        case EPI_STORE_ACT: return launch_tc<BN, A_MN, B_MN, EPI_STORE_ACT>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_GELU: return launch_tc<BN, A_MN, B_MN, EPI_GELU>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_GELU_BWD: return launch_tc<BN, A_MN, B_MN, EPI_GELU_BWD>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_STORE_F32: return launch_tc<BN, A_MN, B_MN, EPI_STORE_F32>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_ACCUM_F32: return launch_tc<BN, A_MN, B_MN, EPI_ACCUM_F32>(M, N, K, A, B, epi, splits, st, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
@@ -461,7 +550,7 @@ cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, cons
     const bool wide = (N % 256 == 0) || N > 2048;
 #define TC_CASE(BNV, AM, BM_)                                                   \
     if (a_mn == AM && b_mn == BM_)                                              \
-        return launch_tc<BNV, AM, BM_>(M, N, K, A, B, epi, splits, st, s);
+        return launch_kind<BNV, AM, BM_>(M, N, K, A, B, epi, splits, st, s);
     if (wide) {
         TC_CASE(256, false, false)
         TC_CASE(256, false, true)

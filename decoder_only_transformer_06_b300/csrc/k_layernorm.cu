@@ -10,11 +10,14 @@ namespace k {
 static constexpr float LN_EPS = 1e-5f;
 static constexpr int LN_WARPS = 8;
 
+// With y != nullptr the row is first formed as x + y (the residual add of
+// the preceding block branch, whose Linear output y is in the activation
+// type) and written to x_out, the residual stream the backward reads.
 template <typename Act, int EPL>
 __global__ void __launch_bounds__(LN_WARPS * 32)
-ln_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g,
-              const float* __restrict__ b, Act* __restrict__ u, float* __restrict__ mu_out,
-              float* __restrict__ rstd_out, int M, int C) {
+ln_fwd_kernel(const float* __restrict__ x, const Act* __restrict__ y, float* __restrict__ x_out,
+              const float* __restrict__ g, const float* __restrict__ b, Act* __restrict__ u,
+              float* __restrict__ mu_out, float* __restrict__ rstd_out, int M, int C) {
     int row = blockIdx.x * LN_WARPS + threadIdx.x / 32;
     int lane = threadIdx.x % 32;
     if (row >= M) return;
@@ -25,6 +28,10 @@ ln_fwd_kernel(const float* __restrict__ x, const float* __restrict__ g,
     for (int j = 0; j < EPL; j++) {
         int c = lane + 32 * j;
         v[j] = c < C ? xr[c] : 0.f;
+        if (y && c < C) {
+            v[j] += to_f(y[(int64_t)row * C + c]);
+            x_out[(int64_t)row * C + c] = v[j];
+        }
         s += v[j];
     }
     float mean = warp_sum(s) / (float)C;
@@ -161,9 +168,9 @@ __device__ __forceinline__ float4 load4<bf16>(const bf16* src) {
 
 template <typename Act, int V4>
 __global__ void __launch_bounds__(LN_WARPS * 32)
-ln_fwd_vec(const float* __restrict__ x, const float* __restrict__ g, const float* __restrict__ b,
-           Act* __restrict__ u, float* __restrict__ mu_out, float* __restrict__ rstd_out, int M,
-           int C) {
+ln_fwd_vec(const float* __restrict__ x, const Act* __restrict__ y, float* __restrict__ x_out,
+           const float* __restrict__ g, const float* __restrict__ b, Act* __restrict__ u,
+           float* __restrict__ mu_out, float* __restrict__ rstd_out, int M, int C) {
     const int row = blockIdx.x * LN_WARPS + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     if (row >= M) return;
@@ -171,10 +178,19 @@ ln_fwd_vec(const float* __restrict__ x, const float* __restrict__ g, const float
     float4 v[V4];
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < V4; j++) {
-        v[j] = xr[lane + 32 * j];
-        s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+    for (int j = 0; j < V4; j++) v[j] = xr[lane + 32 * j];
+    if (y) {
+        const Act* yr = y + (int64_t)row * C;
+        float4* xo = (float4*)(x_out + (int64_t)row * C);
+#pragma unroll
+        for (int j = 0; j < V4; j++) {
+            const float4 a = load4<Act>(yr + 4 * (lane + 32 * j));
+            v[j].x += a.x; v[j].y += a.y; v[j].z += a.z; v[j].w += a.w;
+            xo[lane + 32 * j] = v[j];
+        }
     }
+#pragma unroll
+    for (int j = 0; j < V4; j++) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
     const float mean = warp_sum(s) / (float)C;
     float q = 0.f;
 #pragma unroll
@@ -323,22 +339,24 @@ size_t layernorm_bwd_partial_floats(int M, int C) { return (size_t)ln_bwd_blocks
     if (epl <= EPLV) { CALL(EPLV); return cudaGetLastError(); }
 
 template <typename Act>
-cudaError_t layernorm_fwd(const float* x, const float* g, const float* b, Act* u, float* mu,
-                          float* rstd, int M, int C, cudaStream_t s) {
+cudaError_t layernorm_fwd(const float* x, const Act* y, float* x_out, const float* g,
+                          const float* b, Act* u, float* mu, float* rstd, int M, int C,
+                          cudaStream_t s) {
+    if (y && !x_out) return cudaErrorInvalidValue;
     int epl = (C + 31) / 32;
     int blocks = (M + LN_WARPS - 1) / LN_WARPS;
     if (C % 128 == 0 && C <= 2048) {
         switch (C / 128) {
 #define LNV(V)                                                                                      \
     case V:                                                                                         \
-        ln_fwd_vec<Act, V><<<blocks, LN_WARPS * 32, 0, s>>>(x, g, b, u, mu, rstd, M, C);            \
+        ln_fwd_vec<Act, V><<<blocks, LN_WARPS * 32, 0, s>>>(x, y, x_out, g, b, u, mu, rstd, M, C);            \
         return cudaGetLastError();
             LNV(1) LNV(2) LNV(3) LNV(4) LNV(5) LNV(6) LNV(7) LNV(8)
             LNV(9) LNV(10) LNV(11) LNV(12) LNV(13) LNV(14) LNV(15) LNV(16)
 #undef LNV
         }
     }
-#define LNF(E) ln_fwd_kernel<Act, E><<<blocks, LN_WARPS * 32, 0, s>>>(x, g, b, u, mu, rstd, M, C)
+#define LNF(E) ln_fwd_kernel<Act, E><<<blocks, LN_WARPS * 32, 0, s>>>(x, y, x_out, g, b, u, mu, rstd, M, C)
     LN_DISPATCH(2, LNF)
     LN_DISPATCH(4, LNF)
     LN_DISPATCH(8, LNF)
@@ -402,10 +420,12 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
     return cudaGetLastError();
 }
 
-template cudaError_t layernorm_fwd<float>(const float*, const float*, const float*, float*, float*,
-                                          float*, int, int, cudaStream_t);
-template cudaError_t layernorm_fwd<bf16>(const float*, const float*, const float*, bf16*, float*,
-                                         float*, int, int, cudaStream_t);
+template cudaError_t layernorm_fwd<float>(const float*, const float*, float*, const float*,
+                                          const float*, float*, float*, float*, int, int,
+                                          cudaStream_t);
+template cudaError_t layernorm_fwd<bf16>(const float*, const bf16*, float*, const float*,
+                                         const float*, bf16*, float*, float*, int, int,
+                                         cudaStream_t);
 template cudaError_t layernorm_bwd<float>(const float*, const float*, const float*, const float*,
                                           const float*, float*, float*, bool, float*, float*,
                                           float*, int, int, float*, cudaStream_t);
