@@ -632,7 +632,7 @@ static int backward_impl(gpt2_model* m) {
         if (m->use_bf16)
             RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
                 k::attention_bwd_bf16((const bf16*)a.qkv, (const bf16*)a.att, a.lse, (const bf16*)m->datt,
-                                      (bf16*)m->dqkv, m->Dbuf, B, T, H, m->hs, s));
+                                      (bf16*)m->dqkv, m->Dbuf, B, T, H, m->hs, m->st, s));
         else
             RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
                 k::attention_bwd_f32((const float*)a.qkv, (const float*)a.att, a.lse, (const float*)m->datt,
@@ -985,12 +985,15 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
     if (!qkv || !out || !lse || !dout || !dqkv || !scratch || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
         return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
     cudaError_t r;
-    if (precision == GPT2_BF16)
+    if (precision == GPT2_BF16) {
+        DevState* st = op_state();
+        if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
         r = k::attention_bwd_bf16((const bf16*)qkv, (const bf16*)out, lse, (const bf16*)dout,
-                                  (bf16*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
-    else
+                                  (bf16*)dqkv, scratch, B, T, H, hs, st, (cudaStream_t)stream);
+    } else {
         r = k::attention_bwd_f32((const float*)qkv, (const float*)out, lse, (const float*)dout,
                                  (float*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+    }
     if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");
     if (r != cudaSuccess) return fail_cuda(nullptr, "attention_bwd", r);
     return GPT2_OK;
@@ -1013,13 +1016,17 @@ namespace {
 
 constexpr int64_t NOALLOC_ROWS_MAX = int64_t(1) << 20;   // B*H*T rows, 4 MiB of fp32
 __device__ __align__(256) float g_noalloc_rowsum[NOALLOC_ROWS_MAX];
+// status word of the kernels' bounded waits (zero at load; reported by gpt2_op_sync)
+__device__ __align__(256) DevState g_noalloc_state;
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+DevState* g_noalloc_st[NOALLOC_MAX_DEVICES] = {};
 
-// Device address of g_noalloc_rowsum on the current device (looked up once).
-cudaError_t noalloc_scratch(float** out) {
+// Device addresses of g_noalloc_rowsum and g_noalloc_state on the current
+// device (looked up once per device).
+cudaError_t noalloc_scratch(float** out, DevState** st) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1027,11 +1034,16 @@ cudaError_t noalloc_scratch(float** out) {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
         void* p = nullptr;
+        void* q = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_rowsum);
         if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress(&q, g_noalloc_state);
+        if (e != cudaSuccess) return e;
+        g_noalloc_st[dev] = (DevState*)q;
         g_noalloc_ptr[dev] = (float*)p;
     }
     *out = g_noalloc_ptr[dev];
+    *st = g_noalloc_st[dev];
     return cudaSuccess;
 }
 
@@ -1048,13 +1060,14 @@ extern "C" int gpt2_op_attention_bwd_noalloc(int precision, int B, int T, int H,
                         " exceeds the fixed scratch of the allocation-free attention backward (" +
                         std::to_string(NOALLOC_ROWS_MAX) + " rows)");
     float* scratch = nullptr;
-    cudaError_t r = noalloc_scratch(&scratch);
+    DevState* st = nullptr;
+    cudaError_t r = noalloc_scratch(&scratch, &st);
     if (r != cudaSuccess) return fail_cuda(nullptr, "cudaGetSymbolAddress", r);
     // every row of the scratch is written by the rowsum pass before any read,
     // so stale contents from an earlier call need no clearing
     if (precision == GPT2_BF16)
         r = k::attention_bwd_bf16((const bf16*)qkv, (const bf16*)out, lse, (const bf16*)dout,
-                                  (bf16*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);
+                                  (bf16*)dqkv, scratch, B, T, H, hs, st, (cudaStream_t)stream);
     else
         r = k::attention_bwd_f32((const float*)qkv, (const float*)out, lse, (const float*)dout,
                                  (float*)dqkv, scratch, B, T, H, hs, (cudaStream_t)stream);

@@ -366,4 +366,542 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ backward
+// Deterministic (no atomics) backward in two kernels; the probabilities are
+// recomputed from the forward's lse, D = rowsum(dO * O) comes from a pre-pass.
+// With s the raw score q.k, p = exp(s/sqrt(hs) - lse), dP = dO V^T,
+// dS = P * (dP - D) (the gradient of the scaled scores):
+//   dK = dS^T Q / sqrt(hs), dV = P^T dO   (one CTA per 128-key block)
+//   dQ = dS K / sqrt(hs)                  (one CTA per 128-query block)
+// Both kernels keep the two 128x128 products (S and dP, or their transposes)
+// in TMEM, write the bf16 operands of the accumulating products (P^T and
+// dS^T, or dS) to shared memory in the K-major 128B-swizzled layout, and
+// accumulate dK, dV (or dQ) in TMEM across the blocks of the other operand.
+
+namespace {
+
+constexpr int BW_SLOTS = 3;
+// dK/dV kernel
+constexpr int KV_OFF_K = 0;
+constexpr int KV_OFF_V = KV_OFF_K + AT_TILE;
+constexpr int KV_OFF_Q = KV_OFF_V + AT_TILE;
+constexpr int KV_OFF_DO = KV_OFF_Q + BW_SLOTS * AT_TILE;
+constexpr int KV_OFF_PT = KV_OFF_DO + BW_SLOTS * AT_TILE;
+constexpr int KV_OFF_DST = KV_OFF_PT + AT_P_BYTES;
+constexpr int KV_OFF_LD = KV_OFF_DST + AT_P_BYTES;        // lse2[2][128], D[2][128]
+constexpr int KV_OFF_BAR = KV_OFF_LD + 4 * 128 * 4;
+constexpr size_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
+// dQ kernel
+constexpr int DQ_OFF_Q = 0;
+constexpr int DQ_OFF_DO = DQ_OFF_Q + AT_TILE;
+constexpr int DQ_OFF_K = DQ_OFF_DO + AT_TILE;
+constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;
+constexpr int DQ_OFF_DS = DQ_OFF_V + BW_SLOTS * AT_TILE;
+constexpr int DQ_OFF_BAR = DQ_OFF_DS + AT_P_BYTES;
+constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
+// TMEM columns of both kernels: S (or S^T) 0..127, dP 128..255, the two
+// accumulators at 256 and 320
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_A0 = 256, TM_A1 = 320;
+constexpr float LOG2E_F = 1.4426950408889634f;
+
+// 32 fp32 values of one row as bf16 into a K-major 128B-swizzled operand tile
+// of 128 rows x 128 columns (two 64-column blocks of 16 KB): chunk c holds
+// columns 32c..32c+31.
+__device__ __forceinline__ void put_row_chunk(uint8_t* tile, int row, int c, const float (&v)[32]) {
+    uint8_t* base = tile + (c >> 1) * 16384 + row * 128;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const int piece = (c & 1) * 4 + q;
+        uint4 w = make_uint4(pack2_bf16(v[8 * q + 0], v[8 * q + 1]), pack2_bf16(v[8 * q + 2], v[8 * q + 3]),
+                             pack2_bf16(v[8 * q + 4], v[8 * q + 5]), pack2_bf16(v[8 * q + 6], v[8 * q + 7]));
+        *(uint4*)(base + ((piece ^ (row & 7)) << 4)) = w;
+    }
+}
+
+// 64 fp32 accumulator columns times `scale`, as bf16, to 128 contiguous bytes.
+__device__ __forceinline__ void store_row64(bf16* dst, const uint32_t (&a)[64], float scale) {
+    uint4* d = (uint4*)dst;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+        const float* f = (const float*)&a[8 * c];
+        d[c] = make_uint4(pack2_bf16(f[0] * scale, f[1] * scale), pack2_bf16(f[2] * scale, f[3] * scale),
+                          pack2_bf16(f[4] * scale, f[5] * scale), pack2_bf16(f[6] * scale, f[7] * scale));
+    }
+}
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+}  // namespace
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                     const float* __restrict__ lse, const float* __restrict__ Dg,
+                     bf16* __restrict__ dqkv, int T, int H, DevState* st) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sK = smem + KV_OFF_K;
+    uint8_t* sV = smem + KV_OFF_V;
+    uint8_t* sQ = smem + KV_OFF_Q;
+    uint8_t* sDO = smem + KV_OFF_DO;
+    uint8_t* sPT = smem + KV_OFF_PT;
+    uint8_t* sDST = smem + KV_OFF_DST;
+    float* sL = (float*)(smem + KV_OFF_LD);          // [2][128] lse in log2 units
+    float* sD = sL + 256;                              // [2][128]
+    uint64_t* bars = (uint64_t*)(smem + KV_OFF_BAR);
+    uint64_t* kv_full = bars;
+    uint64_t* qd_full = bars + 1;                      // [3]
+    uint64_t* qd_empty = bars + 4;                     // [3]
+    uint64_t* st_full = bars + 7;
+    uint64_t* st_free = bars + 8;
+    uint64_t* ps_full = bars + 9;
+    uint64_t* ps_free = bars + 10;
+    uint64_t* done = bars + 11;
+    uint32_t* tmem_slot = (uint32_t*)(bars + 12);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int nb = (T + AT_BK - 1) / AT_BK;
+    const int kb = (int)blockIdx.x;                   // key block
+    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int C = H * AT_HS;
+    const int n = nb - kb;                            // query blocks kb..nb-1
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < BW_SLOTS; s++) {
+            mbar_init(&qd_full[s], 1);
+            mbar_init(&qd_empty[s], 1);
+        }
+        mbar_init(st_full, 1);
+        mbar_init(st_free, 4);
+        mbar_init(ps_full, 4);
+        mbar_init(ps_free, 1);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
+            tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, kb * AT_BK, b);
+            tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, kb * AT_BK, b);
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < n; i++) {
+                const int s = i % BW_SLOTS;
+                if (!mbar_wait(&qd_empty[s], (uint32_t)(((i / BW_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&qd_full[s], 2 * AT_TILE);
+                tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &qd_full[s], h * AT_HS, (kb + i) * AT_BQ, b);
+                tma_load_3d(sDO + s * AT_TILE, &tm_do, &qd_full[s], h * AT_HS, (kb + i) * AT_BQ, b);
+                issued++;
+            }
+            if (!ok || *abort_flag) {
+                wait_bounded(kv_full, 0);
+                for (int i = (issued > BW_SLOTS ? issued - BW_SLOTS : 0); i < issued; i++)
+                    wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t id_s = make_idesc(AT_BK, AT_BQ, false, false);
+            constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
+            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
+                           do_addr = smem_u32(sDO), pt_addr = smem_u32(sPT), dst_addr = smem_u32(sDST);
+            bool ok = mbar_wait(kv_full, 0, abort_flag);
+            for (int i = 0; i <= n && ok; i++) {
+                if (i < n) {
+                    const int s = i % BW_SLOTS;
+                    if (!mbar_wait(&qd_full[s], (uint32_t)((i / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(st_free, (uint32_t)((i & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_HS / 16; kk++) {
+                        // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = head dim)
+                        mma_bf16(tmem_base + TM_S, smem_desc(k_addr + 32 * kk, 16, 1024),
+                                 smem_desc(q_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem_base + TM_DP, smem_desc(v_addr + 32 * kk, 16, 1024),
+                                 smem_desc(do_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(st_full);
+                }
+                if (i >= 1) {
+                    const int ii = i - 1, s = ii % BW_SLOTS;
+                    if (!mbar_wait(ps_full, (uint32_t)(ii & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_BQ / 16; kk++) {
+                        // dV += P^T dO, dK += dS^T Q (K = queries; dO and Q read MN-major)
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
+                        mma_bf16(tmem_base + TM_A0, smem_desc(pt_addr + off, 16, 1024),
+                                 smem_desc(do_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                        mma_bf16(tmem_base + TM_A1, smem_desc(dst_addr + off, 16, 1024),
+                                 smem_desc(q_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                    }
+                    mma_commit(ps_free);
+                    mma_commit(&qd_empty[s]);
+                }
+            }
+            // every product issued so far completes before `done` (also on abort)
+            mma_commit(done);
+            if (!ok) wait_bounded(done, 0);
+        }
+    } else {
+        // ---------------- warps 0..3: thread r owns key row r (TMEM lane r)
+        const int r = threadIdx.x;
+        const int key = kb * AT_BK + r;
+        const float sl2 = LOG2E_F * 0.125f;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        bool ok = true;
+        for (int i = 0; i < n; i++) {
+            const int q0 = (kb + i) * AT_BQ, ls = i & 1;
+            {
+                const int q = q0 + r;
+                sL[ls * 128 + r] = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
+                sD[ls * 128 + r] = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+            }
+            softmax_bar();
+            ok = mbar_wait(st_full, (uint32_t)(i & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait(ps_free, (uint32_t)((i & 1) ^ 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const float* L = sL + ls * 128;
+            const float* Dq = sD + ls * 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
+                tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
+                tmem_wait_ld();
+                if (c == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(st_free);
+                }
+                float pv[32], dsv[32];
+#pragma unroll
+                for (int t = 0; t < 32; t++) {
+                    const int qq = 32 * c + t;
+                    float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -L[qq]));
+                    if (i == 0 && qq < r) p = 0.f;          // query before key: masked
+                    pv[t] = p;
+                    dsv[t] = p * (__uint_as_float(dr[t]) - Dq[qq]);
+                }
+                put_row_chunk(sPT, r, c, pv);
+                put_row_chunk(sDST, r, c, dsv);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ps_full);
+        }
+        if (ok) {
+            ok = mbar_wait(done, 0, abort_flag);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                uint32_t dv[64], dk[64];
+                tmem_ld32_nowait(lane_base + TM_A0, dv);
+                tmem_ld32_nowait(lane_base + TM_A0 + 32, dv + 32);
+                tmem_ld32_nowait(lane_base + TM_A1, dk);
+                tmem_ld32_nowait(lane_base + TM_A1 + 32, dk + 32);
+                tmem_wait_ld();
+                if (key < T) {
+                    bf16* row = dqkv + ((int64_t)b * T + key) * 3 * C + h * AT_HS;
+                    store_row64(row + C, dk, 0.125f);
+                    store_row64(row + 2 * C, dv, 1.f);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        atomicOr(&st->err, ERR_TIMEOUT);
+        st->timeout_site = 4;
+    }
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, AT_TMEM_COLS);
+    }
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                    const float* __restrict__ lse, const float* __restrict__ Dg,
+                    bf16* __restrict__ dqkv, int T, int H, DevState* st) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = smem + DQ_OFF_Q;
+    uint8_t* sDO = smem + DQ_OFF_DO;
+    uint8_t* sK = smem + DQ_OFF_K;
+    uint8_t* sV = smem + DQ_OFF_V;
+    uint8_t* sDS = smem + DQ_OFF_DS;
+    uint64_t* bars = (uint64_t*)(smem + DQ_OFF_BAR);
+    uint64_t* qd_full = bars;
+    uint64_t* k_full = bars + 1;                       // [3]
+    uint64_t* k_empty = bars + 4;
+    uint64_t* v_full = bars + 7;
+    uint64_t* v_empty = bars + 10;
+    uint64_t* st_full = bars + 13;
+    uint64_t* st_free = bars + 14;
+    uint64_t* ds_full = bars + 15;
+    uint64_t* ds_free = bars + 16;
+    uint64_t* done = bars + 17;
+    uint32_t* tmem_slot = (uint32_t*)(bars + 18);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int nqb = (T + AT_BQ - 1) / AT_BQ;
+    const int qb = nqb - 1 - (int)blockIdx.x;         // heaviest query blocks first
+    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int C = H * AT_HS;
+    const int nkv = qb + 1;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        mbar_init(qd_full, 1);
+        for (int s = 0; s < BW_SLOTS; s++) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        mbar_init(st_full, 1);
+        mbar_init(st_free, 4);
+        mbar_init(ds_full, 4);
+        mbar_init(ds_free, 1);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            mbar_arrive_expect_tx(qd_full, 2 * AT_TILE);
+            tma_load_3d(sQ, &tm_qkv, qd_full, h * AT_HS, qb * AT_BQ, b);
+            tma_load_3d(sDO, &tm_do, qd_full, h * AT_HS, qb * AT_BQ, b);
+            int nk = 0, nv = 0;
+            bool ok = true;
+            for (int j = 0; j < nkv && ok; j++) {
+                const int s = j % BW_SLOTS;
+                const uint32_t ph = (uint32_t)((j / BW_SLOTS) & 1);
+                if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&k_full[s], AT_TILE);
+                tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
+                nk++;
+                if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&v_full[s], AT_TILE);
+                tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                nv++;
+            }
+            if (!ok || *abort_flag) {
+                wait_bounded(qd_full, 0);
+                for (int j = (nk > BW_SLOTS ? nk - BW_SLOTS : 0); j < nk; j++)
+                    wait_bounded(&k_full[j % BW_SLOTS], (uint32_t)((j / BW_SLOTS) & 1));
+                for (int j = (nv > BW_SLOTS ? nv - BW_SLOTS : 0); j < nv; j++)
+                    wait_bounded(&v_full[j % BW_SLOTS], (uint32_t)((j / BW_SLOTS) & 1));
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
+            constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
+            const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), k_addr = smem_u32(sK),
+                           v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+            bool ok = mbar_wait(qd_full, 0, abort_flag);
+            for (int j = 0; j <= nkv && ok; j++) {
+                if (j < nkv) {
+                    const int s = j % BW_SLOTS;
+                    const uint32_t ph = (uint32_t)((j / BW_SLOTS) & 1);
+                    if (!mbar_wait(&k_full[s], ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&v_full[s], ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(st_free, (uint32_t)((j & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_HS / 16; kk++) {
+                        // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = head dim)
+                        mma_bf16(tmem_base + TM_S, smem_desc(q_addr + 32 * kk, 16, 1024),
+                                 smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem_base + TM_DP, smem_desc(do_addr + 32 * kk, 16, 1024),
+                                 smem_desc(v_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(st_full);
+                    mma_commit(&v_empty[s]);
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, s = jj % BW_SLOTS;
+                    if (!mbar_wait(ds_full, (uint32_t)(jj & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AT_BK / 16; kk++) {
+                        // dQ += dS K (K = keys; K read MN-major)
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_bf16(tmem_base + TM_A0, smem_desc(ds_addr + off, 16, 1024),
+                                 smem_desc(k_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a,
+                                 (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(ds_free);
+                    mma_commit(&k_empty[s]);
+                }
+            }
+            mma_commit(done);
+            if (!ok) wait_bounded(done, 0);
+        }
+    } else {
+        // ---------------- warps 0..3: thread r owns query row r (TMEM lane r)
+        const int r = threadIdx.x;
+        const int q = qb * AT_BQ + r;
+        const float sl2 = LOG2E_F * 0.125f;
+        const float lse2 = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
+        const float Dq = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        bool ok = true;
+        for (int j = 0; j < nkv; j++) {
+            ok = mbar_wait(st_full, (uint32_t)(j & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ok = mbar_wait(ds_free, (uint32_t)((j & 1) ^ 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const int key0 = j * AT_BK;
+            const bool edge = (j == qb) || (key0 + AT_BK > T);
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
+                tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
+                tmem_wait_ld();
+                if (c == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(st_free);
+                }
+                float dsv[32];
+#pragma unroll
+                for (int t = 0; t < 32; t++) {
+                    const int kk = key0 + 32 * c + t;
+                    float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -lse2));
+                    if (edge && (kk > q || kk >= T)) p = 0.f;
+                    dsv[t] = p * (__uint_as_float(dr[t]) - Dq);
+                }
+                put_row_chunk(sDS, r, c, dsv);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ds_full);
+        }
+        if (ok) {
+            ok = mbar_wait(done, 0, abort_flag);
+            if (__all_sync(0xffffffffu, ok)) {
+                tc_fence_after();
+                uint32_t dq[64];
+                tmem_ld32_nowait(lane_base + TM_A0, dq);
+                tmem_ld32_nowait(lane_base + TM_A0 + 32, dq + 32);
+                tmem_wait_ld();
+                if (q < T) store_row64(dqkv + ((int64_t)b * T + q) * 3 * C + h * AT_HS, dq, 0.125f);
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        atomicOr(&st->err, ERR_TIMEOUT);
+        st->timeout_site = 5;
+    }
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, AT_TMEM_COLS);
+    }
+}
+
+// dout [B, T, C] bf16 as a 3-D map {C, T, B}, boxes 64 x 128 x 1, 128B swizzle.
+static bool make_do_map(CUtensorMap* map, const bf16* dout, int B, int T, int C) {
+    EncodeTiledFnA enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)C * 2 * T};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bf16*>(dout), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* D,
+                             bf16* dqkv, int B, int T, int H, int hs, DevState* st, cudaStream_t s) {
+    if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
+    if (((uintptr_t)qkv & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15))
+        return cudaErrorInvalidValue;
+    CUtensorMap mq, md;
+    memset(&mq, 0, sizeof mq);
+    memset(&md, 0, sizeof md);
+    if (!make_qkv_map(&mq, qkv, B, T, H * hs) || !make_do_map(&md, dout, B, T, H * hs))
+        return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)KV_SMEM));
+        CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)DQ_SMEM));
+        attr = true;
+    }
+    dim3 grid((T + AT_BQ - 1) / AT_BQ, B * H);
+    fa_tc_bwd_dkv_kernel<<<grid, AT_THREADS, KV_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, st);
+    CUDA_OK(cudaGetLastError());
+    fa_tc_bwd_dq_kernel<<<grid, AT_THREADS, DQ_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, st);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ D pre-pass
+// D[b,h,i] = sum_c dO[i, h*64+c] * O[i, h*64+c]; one thread per (row, head).
+__global__ void fa_bwd_d_kernel(const bf16* __restrict__ out, const bf16* __restrict__ dout,
+                                float* __restrict__ D, int B, int T, int H) {
+    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)B * T * H) return;
+    int h = (int)(idx % H);
+    int64_t row = idx / H;             // b*T + t
+    int64_t b = row / T, tt = row % T;
+    const int C = H * AT_HS;
+    const uint4* o4 = (const uint4*)(out + row * C + h * AT_HS);
+    const uint4* d4 = (const uint4*)(dout + row * C + h * AT_HS);
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        uint4 a = o4[q], c = d4[q];
+        const __nv_bfloat162* ha = (const __nv_bfloat162*)&a;
+        const __nv_bfloat162* hc = (const __nv_bfloat162*)&c;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            float2 fa = __bfloat1622float2(ha[j]), fc = __bfloat1622float2(hc[j]);
+            s += fa.x * fc.x + fa.y * fc.y;
+        }
+    }
+    D[(b * H + h) * T + tt] = s;
+}
+
+bool attention_bf16_supported(int T, int hs) { return hs == AT_HS && T >= 1; }
+
+cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* lse,
+                               const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,
+                               int hs, DevState* st, cudaStream_t s) {
+    if (!attention_bf16_supported(T, hs)) return cudaErrorInvalidValue;
+    int64_t n = (int64_t)B * T * H;
+    fa_bwd_d_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(out, dout, Dbuf, B, T, H);
+    CUDA_OK(cudaGetLastError());
+    return attention_bwd_tc(qkv, dout, lse, Dbuf, dqkv, B, T, H, hs, st, s);
+}
+
 }  // namespace k
