@@ -7,7 +7,7 @@
 // softmax over key blocks: "Let's reproduce GPT-2" 02:00:18, Flash Attention).
 // Also writes lse = log sum_j exp(S_ij) per query for the backward.
 //
-// One CTA per (128-query block, b, h); 192 threads:
+// Work item = (128-query block, b, h); persistent CTAs, 192 threads:
 //   warps 0..3  softmax: one thread per query row (= its TMEM lane). Reads the
 //               row of S from TMEM, masks, tracks the running max, writes
 //               P = exp(S - max) in bf16 to shared memory as the A operand of
@@ -42,13 +42,13 @@ constexpr int AT_SLOTS = 3;                    // K and V ring depth
 constexpr int AT_TILE = AT_BQ * AT_HS * 2;     // 16 KB: 128 rows x 128 B
 constexpr int AT_P_BYTES = AT_BQ * AT_BK * 2;  // 32 KB
 constexpr int AT_THREADS = 192;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + AT_TILE;
+constexpr int OFF_Q = 0;                       // Q double buffer
+constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
 constexpr int OFF_P = OFF_V + AT_SLOTS * AT_TILE;
 constexpr int OFF_BAR = OFF_P + 2 * AT_P_BYTES;
 constexpr size_t AT_SMEM = OFF_BAR + 256 + 1024;
-constexpr uint32_t TM_O = 256;                 // S[0] at 0, S[1] at 128
+constexpr uint32_t TM_O = 256;                 // S[0] at 0, S[1] at 128, O[0] at 256, O[1] at 320
 constexpr uint32_t AT_TMEM_COLS = 512;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -68,9 +68,15 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 
 }  // namespace
 
+// Persistent: one CTA per SM walks work items w = blockIdx.x, +gridDim.x, ...
+// ordered heaviest first (query block qb = nqb-1 - w / (B*H)). Barrier phases
+// run on counters that every role advances identically: g counts key blocks
+// over all items (K/V ring slots, S and P buffers), `it` counts items (Q and O
+// double buffers), so the next item's Q, K and V load and its first S product
+// runs while the softmax warps finish the previous item.
 __global__ void __launch_bounds__(AT_THREADS, 1)
 fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ out,
-                 float* __restrict__ lse, int T, int H, DevState* st) {
+                 float* __restrict__ lse, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + OFF_Q;
@@ -78,39 +84,41 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
     uint8_t* sV = smem + OFF_V;
     uint8_t* sP = smem + OFF_P;
     uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
-    uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = bars + 4;
-    uint64_t* v_full = bars + 7;
-    uint64_t* v_empty = bars + 10;
-    uint64_t* s_full = bars + 13;
-    uint64_t* s_empty = bars + 15;
-    uint64_t* p_full = bars + 17;
-    uint64_t* pv_done = bars + 19;
-    uint64_t* drain = bars + 21;
-    uint32_t* tmem_slot = (uint32_t*)(bars + 22);
+    uint64_t* q_full = bars;           // [2]
+    uint64_t* q_empty = bars + 2;      // [2]
+    uint64_t* k_full = bars + 4;       // [3]
+    uint64_t* k_empty = bars + 7;
+    uint64_t* v_full = bars + 10;
+    uint64_t* v_empty = bars + 13;
+    uint64_t* s_full = bars + 16;      // [2]
+    uint64_t* s_empty = bars + 18;
+    uint64_t* p_full = bars + 20;
+    uint64_t* pv_done = bars + 22;
+    uint64_t* o_free = bars + 24;      // [2]
+    uint64_t* drain = bars + 26;
+    uint32_t* tmem_slot = (uint32_t*)(bars + 27);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
-    const int qb = nqb - 1 - (int)blockIdx.x;     // heaviest query blocks first
-    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int items = nqb * BH;
     const int C = H * AT_HS;
-    const int nkv = qb + 1;                       // causal: key blocks 0..qb
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+            mbar_init(&o_free[i], 4);
+        }
         for (int s = 0; s < AT_SLOTS; s++) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
-        }
-        for (int i = 0; i < 2; i++) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&pv_done[i], 1);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -125,29 +133,37 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
     if (warp == 4) {
         if (lane == 0) {
             // ---------------- TMA producer
-            mbar_arrive_expect_tx(q_full, AT_TILE);
-            tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, qb * AT_BQ, b);
-            int nk = 0, nv = 0;
+            int g = 0, it = 0, nq = 0, nk = 0, nv = 0;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; j++) {
-                const int s = j % AT_SLOTS;
-                const uint32_t ph = (uint32_t)((j / AT_SLOTS) & 1);
-                if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&k_full[s], AT_TILE);
-                tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
-                nk++;
-                if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&v_full[s], AT_TILE);
-                tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
-                nv++;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
+                const int nkv = qb + 1;
+                const int qs = it & 1;
+                if (!mbar_wait(&q_empty[qs], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&q_full[qs], AT_TILE);
+                tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &q_full[qs], h * AT_HS, qb * AT_BQ, b);
+                nq++;
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % AT_SLOTS;
+                    const uint32_t ph = (uint32_t)((G / AT_SLOTS) & 1);
+                    if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&k_full[s], AT_TILE);
+                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
+                    nk++;
+                    if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&v_full[s], AT_TILE);
+                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                    nv++;
+                }
+                g += nkv;
             }
             if (!ok || *abort_flag) {
                 // wait (bounded) for every copy still in flight before the CTA exits
-                wait_bounded(q_full, 0);
-                for (int j = (nk > AT_SLOTS ? nk - AT_SLOTS : 0); j < nk; j++)
-                    wait_bounded(&k_full[j % AT_SLOTS], (uint32_t)((j / AT_SLOTS) & 1));
-                for (int j = (nv > AT_SLOTS ? nv - AT_SLOTS : 0); j < nv; j++)
-                    wait_bounded(&v_full[j % AT_SLOTS], (uint32_t)((j / AT_SLOTS) & 1));
+                for (int i = (nq > 2 ? nq - 2 : 0); i < nq; i++) wait_bounded(&q_full[i & 1], (uint32_t)((i >> 1) & 1));
+                for (int i = (nk > AT_SLOTS ? nk - AT_SLOTS : 0); i < nk; i++)
+                    wait_bounded(&k_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
+                for (int i = (nv > AT_SLOTS ? nv - AT_SLOTS : 0); i < nv; i++)
+                    wait_bounded(&v_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
             }
         }
     } else if (warp == 5) {
@@ -157,37 +173,47 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
             constexpr uint32_t id_o = make_idesc(AT_BQ, AT_HS, false, true);
             const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV),
                            p_addr = smem_u32(sP);
-            bool ok = mbar_wait(q_full, 0, abort_flag);
-            bool any = false;
-            for (int j = 0; j <= nkv && ok; j++) {
-                if (j < nkv) {
-                    const int s = j % AT_SLOTS, sb = j & 1;
-                    if (!mbar_wait(&k_full[s], (uint32_t)((j / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&s_empty[sb], (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int qb = nqb - 1 - w / BH;
+                const int nkv = qb + 1;
+                const int qs = it & 1, ob = it & 1;
+                if (!mbar_wait(&q_full[qs], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
+                for (int j = 0; j <= nkv && ok; j++) {
+                    if (j < nkv) {
+                        const int G = g + j, s = G % AT_SLOTS, sb = G & 1;
+                        if (!mbar_wait(&k_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&s_empty[sb], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < AT_HS / 16; kk++)
-                        mma_bf16(tmem_base + (uint32_t)(sb * AT_BK), smem_desc(q_addr + 32 * kk, 16, 1024),
-                                 smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                    mma_commit(&s_full[sb]);
-                    mma_commit(&k_empty[s]);
-                    any = true;
-                }
-                if (j >= 1) {
-                    const int i = j - 1, s = i % AT_SLOTS, pb = i & 1;
-                    if (!mbar_wait(&v_full[s], (uint32_t)((i / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&p_full[pb], (uint32_t)((i >> 1) & 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < AT_BK / 16; kk++) {
-                        const uint32_t a = p_addr + pb * AT_P_BYTES + (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t bb = v_addr + s * AT_TILE + kk * 2048;
-                        mma_bf16(tmem_base + TM_O, smem_desc(a, 16, 1024), smem_desc(bb, 8192, 1024), id_o,
-                                 (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < AT_HS / 16; kk++)
+                            mma_bf16(tmem_base + (uint32_t)(sb * AT_BK),
+                                     smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024),
+                                     smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        mma_commit(&s_full[sb]);
+                        mma_commit(&k_empty[s]);
+                        if (j == nkv - 1) mma_commit(&q_empty[qs]);
+                        any = true;
                     }
-                    mma_commit(&pv_done[pb]);
-                    mma_commit(&v_empty[s]);
+                    if (j >= 1) {
+                        const int i = j - 1, G = g + i, s = G % AT_SLOTS, pb = G & 1;
+                        if (i == 0 && !mbar_wait(&o_free[ob], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&v_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&p_full[pb], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < AT_BK / 16; kk++) {
+                            const uint32_t a = p_addr + pb * AT_P_BYTES + (kk >> 2) * 16384 + (kk & 3) * 32;
+                            const uint32_t bb = v_addr + s * AT_TILE + kk * 2048;
+                            mma_bf16(tmem_base + TM_O + ob * AT_HS, smem_desc(a, 16, 1024),
+                                     smem_desc(bb, 8192, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&pv_done[pb]);
+                        mma_commit(&v_empty[s]);
+                    }
                 }
+                g += nkv;
             }
             if (any) {
                 mma_commit(drain);
@@ -197,110 +223,120 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
     } else {
         // ---------------- softmax warps 0..3: thread r owns query row r (TMEM lane r)
         const int r = threadIdx.x;
-        const int q = qb * AT_BQ + r;
         const float sl2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
-        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv; j++) {
-            const int sb = j & 1;
-            ok = mbar_wait(&s_full[sb], (uint32_t)((j >> 1) & 1), abort_flag);
+        int g = 0, it = 0;
+        for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+            const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
+            const int nkv = qb + 1;
+            const int q = qb * AT_BQ + r;
+            const int ob = it & 1;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nkv; j++) {
+                const int G = g + j, sb = G & 1;
+                ok = mbar_wait(&s_full[sb], (uint32_t)((G >> 1) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[128];
+#pragma unroll
+                for (int c = 0; c < 4; c++) tmem_ld32_nowait(lane_base + (uint32_t)(sb * AT_BK + 32 * c), sr + 32 * c);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                // mask (raw scores; the scale is applied in the exponent), row max
+                // as eight independent partial maxima
+                const int key0 = j * AT_BK;
+                const bool edge = (j == qb) || (key0 + AT_BK > T);
+                if (edge) {
+#pragma unroll
+                    for (int i = 0; i < 128; i++)
+                        if (key0 + i > q || key0 + i >= T) sr[i] = __float_as_uint(-INFINITY);
+                }
+                float pm[8];
+#pragma unroll
+                for (int t = 0; t < 8; t++) pm[t] = __uint_as_float(sr[t]);
+#pragma unroll
+                for (int i = 8; i < 128; i++) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sr[i]));
+                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl2;
+                const float m_new = fmaxf(m_run, mx);
+                const bool resc = (j > 0) && (m_new > m_run + 8.f);
+                if (j == 0) m_run = m_new;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // rescale the O row once the previous P V product has landed
+                    ok = mbar_wait(&pv_done[(G - 1) & 1], (uint32_t)(((G - 1) >> 1) & 1), abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
+                    const float f = resc ? ex2f(m_run - m_new) : 1.f;
+                    const uint32_t oaddr = lane_base + TM_O + ob * AT_HS;
+                    uint32_t o[64];
+                    tmem_ld32_nowait(oaddr, o);
+                    tmem_ld32_nowait(oaddr + 32, o + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 64; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                    tmem_st32(oaddr, o);
+                    tmem_st32(oaddr + 32, o + 32);
+                    if (resc) {
+                        l_run *= f;
+                        m_run = m_new;
+                    }
+                }
+                // the P buffer is free once the product that read it (two blocks ago) is done
+                if (G >= 2) {
+                    ok = mbar_wait(&pv_done[sb], (uint32_t)(((G - 2) >> 1) & 1), abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                }
+                float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint8_t* pbuf = sP + sb * AT_P_BYTES + r * 128;
+#pragma unroll
+                for (int kb2 = 0; kb2 < 2; kb2++) {
+#pragma unroll
+                    for (int pq = 0; pq < 8; pq++) {
+                        float e[8];
+#pragma unroll
+                        for (int t = 0; t < 8; t++) {
+                            e[t] = ex2f(fmaf(__uint_as_float(sr[kb2 * 64 + pq * 8 + t]), sl2, -m_run));
+                            ps[t] += e[t];
+                        }
+                        uint4 wv = make_uint4(pack2_bf16(e[0], e[1]), pack2_bf16(e[2], e[3]),
+                                              pack2_bf16(e[4], e[5]), pack2_bf16(e[6], e[7]));
+                        *(uint4*)(pbuf + kb2 * 16384 + ((pq ^ (r & 7)) << 4)) = wv;
+                    }
+                }
+                l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[sb]);
+            }
+            if (!ok) break;
+            // the item's output: O / l and lse, once its last P V product is done
+            const int GL = g + nkv - 1;
+            ok = mbar_wait(&pv_done[GL & 1], (uint32_t)((GL >> 1) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            uint32_t sr[128];
-#pragma unroll
-            for (int c = 0; c < 4; c++) tmem_ld32_nowait(lane_base + (uint32_t)(sb * AT_BK + 32 * c), sr + 32 * c);
+            uint32_t o[64];
+            tmem_ld32_nowait(lane_base + TM_O + ob * AT_HS, o);
+            tmem_ld32_nowait(lane_base + TM_O + ob * AT_HS + 32, o + 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[sb]);
-            // mask (raw scores; the scale is applied in the exponent), row max
-            // as eight independent partial maxima
-            const int key0 = j * AT_BK;
-            const bool edge = (j == qb) || (key0 + AT_BK > T);
-            if (edge) {
+            if (lane == 0) mbar_arrive(&o_free[ob]);
+            if (q < T) {
+                const float inv = 1.f / l_run;
+                uint4* orow = (uint4*)(out + ((int64_t)b * T + q) * C + h * AT_HS);
 #pragma unroll
-                for (int i = 0; i < 128; i++)
-                    if (key0 + i > q || key0 + i >= T) sr[i] = __float_as_uint(-INFINITY);
-            }
-            float pm[8];
-#pragma unroll
-            for (int t = 0; t < 8; t++) pm[t] = __uint_as_float(sr[t]);
-#pragma unroll
-            for (int i = 8; i < 128; i++) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sr[i]));
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl2;
-            const float m_new = fmaxf(m_run, mx);
-            const bool resc = (j > 0) && (m_new > m_run + 8.f);
-            if (j == 0) m_run = m_new;
-            if (__any_sync(0xffffffffu, resc)) {
-                // rescale the O row once the previous P V product has landed
-                ok = mbar_wait(&pv_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();
-                const float f = resc ? ex2f(m_run - m_new) : 1.f;
-                uint32_t o[64];
-                tmem_ld32_nowait(lane_base + TM_O, o);
-                tmem_ld32_nowait(lane_base + TM_O + 32, o + 32);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 64; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                tmem_st32(lane_base + TM_O, o);
-                tmem_st32(lane_base + TM_O + 32, o + 32);
-                if (resc) {
-                    l_run *= f;
-                    m_run = m_new;
+                for (int c = 0; c < 8; c++) {
+                    const float* f = (const float*)&o[8 * c];
+                    orow[c] = make_uint4(pack2_bf16(f[0] * inv, f[1] * inv), pack2_bf16(f[2] * inv, f[3] * inv),
+                                         pack2_bf16(f[4] * inv, f[5] * inv), pack2_bf16(f[6] * inv, f[7] * inv));
                 }
+                lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
             }
-            // the P buffer is free once the product that read it (two blocks ago) is done
-            if (j >= 2) {
-                ok = mbar_wait(&pv_done[sb], (uint32_t)(((j - 2) >> 1) & 1), abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            }
-            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint8_t* pbuf = sP + sb * AT_P_BYTES + r * 128;
-#pragma unroll
-            for (int kb2 = 0; kb2 < 2; kb2++) {
-#pragma unroll
-                for (int pq = 0; pq < 8; pq++) {
-                    float e[8];
-#pragma unroll
-                    for (int t = 0; t < 8; t++) {
-                        e[t] = ex2f(fmaf(__uint_as_float(sr[kb2 * 64 + pq * 8 + t]), sl2, -m_run));
-                        ps[t] += e[t];
-                    }
-                    uint4 w = make_uint4(pack2_bf16(e[0], e[1]), pack2_bf16(e[2], e[3]),
-                                         pack2_bf16(e[4], e[5]), pack2_bf16(e[6], e[7]));
-                    *(uint4*)(pbuf + kb2 * 16384 + ((pq ^ (r & 7)) << 4)) = w;
-                }
-            }
-            const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            l_run += sum;
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[sb]);
-        }
-        if (ok) {
-            ok = mbar_wait(&pv_done[(nkv - 1) & 1], (uint32_t)(((nkv - 1) >> 1) & 1), abort_flag);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-                uint32_t o[64];
-                tmem_ld32_nowait(lane_base + TM_O, o);
-                tmem_ld32_nowait(lane_base + TM_O + 32, o + 32);
-                tmem_wait_ld();
-                if (q < T) {
-                    const float inv = 1.f / l_run;
-                    uint4* orow = (uint4*)(out + ((int64_t)b * T + q) * C + h * AT_HS);
-#pragma unroll
-                    for (int c = 0; c < 8; c++) {
-                        const float* f = (const float*)&o[8 * c];
-                        orow[c] = make_uint4(pack2_bf16(f[0] * inv, f[1] * inv), pack2_bf16(f[2] * inv, f[3] * inv),
-                                             pack2_bf16(f[4] * inv, f[5] * inv), pack2_bf16(f[6] * inv, f[7] * inv));
-                    }
-                    lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
-                }
-            }
+            g += nkv;
         }
     }
     __syncthreads();
@@ -361,8 +397,9 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
                                      (int)AT_SMEM));
         attr = true;
     }
-    dim3 grid((T + AT_BQ - 1) / AT_BQ, B * H);
-    fa_tc_fwd_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, st);
+    const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
+    const int grid = items < num_sms() ? items : num_sms();
+    fa_tc_fwd_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, B * H, st);
     return cudaGetLastError();
 }
 
@@ -371,8 +408,8 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
 // recomputed from the forward's lse, D = rowsum(dO * O) comes from a pre-pass.
 // With s the raw score q.k, p = exp(s/sqrt(hs) - lse), dP = dO V^T,
 // dS = P * (dP - D) (the gradient of the scaled scores):
-//   dK = dS^T Q / sqrt(hs), dV = P^T dO   (one CTA per 128-key block)
-//   dQ = dS K / sqrt(hs)                  (one CTA per 128-query block)
+//   dK = dS^T Q / sqrt(hs), dV = P^T dO   (work item: one 128-key block)
+//   dQ = dS K / sqrt(hs)                  (work item: one 128-query block)
 // Both kernels keep the two 128x128 products (S and dP, or their transposes)
 // in TMEM, write the bf16 operands of the accumulating products (P^T and
 // dS^T, or dS) to shared memory in the K-major 128B-swizzled layout, and
@@ -380,28 +417,29 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
 
 namespace {
 
-constexpr int BW_SLOTS = 3;
-// dK/dV kernel
-constexpr int KV_OFF_K = 0;
-constexpr int KV_OFF_V = KV_OFF_K + AT_TILE;
-constexpr int KV_OFF_Q = KV_OFF_V + AT_TILE;
-constexpr int KV_OFF_DO = KV_OFF_Q + BW_SLOTS * AT_TILE;
-constexpr int KV_OFF_PT = KV_OFF_DO + BW_SLOTS * AT_TILE;
+// dK/dV kernel: K and V double buffered per item, Q and dO in a 2-slot ring
+constexpr int KV_OFF_K = 0;                                  // [2]
+constexpr int KV_OFF_V = KV_OFF_K + 2 * AT_TILE;             // [2]
+constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [2]
+constexpr int KV_OFF_DO = KV_OFF_Q + 2 * AT_TILE;            // [2]
+constexpr int KV_OFF_PT = KV_OFF_DO + 2 * AT_TILE;
 constexpr int KV_OFF_DST = KV_OFF_PT + AT_P_BYTES;
 constexpr int KV_OFF_LD = KV_OFF_DST + AT_P_BYTES;        // lse2[2][128], D[2][128]
 constexpr int KV_OFF_BAR = KV_OFF_LD + 4 * 128 * 4;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
-// dQ kernel
-constexpr int DQ_OFF_Q = 0;
-constexpr int DQ_OFF_DO = DQ_OFF_Q + AT_TILE;
-constexpr int DQ_OFF_K = DQ_OFF_DO + AT_TILE;
+// dQ kernel: Q and dO double buffered per item, K and V in 3-slot rings
+constexpr int BW_SLOTS = 3;
+constexpr int DQ_OFF_Q = 0;                                  // [2]
+constexpr int DQ_OFF_DO = DQ_OFF_Q + 2 * AT_TILE;            // [2]
+constexpr int DQ_OFF_K = DQ_OFF_DO + 2 * AT_TILE;
 constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;
 constexpr int DQ_OFF_DS = DQ_OFF_V + BW_SLOTS * AT_TILE;
 constexpr int DQ_OFF_BAR = DQ_OFF_DS + AT_P_BYTES;
 constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
-// TMEM columns of both kernels: S (or S^T) 0..127, dP 128..255, the two
-// accumulators at 256 and 320
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_A0 = 256, TM_A1 = 320;
+// TMEM columns of both kernels: S (or S^T) 0..127, dP 128..255, then the
+// accumulators of two consecutive work items: dV, dK at 256 + 128*(it&1)
+// (+64), or dQ at 256 + 64*(it&1)
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
 // 32 fp32 values of one row as bf16 into a K-major 128B-swizzled operand tile
@@ -429,14 +467,16 @@ __device__ __forceinline__ void store_row64(bf16* dst, const uint32_t (&a)[64], 
     }
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 }  // namespace
 
+// Persistent like the forward: work items (key block kb, b, h), fewest key
+// blocks last (kb = w / (B*H)); g counts query blocks over all items, `it`
+// counts items (K/V buffers and the dV/dK accumulator pair alternate).
 __global__ void __launch_bounds__(AT_THREADS, 1)
 fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                      const float* __restrict__ lse, const float* __restrict__ Dg,
-                     bf16* __restrict__ dqkv, int T, int H, DevState* st) {
+                     bf16* __restrict__ dqkv, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sK = smem + KV_OFF_K;
@@ -448,35 +488,41 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     float* sL = (float*)(smem + KV_OFF_LD);          // [2][128] lse in log2 units
     float* sD = sL + 256;                              // [2][128]
     uint64_t* bars = (uint64_t*)(smem + KV_OFF_BAR);
-    uint64_t* kv_full = bars;
-    uint64_t* qd_full = bars + 1;                      // [3]
-    uint64_t* qd_empty = bars + 4;                     // [3]
-    uint64_t* st_full = bars + 7;
-    uint64_t* st_free = bars + 8;
-    uint64_t* ps_full = bars + 9;
-    uint64_t* ps_free = bars + 10;
-    uint64_t* done = bars + 11;
-    uint32_t* tmem_slot = (uint32_t*)(bars + 12);
+    uint64_t* kv_full = bars;                          // [2]
+    uint64_t* kv_empty = bars + 2;                     // [2]
+    uint64_t* qd_full = bars + 4;                      // [2]
+    uint64_t* qd_empty = bars + 6;                     // [2]
+    uint64_t* st_full = bars + 8;
+    uint64_t* st_free = bars + 9;
+    uint64_t* ps_full = bars + 10;
+    uint64_t* ps_free = bars + 11;
+    uint64_t* acc_full = bars + 12;                    // [2]
+    uint64_t* acc_free = bars + 14;                    // [2]
+    uint64_t* drain = bars + 16;
+    uint64_t* ld_full = bars + 17;                     // [2] lse/D staged (one arrive per warp)
+    uint32_t* tmem_slot = (uint32_t*)(bars + 19);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nb = (T + AT_BK - 1) / AT_BK;
-    const int kb = (int)blockIdx.x;                   // key block
-    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int items = nb * BH;
     const int C = H * AT_HS;
-    const int n = nb - kb;                            // query blocks kb..nb-1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(kv_full, 1);
-        for (int s = 0; s < BW_SLOTS; s++) {
-            mbar_init(&qd_full[s], 1);
-            mbar_init(&qd_empty[s], 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&qd_full[i], 1);
+            mbar_init(&qd_empty[i], 1);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_free[i], 4);
+            mbar_init(&ld_full[i], 4);
         }
         mbar_init(st_full, 1);
         mbar_init(st_free, 4);
         mbar_init(ps_full, 4);
         mbar_init(ps_free, 1);
-        mbar_init(done, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -489,23 +535,30 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     if (warp == 4) {
         if (lane == 0) {
             // ---------------- TMA producer
-            mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
-            tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, kb * AT_BK, b);
-            tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, kb * AT_BK, b);
-            int issued = 0;
+            int g = 0, it = 0, nkvl = 0, nql = 0;
             bool ok = true;
-            for (int i = 0; i < n; i++) {
-                const int s = i % BW_SLOTS;
-                if (!mbar_wait(&qd_empty[s], (uint32_t)(((i / BW_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&qd_full[s], 2 * AT_TILE);
-                tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &qd_full[s], h * AT_HS, (kb + i) * AT_BQ, b);
-                tma_load_3d(sDO + s * AT_TILE, &tm_do, &qd_full[s], h * AT_HS, (kb + i) * AT_BQ, b);
-                issued++;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
+                const int n = nb - kb;
+                const int ks = it & 1;
+                if (!mbar_wait(&kv_empty[ks], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&kv_full[ks], 2 * AT_TILE);
+                tma_load_3d(sK + ks * AT_TILE, &tm_qkv, &kv_full[ks], C + h * AT_HS, kb * AT_BK, b);
+                tma_load_3d(sV + ks * AT_TILE, &tm_qkv, &kv_full[ks], 2 * C + h * AT_HS, kb * AT_BK, b);
+                nkvl++;
+                for (int i = 0; i < n; i++) {
+                    const int G = g + i, qs = G & 1;
+                    if (!mbar_wait(&qd_empty[qs], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&qd_full[qs], 2 * AT_TILE);
+                    tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
+                    tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
+                    nql++;
+                }
+                g += n;
             }
             if (!ok || *abort_flag) {
-                wait_bounded(kv_full, 0);
-                for (int i = (issued > BW_SLOTS ? issued - BW_SLOTS : 0); i < issued; i++)
-                    wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
+                for (int i = (nkvl > 2 ? nkvl - 2 : 0); i < nkvl; i++) wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1));
+                for (int i = (nql > 2 ? nql - 2 : 0); i < nql; i++) wait_bounded(&qd_full[i & 1], (uint32_t)((i >> 1) & 1));
             }
         }
     } else if (warp == 5) {
@@ -515,111 +568,140 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
             const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
                            do_addr = smem_u32(sDO), pt_addr = smem_u32(sPT), dst_addr = smem_u32(sDST);
-            bool ok = mbar_wait(kv_full, 0, abort_flag);
-            for (int i = 0; i <= n && ok; i++) {
-                if (i < n) {
-                    const int s = i % BW_SLOTS;
-                    if (!mbar_wait(&qd_full[s], (uint32_t)((i / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(st_free, (uint32_t)((i & 1) ^ 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int kb = w / BH;
+                const int n = nb - kb;
+                const int ks = it & 1, ab = it & 1;
+                const uint32_t tdv = TM_ACC + ab * 128, tdk = tdv + 64;
+                if (!mbar_wait(&kv_full[ks], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
+                for (int i = 0; i <= n && ok; i++) {
+                    if (i < n) {
+                        const int G = g + i, qs = G & 1;
+                        if (!mbar_wait(&qd_full[qs], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < AT_HS / 16; kk++) {
-                        // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = head dim)
-                        mma_bf16(tmem_base + TM_S, smem_desc(k_addr + 32 * kk, 16, 1024),
-                                 smem_desc(q_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                        mma_bf16(tmem_base + TM_DP, smem_desc(v_addr + 32 * kk, 16, 1024),
-                                 smem_desc(do_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < AT_HS / 16; kk++) {
+                            // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = head dim)
+                            mma_bf16(tmem_base + TM_S, smem_desc(k_addr + ks * AT_TILE + 32 * kk, 16, 1024),
+                                     smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_DP, smem_desc(v_addr + ks * AT_TILE + 32 * kk, 16, 1024),
+                                     smem_desc(do_addr + qs * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(st_full);
+                        if (i == n - 1) mma_commit(&kv_empty[ks]);
+                        any = true;
                     }
-                    mma_commit(st_full);
-                }
-                if (i >= 1) {
-                    const int ii = i - 1, s = ii % BW_SLOTS;
-                    if (!mbar_wait(ps_full, (uint32_t)(ii & 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                    if (i >= 1) {
+                        const int ii = i - 1, G = g + ii, qs = G & 1;
+                        if (ii == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(ps_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < AT_BQ / 16; kk++) {
-                        // dV += P^T dO, dK += dS^T Q (K = queries; dO and Q read MN-major)
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-                        mma_bf16(tmem_base + TM_A0, smem_desc(pt_addr + off, 16, 1024),
-                                 smem_desc(do_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
-                        mma_bf16(tmem_base + TM_A1, smem_desc(dst_addr + off, 16, 1024),
-                                 smem_desc(q_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                        for (int kk = 0; kk < AT_BQ / 16; kk++) {
+                            // dV += P^T dO, dK += dS^T Q (K = queries; dO and Q read MN-major)
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
+                            mma_bf16(tmem_base + tdv, smem_desc(pt_addr + off, 16, 1024),
+                                     smem_desc(do_addr + qs * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                            mma_bf16(tmem_base + tdk, smem_desc(dst_addr + off, 16, 1024),
+                                     smem_desc(q_addr + qs * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                        }
+                        mma_commit(ps_free);
+                        mma_commit(&qd_empty[qs]);
+                        if (ii == n - 1) mma_commit(&acc_full[ab]);
                     }
-                    mma_commit(ps_free);
-                    mma_commit(&qd_empty[s]);
                 }
+                g += n;
             }
-            // every product issued so far completes before `done` (also on abort)
-            mma_commit(done);
-            if (!ok) wait_bounded(done, 0);
+            if (any) {
+                mma_commit(drain);
+                wait_bounded(drain, 0);
+            }
         }
     } else {
         // ---------------- warps 0..3: thread r owns key row r (TMEM lane r)
         const int r = threadIdx.x;
-        const int key = kb * AT_BK + r;
         const float sl2 = LOG2E_F * 0.125f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
-        for (int i = 0; i < n; i++) {
-            const int q0 = (kb + i) * AT_BQ, ls = i & 1;
-            {
-                const int q = q0 + r;
-                sL[ls * 128 + r] = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
-                sD[ls * 128 + r] = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+        int g = 0, it = 0;
+        for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+            const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
+            const int n = nb - kb;
+            const int key = kb * AT_BK + r;
+            const int ab = it & 1;
+            for (int i = 0; i < n; i++) {
+                const int G = g + i, ls = G & 1;
+                const int q0 = (kb + i) * AT_BQ;
+                {
+                    const int q = q0 + r;
+                    sL[ls * 128 + r] = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
+                    sD[ls * 128 + r] = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+                }
+                // every warp has staged its 32 rows (and, having passed the previous
+                // block's wait, every warp is done reading this slot's old values)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ld_full[ls]);
+                ok = mbar_wait(&ld_full[ls], (uint32_t)((G >> 1) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                ok = mbar_wait(ps_free, (uint32_t)((G & 1) ^ 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const float* L = sL + ls * 128;
+                const float* Dq = sD + ls * 128;
+#pragma unroll 1
+                for (int c = 0; c < 4; c++) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
+                    tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
+                    tmem_wait_ld();
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(st_free);
+                    }
+                    float pv[32], dsv[32];
+#pragma unroll
+                    for (int t = 0; t < 32; t++) {
+                        const int qq = 32 * c + t;
+                        float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -L[qq]));
+                        if (i == 0 && qq < r) p = 0.f;          // query before key: masked
+                        pv[t] = p;
+                        dsv[t] = p * (__uint_as_float(dr[t]) - Dq[qq]);
+                    }
+                    put_row_chunk(sPT, r, c, pv);
+                    put_row_chunk(sDST, r, c, dsv);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ps_full);
             }
-            softmax_bar();
-            ok = mbar_wait(st_full, (uint32_t)(i & 1), abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            ok = mbar_wait(ps_free, (uint32_t)((i & 1) ^ 1), abort_flag);
+            if (!ok) break;
+            ok = mbar_wait(&acc_full[ab], (uint32_t)((it >> 1) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const float* L = sL + ls * 128;
-            const float* Dq = sD + ls * 128;
-#pragma unroll 1
-            for (int c = 0; c < 4; c++) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
-                tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
-                tmem_wait_ld();
-                if (c == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(st_free);
-                }
-                float pv[32], dsv[32];
-#pragma unroll
-                for (int t = 0; t < 32; t++) {
-                    const int qq = 32 * c + t;
-                    float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -L[qq]));
-                    if (i == 0 && qq < r) p = 0.f;          // query before key: masked
-                    pv[t] = p;
-                    dsv[t] = p * (__uint_as_float(dr[t]) - Dq[qq]);
-                }
-                put_row_chunk(sPT, r, c, pv);
-                put_row_chunk(sDST, r, c, dsv);
-            }
-            fence_async_smem();
+            uint32_t dv[64], dk[64];
+            const uint32_t tdv = lane_base + TM_ACC + ab * 128;
+            tmem_ld32_nowait(tdv, dv);
+            tmem_ld32_nowait(tdv + 32, dv + 32);
+            tmem_ld32_nowait(tdv + 64, dk);
+            tmem_ld32_nowait(tdv + 96, dk + 32);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(ps_full);
-        }
-        if (ok) {
-            ok = mbar_wait(done, 0, abort_flag);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-                uint32_t dv[64], dk[64];
-                tmem_ld32_nowait(lane_base + TM_A0, dv);
-                tmem_ld32_nowait(lane_base + TM_A0 + 32, dv + 32);
-                tmem_ld32_nowait(lane_base + TM_A1, dk);
-                tmem_ld32_nowait(lane_base + TM_A1 + 32, dk + 32);
-                tmem_wait_ld();
-                if (key < T) {
-                    bf16* row = dqkv + ((int64_t)b * T + key) * 3 * C + h * AT_HS;
-                    store_row64(row + C, dk, 0.125f);
-                    store_row64(row + 2 * C, dv, 1.f);
-                }
+            if (lane == 0) mbar_arrive(&acc_free[ab]);
+            if (key < T) {
+                bf16* row = dqkv + ((int64_t)b * T + key) * 3 * C + h * AT_HS;
+                store_row64(row + C, dk, 0.125f);
+                store_row64(row + 2 * C, dv, 1.f);
             }
+            g += n;
         }
     }
     __syncthreads();
@@ -633,10 +715,11 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     }
 }
 
+// Persistent: work items (query block qb, b, h), heaviest first.
 __global__ void __launch_bounds__(AT_THREADS, 1)
 fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                     const float* __restrict__ lse, const float* __restrict__ Dg,
-                    bf16* __restrict__ dqkv, int T, int H, DevState* st) {
+                    bf16* __restrict__ dqkv, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + DQ_OFF_Q;
@@ -645,28 +728,34 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     uint8_t* sV = smem + DQ_OFF_V;
     uint8_t* sDS = smem + DQ_OFF_DS;
     uint64_t* bars = (uint64_t*)(smem + DQ_OFF_BAR);
-    uint64_t* qd_full = bars;
-    uint64_t* k_full = bars + 1;                       // [3]
-    uint64_t* k_empty = bars + 4;
-    uint64_t* v_full = bars + 7;
-    uint64_t* v_empty = bars + 10;
-    uint64_t* st_full = bars + 13;
-    uint64_t* st_free = bars + 14;
-    uint64_t* ds_full = bars + 15;
-    uint64_t* ds_free = bars + 16;
-    uint64_t* done = bars + 17;
-    uint32_t* tmem_slot = (uint32_t*)(bars + 18);
+    uint64_t* qd_full = bars;                          // [2]
+    uint64_t* qd_empty = bars + 2;                     // [2]
+    uint64_t* k_full = bars + 4;                       // [3]
+    uint64_t* k_empty = bars + 7;
+    uint64_t* v_full = bars + 10;
+    uint64_t* v_empty = bars + 13;
+    uint64_t* st_full = bars + 16;
+    uint64_t* st_free = bars + 17;
+    uint64_t* ds_full = bars + 18;
+    uint64_t* ds_free = bars + 19;
+    uint64_t* acc_full = bars + 20;                    // [2]
+    uint64_t* acc_free = bars + 22;                    // [2]
+    uint64_t* drain = bars + 24;
+    uint32_t* tmem_slot = (uint32_t*)(bars + 25);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
-    const int qb = nqb - 1 - (int)blockIdx.x;         // heaviest query blocks first
-    const int bh = blockIdx.y, h = bh % H, b = bh / H;
+    const int items = nqb * BH;
     const int C = H * AT_HS;
-    const int nkv = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(qd_full, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&qd_full[i], 1);
+            mbar_init(&qd_empty[i], 1);
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_free[i], 4);
+        }
         for (int s = 0; s < BW_SLOTS; s++) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -677,7 +766,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
         mbar_init(st_free, 4);
         mbar_init(ds_full, 4);
         mbar_init(ds_free, 1);
-        mbar_init(done, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -690,29 +779,37 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     if (warp == 4) {
         if (lane == 0) {
             // ---------------- TMA producer
-            mbar_arrive_expect_tx(qd_full, 2 * AT_TILE);
-            tma_load_3d(sQ, &tm_qkv, qd_full, h * AT_HS, qb * AT_BQ, b);
-            tma_load_3d(sDO, &tm_do, qd_full, h * AT_HS, qb * AT_BQ, b);
-            int nk = 0, nv = 0;
+            int g = 0, it = 0, nql = 0, nk = 0, nv = 0;
             bool ok = true;
-            for (int j = 0; j < nkv && ok; j++) {
-                const int s = j % BW_SLOTS;
-                const uint32_t ph = (uint32_t)((j / BW_SLOTS) & 1);
-                if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&k_full[s], AT_TILE);
-                tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
-                nk++;
-                if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&v_full[s], AT_TILE);
-                tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
-                nv++;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
+                const int nkv = qb + 1;
+                const int qs = it & 1;
+                if (!mbar_wait(&qd_empty[qs], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                mbar_arrive_expect_tx(&qd_full[qs], 2 * AT_TILE);
+                tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, qb * AT_BQ, b);
+                tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, qb * AT_BQ, b);
+                nql++;
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % BW_SLOTS;
+                    const uint32_t ph = (uint32_t)((G / BW_SLOTS) & 1);
+                    if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&k_full[s], AT_TILE);
+                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
+                    nk++;
+                    if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&v_full[s], AT_TILE);
+                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                    nv++;
+                }
+                g += nkv;
             }
             if (!ok || *abort_flag) {
-                wait_bounded(qd_full, 0);
-                for (int j = (nk > BW_SLOTS ? nk - BW_SLOTS : 0); j < nk; j++)
-                    wait_bounded(&k_full[j % BW_SLOTS], (uint32_t)((j / BW_SLOTS) & 1));
-                for (int j = (nv > BW_SLOTS ? nv - BW_SLOTS : 0); j < nv; j++)
-                    wait_bounded(&v_full[j % BW_SLOTS], (uint32_t)((j / BW_SLOTS) & 1));
+                for (int i = (nql > 2 ? nql - 2 : 0); i < nql; i++) wait_bounded(&qd_full[i & 1], (uint32_t)((i >> 1) & 1));
+                for (int i = (nk > BW_SLOTS ? nk - BW_SLOTS : 0); i < nk; i++)
+                    wait_bounded(&k_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
+                for (int i = (nv > BW_SLOTS ? nv - BW_SLOTS : 0); i < nv; i++)
+                    wait_bounded(&v_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
             }
         }
     } else if (warp == 5) {
@@ -722,98 +819,121 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
             const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), k_addr = smem_u32(sK),
                            v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
-            bool ok = mbar_wait(qd_full, 0, abort_flag);
-            for (int j = 0; j <= nkv && ok; j++) {
-                if (j < nkv) {
-                    const int s = j % BW_SLOTS;
-                    const uint32_t ph = (uint32_t)((j / BW_SLOTS) & 1);
-                    if (!mbar_wait(&k_full[s], ph, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&v_full[s], ph, abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(st_free, (uint32_t)((j & 1) ^ 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int qb = nqb - 1 - w / BH;
+                const int nkv = qb + 1;
+                const int qs = it & 1, ab = it & 1;
+                if (!mbar_wait(&qd_full[qs], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
+                for (int j = 0; j <= nkv && ok; j++) {
+                    if (j < nkv) {
+                        const int G = g + j, s = G % BW_SLOTS;
+                        const uint32_t ph = (uint32_t)((G / BW_SLOTS) & 1);
+                        if (!mbar_wait(&k_full[s], ph, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&v_full[s], ph, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < AT_HS / 16; kk++) {
-                        // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = head dim)
-                        mma_bf16(tmem_base + TM_S, smem_desc(q_addr + 32 * kk, 16, 1024),
-                                 smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                        mma_bf16(tmem_base + TM_DP, smem_desc(do_addr + 32 * kk, 16, 1024),
-                                 smem_desc(v_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < AT_HS / 16; kk++) {
+                            // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = head dim)
+                            mma_bf16(tmem_base + TM_S, smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024),
+                                     smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_DP, smem_desc(do_addr + qs * AT_TILE + 32 * kk, 16, 1024),
+                                     smem_desc(v_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(st_full);
+                        mma_commit(&v_empty[s]);
+                        if (j == nkv - 1) mma_commit(&qd_empty[qs]);
+                        any = true;
                     }
-                    mma_commit(st_full);
-                    mma_commit(&v_empty[s]);
-                }
-                if (j >= 1) {
-                    const int jj = j - 1, s = jj % BW_SLOTS;
-                    if (!mbar_wait(ds_full, (uint32_t)(jj & 1), abort_flag)) { ok = false; break; }
-                    tc_fence_after();
+                    if (j >= 1) {
+                        const int jj = j - 1, G = g + jj, s = G % BW_SLOTS;
+                        if (jj == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(ds_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < AT_BK / 16; kk++) {
-                        // dQ += dS K (K = keys; K read MN-major)
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_bf16(tmem_base + TM_A0, smem_desc(ds_addr + off, 16, 1024),
-                                 smem_desc(k_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a,
-                                 (jj > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < AT_BK / 16; kk++) {
+                            // dQ += dS K (K = keys; K read MN-major)
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_bf16(tmem_base + TM_ACC + ab * AT_HS, smem_desc(ds_addr + off, 16, 1024),
+                                     smem_desc(k_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a,
+                                     (jj > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(ds_free);
+                        mma_commit(&k_empty[s]);
+                        if (jj == nkv - 1) mma_commit(&acc_full[ab]);
                     }
-                    mma_commit(ds_free);
-                    mma_commit(&k_empty[s]);
                 }
+                g += nkv;
             }
-            mma_commit(done);
-            if (!ok) wait_bounded(done, 0);
+            if (any) {
+                mma_commit(drain);
+                wait_bounded(drain, 0);
+            }
         }
     } else {
         // ---------------- warps 0..3: thread r owns query row r (TMEM lane r)
         const int r = threadIdx.x;
-        const int q = qb * AT_BQ + r;
         const float sl2 = LOG2E_F * 0.125f;
-        const float lse2 = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
-        const float Dq = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
-        for (int j = 0; j < nkv; j++) {
-            ok = mbar_wait(st_full, (uint32_t)(j & 1), abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            ok = mbar_wait(ds_free, (uint32_t)((j & 1) ^ 1), abort_flag);
+        int g = 0, it = 0;
+        for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+            const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
+            const int nkv = qb + 1;
+            const int q = qb * AT_BQ + r;
+            const int ab = it & 1;
+            const float lse2 = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
+            const float Dq = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+            for (int j = 0; j < nkv; j++) {
+                const int G = g + j;
+                ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                ok = mbar_wait(ds_free, (uint32_t)((G & 1) ^ 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const int key0 = j * AT_BK;
+                const bool edge = (j == qb) || (key0 + AT_BK > T);
+#pragma unroll 1
+                for (int c = 0; c < 4; c++) {
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
+                    tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
+                    tmem_wait_ld();
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(st_free);
+                    }
+                    float dsv[32];
+#pragma unroll
+                    for (int t = 0; t < 32; t++) {
+                        const int kk = key0 + 32 * c + t;
+                        float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -lse2));
+                        if (edge && (kk > q || kk >= T)) p = 0.f;
+                        dsv[t] = p * (__uint_as_float(dr[t]) - Dq);
+                    }
+                    put_row_chunk(sDS, r, c, dsv);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
+            }
+            if (!ok) break;
+            ok = mbar_wait(&acc_full[ab], (uint32_t)((it >> 1) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            const int key0 = j * AT_BK;
-            const bool edge = (j == qb) || (key0 + AT_BK > T);
-#pragma unroll 1
-            for (int c = 0; c < 4; c++) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
-                tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
-                tmem_wait_ld();
-                if (c == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(st_free);
-                }
-                float dsv[32];
-#pragma unroll
-                for (int t = 0; t < 32; t++) {
-                    const int kk = key0 + 32 * c + t;
-                    float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -lse2));
-                    if (edge && (kk > q || kk >= T)) p = 0.f;
-                    dsv[t] = p * (__uint_as_float(dr[t]) - Dq);
-                }
-                put_row_chunk(sDS, r, c, dsv);
-            }
-            fence_async_smem();
+            uint32_t dq[64];
+            tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS, dq);
+            tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS + 32, dq + 32);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(ds_full);
-        }
-        if (ok) {
-            ok = mbar_wait(done, 0, abort_flag);
-            if (__all_sync(0xffffffffu, ok)) {
-                tc_fence_after();
-                uint32_t dq[64];
-                tmem_ld32_nowait(lane_base + TM_A0, dq);
-                tmem_ld32_nowait(lane_base + TM_A0 + 32, dq + 32);
-                tmem_wait_ld();
-                if (q < T) store_row64(dqkv + ((int64_t)b * T + q) * 3 * C + h * AT_HS, dq, 0.125f);
-            }
+            if (lane == 0) mbar_arrive(&acc_free[ab]);
+            if (q < T) store_row64(dqkv + ((int64_t)b * T + q) * 3 * C + h * AT_HS, dq, 0.125f);
+            g += nkv;
         }
     }
     __syncthreads();
@@ -858,10 +978,11 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse
                                      (int)DQ_SMEM));
         attr = true;
     }
-    dim3 grid((T + AT_BQ - 1) / AT_BQ, B * H);
-    fa_tc_bwd_dkv_kernel<<<grid, AT_THREADS, KV_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, st);
+    const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
+    const int grid = items < num_sms() ? items : num_sms();
+    fa_tc_bwd_dkv_kernel<<<grid, AT_THREADS, KV_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, B * H, st);
     CUDA_OK(cudaGetLastError());
-    fa_tc_bwd_dq_kernel<<<grid, AT_THREADS, DQ_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, st);
+    fa_tc_bwd_dq_kernel<<<grid, AT_THREADS, DQ_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, B * H, st);
     return cudaGetLastError();
 }
 
