@@ -10,18 +10,20 @@
 // Work item = (128-query block, b, h); persistent CTAs, 192 threads:
 //   warps 0..3  softmax: one thread per query row (= its TMEM lane). Reads the
 //               row of S from TMEM, masks, tracks the running max, writes
-//               P = exp(S - max) in bf16 to shared memory as the A operand of
-//               the P V product, rescales the O row in TMEM when the max grew
+//               P = exp(S - max) in bf16 back to TMEM, where the P V product
+//               reads it as its A operand (keeping P out of shared memory,
+//               whose bandwidth the S and P V operand reads and the K/V
+//               copies already use up), rescales the O row in TMEM when the max grew
 //               by more than 2^8 (otherwise P may exceed 1 by up to 2^8, which
 //               the final division by the row sum absorbs exactly).
-//   warp 4      TMA producer: Q once, then K and V blocks of 128 keys into
-//               three-slot rings (separate K and V slots so a K slot frees as
-//               soon as its S product is done).
-//   warp 5      allocates 512 TMEM columns (S double buffer 2x128, O 64);
-//               lane 0 issues S_j = Q K_j^T (M=128, N=128, K=64) into S[j%2]
-//               and O += P_{j-1} V_{j-1} (M=128, N=64, K=128), so the tensor
-//               core computes S_{j+1} and P_{j-1} V_{j-1} while the softmax
-//               works on S_j.
+//   warp 4      TMA producer: Q once per item, then K and V of each block of
+//               128 keys into one slot of a three-slot ring.
+//   warp 5      allocates 512 TMEM columns (S double buffer, O double buffer,
+//               P double buffer); lane 0 issues S_j = Q K_j^T (M=128, N=128,
+//               K=64) into S[j%2].
+//   warp 6      lane 0 issues O += P_j V_j (M=128, N=64, K=128; A = P from
+//               TMEM), so the tensor core computes S_{j+1} and P_j V_j while
+//               the softmax works on S_{j+1}.
 // Every mbarrier wait is bounded; on expiry the CTA records ERR_TIMEOUT,
 // drains its copies and MMAs (bounded), frees TMEM and returns.
 #include "common.cuh"
@@ -41,14 +43,16 @@ constexpr int AT_HS = 64;                      // head size
 constexpr int AT_SLOTS = 3;                    // K and V ring depth
 constexpr int AT_TILE = AT_BQ * AT_HS * 2;     // 16 KB: 128 rows x 128 B
 constexpr int AT_P_BYTES = AT_BQ * AT_BK * 2;  // 32 KB
-constexpr int AT_THREADS = 192;
+constexpr int AT_THREADS = 192;                // backward kernels
+constexpr int FW_THREADS = 224;                // forward: 4 softmax warps, producer, two MMA issuers
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
-constexpr int OFF_P = OFF_V + AT_SLOTS * AT_TILE;
-constexpr int OFF_BAR = OFF_P + 2 * AT_P_BYTES;
+constexpr int OFF_BAR = OFF_V + AT_SLOTS * AT_TILE;
 constexpr size_t AT_SMEM = OFF_BAR + 256 + 1024;
-constexpr uint32_t TM_O = 256;                 // S[0] at 0, S[1] at 128, O[0] at 256, O[1] at 320
+// forward TMEM columns: S[0] 0..127, S[1] 128..255, O[0] 256..319, O[1]
+// 320..383, P[0] 384..447, P[1] 448..511 (P: bf16 pairs, the A operand of P V)
+constexpr uint32_t TM_O = 256, TM_P = 384;
 constexpr uint32_t AT_TMEM_COLS = 512;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -73,8 +77,10 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 // run on counters that every role advances identically: g counts key blocks
 // over all items (K/V ring slots, S and P buffers), `it` counts items (Q and O
 // double buffers), so the next item's Q, K and V load and its first S product
-// runs while the softmax warps finish the previous item.
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// runs while the softmax warps finish the previous item. Two threads issue the
+// tensor-core work, one the S products and one the P V products, so that
+// neither chain of barrier waits delays the other.
+__global__ void __launch_bounds__(FW_THREADS, 1)
 fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ out,
                  float* __restrict__ lse, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
@@ -82,21 +88,18 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
     uint8_t* sQ = smem + OFF_Q;
     uint8_t* sK = smem + OFF_K;
     uint8_t* sV = smem + OFF_V;
-    uint8_t* sP = smem + OFF_P;
     uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
     uint64_t* q_full = bars;           // [2]
     uint64_t* q_empty = bars + 2;      // [2]
-    uint64_t* k_full = bars + 4;       // [3]
-    uint64_t* k_empty = bars + 7;
-    uint64_t* v_full = bars + 10;
-    uint64_t* v_empty = bars + 13;
-    uint64_t* s_full = bars + 16;      // [2]
-    uint64_t* s_empty = bars + 18;
-    uint64_t* p_full = bars + 20;
-    uint64_t* pv_done = bars + 22;
-    uint64_t* o_free = bars + 24;      // [2]
-    uint64_t* drain = bars + 26;
-    uint32_t* tmem_slot = (uint32_t*)(bars + 27);
+    uint64_t* kv_full = bars + 4;      // [3] K and V block j
+    uint64_t* kv_empty = bars + 7;     // [3]
+    uint64_t* s_full = bars + 10;      // [2]
+    uint64_t* s_empty = bars + 12;
+    uint64_t* p_full = bars + 14;
+    uint64_t* pv_done = bars + 16;
+    uint64_t* o_free = bars + 18;      // [2]
+    uint64_t* drain = bars + 20;       // [2] one per issuing thread
+    uint32_t* tmem_slot = (uint32_t*)(bars + 22);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
@@ -113,14 +116,12 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
             mbar_init(&o_free[i], 4);
+            mbar_init(&drain[i], 1);
         }
         for (int s = 0; s < AT_SLOTS; s++) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
         }
-        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -133,7 +134,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
     if (warp == 4) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int g = 0, it = 0, nq = 0, nk = 0, nv = 0;
+            int g = 0, it = 0, nq = 0, nkv_l = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
                 const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
@@ -145,79 +146,86 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
                 nq++;
                 for (int j = 0; j < nkv; j++) {
                     const int G = g + j, s = G % AT_SLOTS;
-                    const uint32_t ph = (uint32_t)((G / AT_SLOTS) & 1);
-                    if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&k_full[s], AT_TILE);
-                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
-                    nk++;
-                    if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&v_full[s], AT_TILE);
-                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
-                    nv++;
+                    if (!mbar_wait(&kv_empty[s], (uint32_t)(((G / AT_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
+                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, j * AT_BK, b);
+                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                    nkv_l++;
                 }
                 g += nkv;
             }
             if (!ok || *abort_flag) {
                 // wait (bounded) for every copy still in flight before the CTA exits
                 for (int i = (nq > 2 ? nq - 2 : 0); i < nq; i++) wait_bounded(&q_full[i & 1], (uint32_t)((i >> 1) & 1));
-                for (int i = (nk > AT_SLOTS ? nk - AT_SLOTS : 0); i < nk; i++)
-                    wait_bounded(&k_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
-                for (int i = (nv > AT_SLOTS ? nv - AT_SLOTS : 0); i < nv; i++)
-                    wait_bounded(&v_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
+                for (int i = (nkv_l > AT_SLOTS ? nkv_l - AT_SLOTS : 0); i < nkv_l; i++)
+                    wait_bounded(&kv_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- S = Q K^T issuer
             constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
-            constexpr uint32_t id_o = make_idesc(AT_BQ, AT_HS, false, true);
-            const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV),
-                           p_addr = smem_u32(sP);
+            const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024), dk0 = smem_desc(smem_u32(sK), 16, 1024);
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
                 const int qb = nqb - 1 - w / BH;
                 const int nkv = qb + 1;
-                const int qs = it & 1, ob = it & 1;
+                const int qs = it & 1;
                 if (!mbar_wait(&q_full[qs], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
-                for (int j = 0; j <= nkv && ok; j++) {
-                    if (j < nkv) {
-                        const int G = g + j, s = G % AT_SLOTS, sb = G & 1;
-                        if (!mbar_wait(&k_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(&s_empty[sb], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % AT_SLOTS, sb = G & 1;
+                    if (!mbar_wait(&kv_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&s_empty[sb], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dq = desc_adv(dq0, qs * AT_TILE), dk = desc_adv(dk0, s * AT_TILE);
 #pragma unroll
-                        for (int kk = 0; kk < AT_HS / 16; kk++)
-                            mma_bf16(tmem_base + (uint32_t)(sb * AT_BK),
-                                     smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024),
-                                     smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                        mma_commit(&s_full[sb]);
-                        mma_commit(&k_empty[s]);
-                        if (j == nkv - 1) mma_commit(&q_empty[qs]);
-                        any = true;
-                    }
-                    if (j >= 1) {
-                        const int i = j - 1, G = g + i, s = G % AT_SLOTS, pb = G & 1;
-                        if (i == 0 && !mbar_wait(&o_free[ob], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(&v_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(&p_full[pb], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < AT_BK / 16; kk++) {
-                            const uint32_t a = p_addr + pb * AT_P_BYTES + (kk >> 2) * 16384 + (kk & 3) * 32;
-                            const uint32_t bb = v_addr + s * AT_TILE + kk * 2048;
-                            mma_bf16(tmem_base + TM_O + ob * AT_HS, smem_desc(a, 16, 1024),
-                                     smem_desc(bb, 8192, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&pv_done[pb]);
-                        mma_commit(&v_empty[s]);
-                    }
+                    for (int kk = 0; kk < AT_HS / 16; kk++)
+                        mma_bf16(tmem_base + (uint32_t)(sb * AT_BK), desc_adv(dq, 32 * kk), desc_adv(dk, 32 * kk),
+                                 id_s, kk > 0 ? 1u : 0u);
+                    mma_commit(&s_full[sb]);
+                    if (j == nkv - 1) mma_commit(&q_empty[qs]);
+                    any = true;
                 }
                 g += nkv;
             }
             if (any) {
-                mma_commit(drain);
-                wait_bounded(drain, 0);
+                mma_commit(&drain[0]);
+                wait_bounded(&drain[0], 0);
+            }
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            // ---------------- O += P V issuer (P read from TMEM, V MN-major)
+            constexpr uint32_t id_o = make_idesc(AT_BQ, AT_HS, false, true);
+            const uint64_t dv0 = smem_desc(smem_u32(sV), 8192, 1024);
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int qb = nqb - 1 - w / BH;
+                const int nkv = qb + 1;
+                const int ob = it & 1;
+                if (!mbar_wait(&o_free[ob], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % AT_SLOTS, pb = G & 1;
+                    if (!mbar_wait(&kv_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&p_full[pb], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dv = desc_adv(dv0, s * AT_TILE);
+                    const uint32_t tp = tmem_base + TM_P + pb * (AT_BK / 2);
+#pragma unroll
+                    for (int kk = 0; kk < AT_BK / 16; kk++)
+                        mma_bf16_ta(tmem_base + TM_O + ob * AT_HS, tp + kk * 8, desc_adv(dv, kk * 2048), id_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&pv_done[pb]);
+                    mma_commit(&kv_empty[s]);
+                    any = true;
+                }
+                g += nkv;
+            }
+            if (any) {
+                mma_commit(&drain[1]);
+                wait_bounded(&drain[1], 0);
             }
         }
     } else {
@@ -288,26 +296,24 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
                 if (G >= 2) {
                     ok = mbar_wait(&pv_done[sb], (uint32_t)(((G - 2) >> 1) & 1), abort_flag);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                    tc_fence_after();
                 }
                 float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint8_t* pbuf = sP + sb * AT_P_BYTES + r * 128;
+                const uint32_t prow = lane_base + TM_P + sb * (AT_BK / 2);
 #pragma unroll
-                for (int kb2 = 0; kb2 < 2; kb2++) {
+                for (int hf = 0; hf < 2; hf++) {
+                    uint32_t pk[32];                    // 64 probabilities as bf16 pairs
 #pragma unroll
-                    for (int pq = 0; pq < 8; pq++) {
-                        float e[8];
-#pragma unroll
-                        for (int t = 0; t < 8; t++) {
-                            e[t] = ex2f(fmaf(__uint_as_float(sr[kb2 * 64 + pq * 8 + t]), sl2, -m_run));
-                            ps[t] += e[t];
-                        }
-                        uint4 wv = make_uint4(pack2_bf16(e[0], e[1]), pack2_bf16(e[2], e[3]),
-                                              pack2_bf16(e[4], e[5]), pack2_bf16(e[6], e[7]));
-                        *(uint4*)(pbuf + kb2 * 16384 + ((pq ^ (r & 7)) << 4)) = wv;
+                    for (int c = 0; c < 32; c++) {
+                        const float e0 = ex2f(fmaf(__uint_as_float(sr[hf * 64 + 2 * c]), sl2, -m_run));
+                        const float e1 = ex2f(fmaf(__uint_as_float(sr[hf * 64 + 2 * c + 1]), sl2, -m_run));
+                        ps[(2 * c) & 7] += e0;
+                        ps[(2 * c + 1) & 7] += e1;
+                        pk[c] = pack2_bf16(e0, e1);
                     }
+                    tmem_st32(prow + 32 * hf, pk);
                 }
                 l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-                fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
@@ -399,7 +405,7 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
-    fa_tc_fwd_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, B * H, st);
+    fa_tc_fwd_kernel<<<grid, FW_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, B * H, st);
     return cudaGetLastError();
 }
 
@@ -566,8 +572,10 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             // ---------------- MMA issuer
             constexpr uint32_t id_s = make_idesc(AT_BK, AT_BQ, false, false);
             constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
-            const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
-                           do_addr = smem_u32(sDO), pt_addr = smem_u32(sPT), dst_addr = smem_u32(sDST);
+            const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024), dv0 = smem_desc(smem_u32(sV), 16, 1024),
+                           dq0 = smem_desc(smem_u32(sQ), 16, 1024), ddo0 = smem_desc(smem_u32(sDO), 16, 1024),
+                           dqm0 = smem_desc(smem_u32(sQ), 8192, 1024), ddom0 = smem_desc(smem_u32(sDO), 8192, 1024),
+                           dpt0 = smem_desc(smem_u32(sPT), 16, 1024), dst0 = smem_desc(smem_u32(sDST), 16, 1024);
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -582,13 +590,15 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                         if (!mbar_wait(&qd_full[qs], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
                         if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dk = desc_adv(dk0, ks * AT_TILE), dv = desc_adv(dv0, ks * AT_TILE),
+                                       dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE);
 #pragma unroll
                         for (int kk = 0; kk < AT_HS / 16; kk++) {
                             // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = head dim)
-                            mma_bf16(tmem_base + TM_S, smem_desc(k_addr + ks * AT_TILE + 32 * kk, 16, 1024),
-                                     smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                            mma_bf16(tmem_base + TM_DP, smem_desc(v_addr + ks * AT_TILE + 32 * kk, 16, 1024),
-                                     smem_desc(do_addr + qs * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_S, desc_adv(dk, 32 * kk), desc_adv(dq, 32 * kk), id_s,
+                                     kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_DP, desc_adv(dv, 32 * kk), desc_adv(ddo, 32 * kk), id_s,
+                                     kk > 0 ? 1u : 0u);
                         }
                         mma_commit(st_full);
                         if (i == n - 1) mma_commit(&kv_empty[ks]);
@@ -599,15 +609,14 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                         if (ii == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
                         if (!mbar_wait(ps_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t ddom = desc_adv(ddom0, qs * AT_TILE), dqm = desc_adv(dqm0, qs * AT_TILE);
 #pragma unroll
                         for (int kk = 0; kk < AT_BQ / 16; kk++) {
                             // dV += P^T dO, dK += dS^T Q (K = queries; dO and Q read MN-major)
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                             const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-                            mma_bf16(tmem_base + tdv, smem_desc(pt_addr + off, 16, 1024),
-                                     smem_desc(do_addr + qs * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
-                            mma_bf16(tmem_base + tdk, smem_desc(dst_addr + off, 16, 1024),
-                                     smem_desc(q_addr + qs * AT_TILE + kk * 2048, 8192, 1024), id_a, acc);
+                            mma_bf16(tmem_base + tdv, desc_adv(dpt0, off), desc_adv(ddom, kk * 2048), id_a, acc);
+                            mma_bf16(tmem_base + tdk, desc_adv(dst0, off), desc_adv(dqm, kk * 2048), id_a, acc);
                         }
                         mma_commit(ps_free);
                         mma_commit(&qd_empty[qs]);
@@ -817,8 +826,9 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             // ---------------- MMA issuer
             constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
             constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
-            const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), k_addr = smem_u32(sK),
-                           v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+            const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024), ddo0 = smem_desc(smem_u32(sDO), 16, 1024),
+                           dk0 = smem_desc(smem_u32(sK), 16, 1024), dv0 = smem_desc(smem_u32(sV), 16, 1024),
+                           dkm0 = smem_desc(smem_u32(sK), 8192, 1024), dds0 = smem_desc(smem_u32(sDS), 16, 1024);
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -834,13 +844,15 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                         if (!mbar_wait(&v_full[s], ph, abort_flag)) { ok = false; break; }
                         if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE),
+                                       dk = desc_adv(dk0, s * AT_TILE), dv = desc_adv(dv0, s * AT_TILE);
 #pragma unroll
                         for (int kk = 0; kk < AT_HS / 16; kk++) {
                             // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = head dim)
-                            mma_bf16(tmem_base + TM_S, smem_desc(q_addr + qs * AT_TILE + 32 * kk, 16, 1024),
-                                     smem_desc(k_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-                            mma_bf16(tmem_base + TM_DP, smem_desc(do_addr + qs * AT_TILE + 32 * kk, 16, 1024),
-                                     smem_desc(v_addr + s * AT_TILE + 32 * kk, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_S, desc_adv(dq, 32 * kk), desc_adv(dk, 32 * kk), id_s,
+                                     kk > 0 ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_DP, desc_adv(ddo, 32 * kk), desc_adv(dv, 32 * kk), id_s,
+                                     kk > 0 ? 1u : 0u);
                         }
                         mma_commit(st_full);
                         mma_commit(&v_empty[s]);
@@ -852,13 +864,13 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                         if (jj == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
                         if (!mbar_wait(ds_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dkm = desc_adv(dkm0, s * AT_TILE);
 #pragma unroll
                         for (int kk = 0; kk < AT_BK / 16; kk++) {
                             // dQ += dS K (K = keys; K read MN-major)
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_bf16(tmem_base + TM_ACC + ab * AT_HS, smem_desc(ds_addr + off, 16, 1024),
-                                     smem_desc(k_addr + s * AT_TILE + kk * 2048, 8192, 1024), id_a,
-                                     (jj > 0 || kk > 0) ? 1u : 0u);
+                            mma_bf16(tmem_base + TM_ACC + ab * AT_HS, desc_adv(dds0, off), desc_adv(dkm, kk * 2048),
+                                     id_a, (jj > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(ds_free);
                         mma_commit(&k_empty[s]);

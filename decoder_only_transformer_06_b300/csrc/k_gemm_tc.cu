@@ -234,7 +234,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             constexpr uint32_t idesc = make_idesc(TC_BM, BN, A_MN, B_MN);
             constexpr uint32_t A_LBO = A_MN ? 8192 : 16, B_LBO = B_MN ? 8192 : 16;
             constexpr uint32_t KSTEP_A = A_MN ? 2048 : 32, KSTEP_B = B_MN ? 2048 : 32;
-            const uint32_t sA0 = smem_u32(sA), sB0 = smem_u32(sB);
+            const uint64_t dA0 = smem_desc(smem_u32(sA), A_LBO, 1024);
+            const uint64_t dB0 = smem_desc(smem_u32(sB), B_LBO, 1024);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -250,14 +251,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = sA0 + stage * Cfg::A_BYTES;
-                    const uint32_t b_addr = sB0 + stage * Cfg::B_BYTES;
+                    const uint64_t ad = desc_adv(dA0, stage * Cfg::A_BYTES);
+                    const uint64_t bd = desc_adv(dB0, stage * Cfg::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < TC_BK / 16; kk++) {
-                        uint64_t ad = smem_desc(a_addr + kk * KSTEP_A, A_LBO, 1024);
-                        uint64_t bd = smem_desc(b_addr + kk * KSTEP_B, B_LBO, 1024);
-                        mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < TC_BK / 16; kk++)
+                        mma_bf16(d_tmem, desc_adv(ad, kk * KSTEP_A), desc_adv(bd, kk * KSTEP_B), idesc,
+                                 (kb > kb0 || kk > 0) ? 1u : 0u);
                     any = true;
                     mma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }

@@ -82,6 +82,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
+// D (+)= A B with A (M x 16, 16-bit) read from tensor memory: lane m holds row
+// m, and each 32-bit column holds two consecutive K elements (the lower K
+// index in the low half), so one instruction reads 8 columns from a_tmem.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -115,6 +126,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// A descriptor moved by `bytes` (a multiple of 16) along shared memory: the
+// start-address field is the low 14 bits (address >> 4) and stays below 2^14
+// for any shared-memory address, so a plain add is exact. Issue loops build
+// their descriptors once and advance them this way: rebuilding a descriptor
+// per tcgen05.mma made the issuing thread, not the tensor core, the limit
+// (about 150 cycles per MMA against 64-128 for the product itself).
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Instruction descriptor, kind::f16: D fp32 (bit 4), A and B bf16 (bits 7,
 // 10), A/B major in bits 15/16 (1 = MN-major), N>>3 in bits 17-22, M>>4 in
