@@ -42,8 +42,6 @@ constexpr int AT_BK = 128;                     // keys per block
 constexpr int AT_HS = 64;                      // head size
 constexpr int AT_SLOTS = 3;                    // K and V ring depth
 constexpr int AT_TILE = AT_BQ * AT_HS * 2;     // 16 KB: 128 rows x 128 B
-constexpr int AT_P_BYTES = AT_BQ * AT_BK * 2;  // 32 KB
-constexpr int AT_THREADS = 192;                // backward kernels
 constexpr int FW_THREADS = 224;                // forward: 4 softmax warps, producer, two MMA issuers
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
@@ -423,90 +421,80 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
 
 namespace {
 
-// dK/dV kernel: K and V double buffered per item, Q and dO in a 2-slot ring
+constexpr int BW_THREADS = 224;                 // 4 softmax warps, producer, two MMA issuers
+constexpr int BW_SLOTS = 3;
+constexpr int OUT_SLAB = 32 * AT_HS * 2;          // one warp's 32 output rows, 4 KB
+// dK/dV kernel: K and V double buffered per item, Q and dO in a 3-slot ring,
+// per-warp staging of the dK and dV rows for their TMA stores
 constexpr int KV_OFF_K = 0;                                  // [2]
 constexpr int KV_OFF_V = KV_OFF_K + 2 * AT_TILE;             // [2]
-constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [2]
-constexpr int KV_OFF_DO = KV_OFF_Q + 2 * AT_TILE;            // [2]
-constexpr int KV_OFF_PT = KV_OFF_DO + 2 * AT_TILE;
-constexpr int KV_OFF_DST = KV_OFF_PT + AT_P_BYTES;
-constexpr int KV_OFF_LD = KV_OFF_DST + AT_P_BYTES;        // lse2[2][128], D[2][128]
+constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [3]
+constexpr int KV_OFF_DO = KV_OFF_Q + BW_SLOTS * AT_TILE;     // [3]
+constexpr int KV_OFF_OUT = KV_OFF_DO + BW_SLOTS * AT_TILE;   // [4 warps][dK, dV] slabs
+constexpr int KV_OFF_LD = KV_OFF_OUT + 8 * OUT_SLAB;         // lse2[2][128], D[2][128]
 constexpr int KV_OFF_BAR = KV_OFF_LD + 4 * 128 * 4;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
-// dQ kernel: Q and dO double buffered per item, K and V in 3-slot rings
-constexpr int BW_SLOTS = 3;
+// dQ kernel: Q and dO double buffered per item, K and V in a 3-slot ring
 constexpr int DQ_OFF_Q = 0;                                  // [2]
 constexpr int DQ_OFF_DO = DQ_OFF_Q + 2 * AT_TILE;            // [2]
-constexpr int DQ_OFF_K = DQ_OFF_DO + 2 * AT_TILE;
-constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;
-constexpr int DQ_OFF_DS = DQ_OFF_V + BW_SLOTS * AT_TILE;
-constexpr int DQ_OFF_BAR = DQ_OFF_DS + AT_P_BYTES;
+constexpr int DQ_OFF_K = DQ_OFF_DO + 2 * AT_TILE;            // [3]
+constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;      // [3]
+constexpr int DQ_OFF_OUT = DQ_OFF_V + BW_SLOTS * AT_TILE;    // [4 warps] dQ slabs
+constexpr int DQ_OFF_BAR = DQ_OFF_OUT + 4 * OUT_SLAB;
 constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
-// TMEM columns of both kernels: S (or S^T) 0..127, dP 128..255, then the
-// accumulators of two consecutive work items: dV, dK at 256 + 128*(it&1)
-// (+64), or dQ at 256 + 64*(it&1)
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256;
+// TMEM columns. dK/dV: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383,
+// P^T 384..447 and dS^T 448..511 (bf16 pairs, the A operands of dV and dK).
+// dQ: S 0..127, dP 128..255, dQ[2] 256..383, dS 384..447.
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256, TM_PT = 384, TM_DST = 448;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
-// 32 fp32 values of one row as bf16 into a K-major 128B-swizzled operand tile
-// of 128 rows x 128 columns (two 64-column blocks of 16 KB): chunk c holds
-// columns 32c..32c+31.
-__device__ __forceinline__ void put_row_chunk(uint8_t* tile, int row, int c, const float (&v)[32]) {
-    uint8_t* base = tile + (c >> 1) * 16384 + row * 128;
+// A warp's 32 rows x 64 columns of an output tile (fp32 accumulator values
+// times `scale`) as bf16 into a 128B-swizzled 4 KB slab: lane = row, 16-byte
+// piece q of row r at r*128 + ((q ^ (r & 7)) << 4), the layout the TMA store
+// of a 64 x 32 box expects.
+__device__ __forceinline__ void stage_out_slab(uint8_t* slab, int lane, const uint32_t (&a)[64], float scale) {
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const int piece = (c & 1) * 4 + q;
-        uint4 w = make_uint4(pack2_bf16(v[8 * q + 0], v[8 * q + 1]), pack2_bf16(v[8 * q + 2], v[8 * q + 3]),
-                             pack2_bf16(v[8 * q + 4], v[8 * q + 5]), pack2_bf16(v[8 * q + 6], v[8 * q + 7]));
-        *(uint4*)(base + ((piece ^ (row & 7)) << 4)) = w;
+    for (int q = 0; q < 8; q++) {
+        const float* f = (const float*)&a[8 * q];
+        *(uint4*)(slab + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(pack2_bf16(f[0] * scale, f[1] * scale), pack2_bf16(f[2] * scale, f[3] * scale),
+                       pack2_bf16(f[4] * scale, f[5] * scale), pack2_bf16(f[6] * scale, f[7] * scale));
     }
 }
-
-// 64 fp32 accumulator columns times `scale`, as bf16, to 128 contiguous bytes.
-__device__ __forceinline__ void store_row64(bf16* dst, const uint32_t (&a)[64], float scale) {
-    uint4* d = (uint4*)dst;
-#pragma unroll
-    for (int c = 0; c < 8; c++) {
-        const float* f = (const float*)&a[8 * c];
-        d[c] = make_uint4(pack2_bf16(f[0] * scale, f[1] * scale), pack2_bf16(f[2] * scale, f[3] * scale),
-                          pack2_bf16(f[4] * scale, f[5] * scale), pack2_bf16(f[6] * scale, f[7] * scale));
-    }
-}
-
 
 }  // namespace
 
 // Persistent like the forward: work items (key block kb, b, h), fewest key
 // blocks last (kb = w / (B*H)); g counts query blocks over all items, `it`
-// counts items (K/V buffers and the dV/dK accumulator pair alternate).
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// counts items. Warp 5 issues S^T = K Q^T and dP^T = V dO^T, warp 6 the
+// accumulating dV += P^T dO and dK += dS^T Q with P^T, dS^T read from TMEM.
+__global__ void __launch_bounds__(BW_THREADS, 1)
 fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                     const float* __restrict__ lse, const float* __restrict__ Dg,
-                     bf16* __restrict__ dqkv, int T, int H, int BH, DevState* st) {
+                     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
+                     const float* __restrict__ Dg, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sK = smem + KV_OFF_K;
     uint8_t* sV = smem + KV_OFF_V;
     uint8_t* sQ = smem + KV_OFF_Q;
     uint8_t* sDO = smem + KV_OFF_DO;
-    uint8_t* sPT = smem + KV_OFF_PT;
-    uint8_t* sDST = smem + KV_OFF_DST;
+    uint8_t* sOut = smem + KV_OFF_OUT;
     float* sL = (float*)(smem + KV_OFF_LD);          // [2][128] lse in log2 units
     float* sD = sL + 256;                              // [2][128]
     uint64_t* bars = (uint64_t*)(smem + KV_OFF_BAR);
     uint64_t* kv_full = bars;                          // [2]
     uint64_t* kv_empty = bars + 2;                     // [2]
-    uint64_t* qd_full = bars + 4;                      // [2]
-    uint64_t* qd_empty = bars + 6;                     // [2]
-    uint64_t* st_full = bars + 8;
-    uint64_t* st_free = bars + 9;
-    uint64_t* ps_full = bars + 10;
-    uint64_t* ps_free = bars + 11;
-    uint64_t* acc_full = bars + 12;                    // [2]
-    uint64_t* acc_free = bars + 14;                    // [2]
-    uint64_t* drain = bars + 16;
-    uint64_t* ld_full = bars + 17;                     // [2] lse/D staged (one arrive per warp)
-    uint32_t* tmem_slot = (uint32_t*)(bars + 19);
+    uint64_t* qd_full = bars + 4;                      // [3]
+    uint64_t* qd_empty = bars + 7;                     // [3]
+    uint64_t* st_full = bars + 10;
+    uint64_t* st_free = bars + 11;
+    uint64_t* ps_full = bars + 12;
+    uint64_t* ps_free = bars + 13;
+    uint64_t* acc_full = bars + 14;
+    uint64_t* acc_free = bars + 15;
+    uint64_t* ld_full = bars + 16;                     // [2]
+    uint64_t* drain = bars + 18;                       // [2]
+    uint32_t* tmem_slot = (uint32_t*)(bars + 20);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nb = (T + AT_BK - 1) / AT_BK;
@@ -518,17 +506,19 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         for (int i = 0; i < 2; i++) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
-            mbar_init(&qd_full[i], 1);
-            mbar_init(&qd_empty[i], 1);
-            mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_free[i], 4);
             mbar_init(&ld_full[i], 4);
+            mbar_init(&drain[i], 1);
+        }
+        for (int s = 0; s < BW_SLOTS; s++) {
+            mbar_init(&qd_full[s], 1);
+            mbar_init(&qd_empty[s], 1);
         }
         mbar_init(st_full, 1);
         mbar_init(st_free, 4);
         mbar_init(ps_full, 4);
         mbar_init(ps_free, 1);
-        mbar_init(drain, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_free, 4);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -553,8 +543,8 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                 tma_load_3d(sV + ks * AT_TILE, &tm_qkv, &kv_full[ks], 2 * C + h * AT_HS, kb * AT_BK, b);
                 nkvl++;
                 for (int i = 0; i < n; i++) {
-                    const int G = g + i, qs = G & 1;
-                    if (!mbar_wait(&qd_empty[qs], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    const int G = g + i, qs = G % BW_SLOTS;
+                    if (!mbar_wait(&qd_empty[qs], (uint32_t)(((G / BW_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
                     mbar_arrive_expect_tx(&qd_full[qs], 2 * AT_TILE);
                     tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
                     tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
@@ -564,70 +554,78 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             }
             if (!ok || *abort_flag) {
                 for (int i = (nkvl > 2 ? nkvl - 2 : 0); i < nkvl; i++) wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1));
-                for (int i = (nql > 2 ? nql - 2 : 0); i < nql; i++) wait_bounded(&qd_full[i & 1], (uint32_t)((i >> 1) & 1));
+                for (int i = (nql > BW_SLOTS ? nql - BW_SLOTS : 0); i < nql; i++)
+                    wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- S^T = K Q^T, dP^T = V dO^T (M = keys, N = queries, K = head dim)
             constexpr uint32_t id_s = make_idesc(AT_BK, AT_BQ, false, false);
-            constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
             const uint64_t dk0 = smem_desc(smem_u32(sK), 16, 1024), dv0 = smem_desc(smem_u32(sV), 16, 1024),
-                           dq0 = smem_desc(smem_u32(sQ), 16, 1024), ddo0 = smem_desc(smem_u32(sDO), 16, 1024),
-                           dqm0 = smem_desc(smem_u32(sQ), 8192, 1024), ddom0 = smem_desc(smem_u32(sDO), 8192, 1024),
-                           dpt0 = smem_desc(smem_u32(sPT), 16, 1024), dst0 = smem_desc(smem_u32(sDST), 16, 1024);
+                           dq0 = smem_desc(smem_u32(sQ), 16, 1024), ddo0 = smem_desc(smem_u32(sDO), 16, 1024);
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
-                const int kb = w / BH;
-                const int n = nb - kb;
-                const int ks = it & 1, ab = it & 1;
-                const uint32_t tdv = TM_ACC + ab * 128, tdk = tdv + 64;
+                const int n = nb - w / BH;
+                const int ks = it & 1;
                 if (!mbar_wait(&kv_full[ks], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
-                for (int i = 0; i <= n && ok; i++) {
-                    if (i < n) {
-                        const int G = g + i, qs = G & 1;
-                        if (!mbar_wait(&qd_full[qs], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t dk = desc_adv(dk0, ks * AT_TILE), dv = desc_adv(dv0, ks * AT_TILE),
-                                       dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE);
+                const uint64_t dk = desc_adv(dk0, ks * AT_TILE), dv = desc_adv(dv0, ks * AT_TILE);
+                for (int i = 0; i < n; i++) {
+                    const int G = g + i, qs = G % BW_SLOTS;
+                    if (!mbar_wait(&qd_full[qs], (uint32_t)((G / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE);
 #pragma unroll
-                        for (int kk = 0; kk < AT_HS / 16; kk++) {
-                            // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries, K = head dim)
-                            mma_bf16(tmem_base + TM_S, desc_adv(dk, 32 * kk), desc_adv(dq, 32 * kk), id_s,
-                                     kk > 0 ? 1u : 0u);
-                            mma_bf16(tmem_base + TM_DP, desc_adv(dv, 32 * kk), desc_adv(ddo, 32 * kk), id_s,
-                                     kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(st_full);
-                        if (i == n - 1) mma_commit(&kv_empty[ks]);
-                        any = true;
+                    for (int kk = 0; kk < AT_HS / 16; kk++) {
+                        mma_bf16(tmem_base + TM_S, desc_adv(dk, 32 * kk), desc_adv(dq, 32 * kk), id_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem_base + TM_DP, desc_adv(dv, 32 * kk), desc_adv(ddo, 32 * kk), id_s, kk > 0 ? 1u : 0u);
                     }
-                    if (i >= 1) {
-                        const int ii = i - 1, G = g + ii, qs = G & 1;
-                        if (ii == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(ps_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t ddom = desc_adv(ddom0, qs * AT_TILE), dqm = desc_adv(dqm0, qs * AT_TILE);
-#pragma unroll
-                        for (int kk = 0; kk < AT_BQ / 16; kk++) {
-                            // dV += P^T dO, dK += dS^T Q (K = queries; dO and Q read MN-major)
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-                            mma_bf16(tmem_base + tdv, desc_adv(dpt0, off), desc_adv(ddom, kk * 2048), id_a, acc);
-                            mma_bf16(tmem_base + tdk, desc_adv(dst0, off), desc_adv(dqm, kk * 2048), id_a, acc);
-                        }
-                        mma_commit(ps_free);
-                        mma_commit(&qd_empty[qs]);
-                        if (ii == n - 1) mma_commit(&acc_full[ab]);
-                    }
+                    mma_commit(st_full);
+                    if (i == n - 1) mma_commit(&kv_empty[ks]);
+                    any = true;
                 }
                 g += n;
             }
             if (any) {
-                mma_commit(drain);
-                wait_bounded(drain, 0);
+                mma_commit(&drain[0]);
+                wait_bounded(&drain[0], 0);
+            }
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            // ---------------- dV += P^T dO, dK += dS^T Q (A from TMEM; dO, Q read MN-major)
+            constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
+            const uint64_t dqm0 = smem_desc(smem_u32(sQ), 8192, 1024), ddom0 = smem_desc(smem_u32(sDO), 8192, 1024);
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int n = nb - w / BH;
+                if (!mbar_wait(acc_free, (uint32_t)((it & 1) ^ 1), abort_flag)) { ok = false; break; }
+                for (int i = 0; i < n; i++) {
+                    const int G = g + i, qs = G % BW_SLOTS;
+                    if (!mbar_wait(&qd_full[qs], (uint32_t)((G / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(ps_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dqm = desc_adv(dqm0, qs * AT_TILE), ddom = desc_adv(ddom0, qs * AT_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < AT_BQ / 16; kk++) {
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        mma_bf16_ta(tmem_base + TM_ACC, tmem_base + TM_PT + kk * 8, desc_adv(ddom, kk * 2048), id_a, acc);
+                        mma_bf16_ta(tmem_base + TM_ACC + AT_HS, tmem_base + TM_DST + kk * 8, desc_adv(dqm, kk * 2048),
+                                    id_a, acc);
+                    }
+                    mma_commit(ps_free);
+                    mma_commit(&qd_empty[qs]);
+                    if (i == n - 1) mma_commit(acc_full);
+                    any = true;
+                }
+                g += n;
+            }
+            if (any) {
+                mma_commit(&drain[1]);
+                wait_bounded(&drain[1], 0);
             }
         }
     } else {
@@ -635,13 +633,12 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         const int r = threadIdx.x;
         const float sl2 = LOG2E_F * 0.125f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        uint8_t* slab = sOut + warp * 2 * OUT_SLAB;        // [dK, dV] of this warp's 32 rows
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
             const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
             const int n = nb - kb;
-            const int key = kb * AT_BK + r;
-            const int ab = it & 1;
             for (int i = 0; i < n; i++) {
                 const int G = g + i, ls = G & 1;
                 const int q0 = (kb + i) * AT_BQ;
@@ -658,6 +655,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                // P^T / dS^T in TMEM are free once the previous block's products read them
                 ok = mbar_wait(ps_free, (uint32_t)((G & 1) ^ 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
@@ -674,44 +672,60 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                         __syncwarp();
                         if (lane == 0) mbar_arrive(st_free);
                     }
-                    float pv[32], dsv[32];
+                    uint32_t pp[16], pd[16];
 #pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        const int qq = 32 * c + t;
-                        float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -L[qq]));
-                        if (i == 0 && qq < r) p = 0.f;          // query before key: masked
-                        pv[t] = p;
-                        dsv[t] = p * (__uint_as_float(dr[t]) - Dq[qq]);
+                    for (int t = 0; t < 16; t++) {
+                        float p[2], d[2];
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            const int qq = 32 * c + 2 * t + u;
+                            float e = ex2f(fmaf(__uint_as_float(sr[2 * t + u]), sl2, -L[qq]));
+                            if (i == 0 && qq < r) e = 0.f;          // query before key: masked
+                            p[u] = e;
+                            d[u] = e * (__uint_as_float(dr[2 * t + u]) - Dq[qq]);
+                        }
+                        pp[t] = pack2_bf16(p[0], p[1]);
+                        pd[t] = pack2_bf16(d[0], d[1]);
                     }
-                    put_row_chunk(sPT, r, c, pv);
-                    put_row_chunk(sDST, r, c, dsv);
+                    tmem_st16(lane_base + TM_PT + 16 * c, pp);
+                    tmem_st16(lane_base + TM_DST + 16 * c, pd);
                 }
-                fence_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ps_full);
             }
             if (!ok) break;
-            ok = mbar_wait(&acc_full[ab], (uint32_t)((it >> 1) & 1), abort_flag);
+            // the item's dK, dV rows: out of TMEM, staged, one TMA store per warp and tensor
+            ok = mbar_wait(acc_full, (uint32_t)(it & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t dv[64], dk[64];
-            const uint32_t tdv = lane_base + TM_ACC + ab * 128;
-            tmem_ld32_nowait(tdv, dv);
-            tmem_ld32_nowait(tdv + 32, dv + 32);
-            tmem_ld32_nowait(tdv + 64, dk);
-            tmem_ld32_nowait(tdv + 96, dk + 32);
+            tmem_ld32_nowait(lane_base + TM_ACC, dv);
+            tmem_ld32_nowait(lane_base + TM_ACC + 32, dv + 32);
+            tmem_ld32_nowait(lane_base + TM_ACC + 64, dk);
+            tmem_ld32_nowait(lane_base + TM_ACC + 96, dk + 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_free[ab]);
-            if (key < T) {
-                bf16* row = dqkv + ((int64_t)b * T + key) * 3 * C + h * AT_HS;
-                store_row64(row + C, dk, 0.125f);
-                store_row64(row + 2 * C, dv, 1.f);
+            if (lane == 0) mbar_arrive(acc_free);
+            if (lane == 0) tma_wait_read<0>();               // the previous item's stores have read the slabs
+            __syncwarp();
+            stage_out_slab(slab, lane, dk, 0.125f);
+            stage_out_slab(slab + OUT_SLAB, lane, dv, 1.f);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int row0 = kb * AT_BK + warp * 32;
+                if (row0 < T) {
+                    tma_store_3d(&tm_out, slab, C + h * AT_HS, row0, b);
+                    tma_store_3d(&tm_out, slab + OUT_SLAB, 2 * C + h * AT_HS, row0, b);
+                }
+                tma_commit();
             }
             g += n;
         }
+        if (lane == 0) tma_wait_all();
     }
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) {
@@ -724,33 +738,32 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     }
 }
 
-// Persistent: work items (query block qb, b, h), heaviest first.
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// Persistent: work items (query block qb, b, h), heaviest first. Warp 5 issues
+// S = Q K^T and dP = dO V^T, warp 6 the accumulating dQ += dS K (dS from TMEM).
+__global__ void __launch_bounds__(BW_THREADS, 1)
 fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                    const float* __restrict__ lse, const float* __restrict__ Dg,
-                    bf16* __restrict__ dqkv, int T, int H, int BH, DevState* st) {
+                    const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
+                    const float* __restrict__ Dg, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + DQ_OFF_Q;
     uint8_t* sDO = smem + DQ_OFF_DO;
     uint8_t* sK = smem + DQ_OFF_K;
     uint8_t* sV = smem + DQ_OFF_V;
-    uint8_t* sDS = smem + DQ_OFF_DS;
+    uint8_t* sOut = smem + DQ_OFF_OUT;
     uint64_t* bars = (uint64_t*)(smem + DQ_OFF_BAR);
     uint64_t* qd_full = bars;                          // [2]
     uint64_t* qd_empty = bars + 2;                     // [2]
-    uint64_t* k_full = bars + 4;                       // [3]
-    uint64_t* k_empty = bars + 7;
-    uint64_t* v_full = bars + 10;
-    uint64_t* v_empty = bars + 13;
-    uint64_t* st_full = bars + 16;
-    uint64_t* st_free = bars + 17;
-    uint64_t* ds_full = bars + 18;
-    uint64_t* ds_free = bars + 19;
-    uint64_t* acc_full = bars + 20;                    // [2]
-    uint64_t* acc_free = bars + 22;                    // [2]
-    uint64_t* drain = bars + 24;
-    uint32_t* tmem_slot = (uint32_t*)(bars + 25);
+    uint64_t* kv_full = bars + 4;                      // [3]
+    uint64_t* kv_empty = bars + 7;                     // [3]
+    uint64_t* st_full = bars + 10;
+    uint64_t* st_free = bars + 11;
+    uint64_t* ds_full = bars + 12;
+    uint64_t* ds_free = bars + 13;
+    uint64_t* acc_full = bars + 14;                    // [2]
+    uint64_t* acc_free = bars + 16;                    // [2]
+    uint64_t* drain = bars + 18;                       // [2]
+    uint32_t* tmem_slot = (uint32_t*)(bars + 20);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
@@ -764,18 +777,16 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             mbar_init(&qd_empty[i], 1);
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_free[i], 4);
+            mbar_init(&drain[i], 1);
         }
         for (int s = 0; s < BW_SLOTS; s++) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
         }
         mbar_init(st_full, 1);
         mbar_init(st_free, 4);
         mbar_init(ds_full, 4);
         mbar_init(ds_free, 1);
-        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -788,7 +799,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     if (warp == 4) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int g = 0, it = 0, nql = 0, nk = 0, nv = 0;
+            int g = 0, it = 0, nql = 0, nkvl = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
                 const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
@@ -801,87 +812,86 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                 nql++;
                 for (int j = 0; j < nkv; j++) {
                     const int G = g + j, s = G % BW_SLOTS;
-                    const uint32_t ph = (uint32_t)((G / BW_SLOTS) & 1);
-                    if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&k_full[s], AT_TILE);
-                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, j * AT_BK, b);
-                    nk++;
-                    if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&v_full[s], AT_TILE);
-                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &v_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
-                    nv++;
+                    if (!mbar_wait(&kv_empty[s], (uint32_t)(((G / BW_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
+                    tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, j * AT_BK, b);
+                    tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, j * AT_BK, b);
+                    nkvl++;
                 }
                 g += nkv;
             }
             if (!ok || *abort_flag) {
                 for (int i = (nql > 2 ? nql - 2 : 0); i < nql; i++) wait_bounded(&qd_full[i & 1], (uint32_t)((i >> 1) & 1));
-                for (int i = (nk > BW_SLOTS ? nk - BW_SLOTS : 0); i < nk; i++)
-                    wait_bounded(&k_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
-                for (int i = (nv > BW_SLOTS ? nv - BW_SLOTS : 0); i < nv; i++)
-                    wait_bounded(&v_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
+                for (int i = (nkvl > BW_SLOTS ? nkvl - BW_SLOTS : 0); i < nkvl; i++)
+                    wait_bounded(&kv_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- S = Q K^T, dP = dO V^T (M = queries, N = keys, K = head dim)
             constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
-            constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
             const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024), ddo0 = smem_desc(smem_u32(sDO), 16, 1024),
-                           dk0 = smem_desc(smem_u32(sK), 16, 1024), dv0 = smem_desc(smem_u32(sV), 16, 1024),
-                           dkm0 = smem_desc(smem_u32(sK), 8192, 1024), dds0 = smem_desc(smem_u32(sDS), 16, 1024);
+                           dk0 = smem_desc(smem_u32(sK), 16, 1024), dv0 = smem_desc(smem_u32(sV), 16, 1024);
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
-                const int qb = nqb - 1 - w / BH;
-                const int nkv = qb + 1;
-                const int qs = it & 1, ab = it & 1;
+                const int nkv = nqb - w / BH;
+                const int qs = it & 1;
                 if (!mbar_wait(&qd_full[qs], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
-                for (int j = 0; j <= nkv && ok; j++) {
-                    if (j < nkv) {
-                        const int G = g + j, s = G % BW_SLOTS;
-                        const uint32_t ph = (uint32_t)((G / BW_SLOTS) & 1);
-                        if (!mbar_wait(&k_full[s], ph, abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(&v_full[s], ph, abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE),
-                                       dk = desc_adv(dk0, s * AT_TILE), dv = desc_adv(dv0, s * AT_TILE);
+                const uint64_t dq = desc_adv(dq0, qs * AT_TILE), ddo = desc_adv(ddo0, qs * AT_TILE);
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % BW_SLOTS;
+                    if (!mbar_wait(&kv_full[s], (uint32_t)((G / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(st_free, (uint32_t)((G & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dk = desc_adv(dk0, s * AT_TILE), dv = desc_adv(dv0, s * AT_TILE);
 #pragma unroll
-                        for (int kk = 0; kk < AT_HS / 16; kk++) {
-                            // S = Q K^T and dP = dO V^T (M = queries, N = keys, K = head dim)
-                            mma_bf16(tmem_base + TM_S, desc_adv(dq, 32 * kk), desc_adv(dk, 32 * kk), id_s,
-                                     kk > 0 ? 1u : 0u);
-                            mma_bf16(tmem_base + TM_DP, desc_adv(ddo, 32 * kk), desc_adv(dv, 32 * kk), id_s,
-                                     kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(st_full);
-                        mma_commit(&v_empty[s]);
-                        if (j == nkv - 1) mma_commit(&qd_empty[qs]);
-                        any = true;
+                    for (int kk = 0; kk < AT_HS / 16; kk++) {
+                        mma_bf16(tmem_base + TM_S, desc_adv(dq, 32 * kk), desc_adv(dk, 32 * kk), id_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem_base + TM_DP, desc_adv(ddo, 32 * kk), desc_adv(dv, 32 * kk), id_s, kk > 0 ? 1u : 0u);
                     }
-                    if (j >= 1) {
-                        const int jj = j - 1, G = g + jj, s = G % BW_SLOTS;
-                        if (jj == 0 && !mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                        if (!mbar_wait(ds_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t dkm = desc_adv(dkm0, s * AT_TILE);
-#pragma unroll
-                        for (int kk = 0; kk < AT_BK / 16; kk++) {
-                            // dQ += dS K (K = keys; K read MN-major)
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_bf16(tmem_base + TM_ACC + ab * AT_HS, desc_adv(dds0, off), desc_adv(dkm, kk * 2048),
-                                     id_a, (jj > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(ds_free);
-                        mma_commit(&k_empty[s]);
-                        if (jj == nkv - 1) mma_commit(&acc_full[ab]);
-                    }
+                    mma_commit(st_full);
+                    if (j == nkv - 1) mma_commit(&qd_empty[qs]);
+                    any = true;
                 }
                 g += nkv;
             }
             if (any) {
-                mma_commit(drain);
-                wait_bounded(drain, 0);
+                mma_commit(&drain[0]);
+                wait_bounded(&drain[0], 0);
+            }
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            // ---------------- dQ += dS K (A = dS from TMEM, K read MN-major)
+            constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
+            const uint64_t dkm0 = smem_desc(smem_u32(sK), 8192, 1024);
+            bool ok = true, any = false;
+            int g = 0, it = 0;
+            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+                const int nkv = nqb - w / BH;
+                const int ab = it & 1;
+                if (!mbar_wait(&acc_free[ab], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                for (int j = 0; j < nkv; j++) {
+                    const int G = g + j, s = G % BW_SLOTS;
+                    if (!mbar_wait(&kv_full[s], (uint32_t)((G / BW_SLOTS) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(ds_full, (uint32_t)(G & 1), abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dkm = desc_adv(dkm0, s * AT_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < AT_BK / 16; kk++)
+                        mma_bf16_ta(tmem_base + TM_ACC + ab * AT_HS, tmem_base + TM_PT + kk * 8,
+                                    desc_adv(dkm, kk * 2048), id_a, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(ds_free);
+                    mma_commit(&kv_empty[s]);
+                    if (j == nkv - 1) mma_commit(&acc_full[ab]);
+                    any = true;
+                }
+                g += nkv;
+            }
+            if (any) {
+                mma_commit(&drain[1]);
+                wait_bounded(&drain[1], 0);
             }
         }
     } else {
@@ -889,6 +899,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
         const int r = threadIdx.x;
         const float sl2 = LOG2E_F * 0.125f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        uint8_t* slab = sOut + warp * OUT_SLAB;
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -918,17 +929,22 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                         __syncwarp();
                         if (lane == 0) mbar_arrive(st_free);
                     }
-                    float dsv[32];
+                    uint32_t pd[16];
 #pragma unroll
-                    for (int t = 0; t < 32; t++) {
-                        const int kk = key0 + 32 * c + t;
-                        float p = ex2f(fmaf(__uint_as_float(sr[t]), sl2, -lse2));
-                        if (edge && (kk > q || kk >= T)) p = 0.f;
-                        dsv[t] = p * (__uint_as_float(dr[t]) - Dq);
+                    for (int t = 0; t < 16; t++) {
+                        float d[2];
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            const int kk = key0 + 32 * c + 2 * t + u;
+                            float e = ex2f(fmaf(__uint_as_float(sr[2 * t + u]), sl2, -lse2));
+                            if (edge && (kk > q || kk >= T)) e = 0.f;
+                            d[u] = e * (__uint_as_float(dr[2 * t + u]) - Dq);
+                        }
+                        pd[t] = pack2_bf16(d[0], d[1]);
                     }
-                    put_row_chunk(sDS, r, c, dsv);
+                    tmem_st16(lane_base + TM_PT + 16 * c, pd);
                 }
-                fence_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ds_full);
@@ -944,9 +960,19 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_free[ab]);
-            if (q < T) store_row64(dqkv + ((int64_t)b * T + q) * 3 * C + h * AT_HS, dq, 0.125f);
+            if (lane == 0) tma_wait_read<0>();
+            __syncwarp();
+            stage_out_slab(slab, lane, dq, 0.125f);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int row0 = qb * AT_BQ + warp * 32;
+                if (row0 < T) tma_store_3d(&tm_out, slab, h * AT_HS, row0, b);
+                tma_commit();
+            }
             g += nkv;
         }
+        if (lane == 0) tma_wait_all();
     }
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) {
@@ -972,15 +998,31 @@ static bool make_do_map(CUtensorMap* map, const bf16* dout, int B, int T, int C)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// dqkv [B, T, 3C] bf16 as the target of the per-warp output stores: 3-D map
+// {3C, T, B}, boxes of 64 x 32 x 1 with 128B swizzle (rows beyond T clipped).
+static bool make_dqkv_map(CUtensorMap* map, bf16* dqkv, int B, int T, int C) {
+    EncodeTiledFnA enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)3 * C, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)3 * C * 2 * T};
+    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dqkv, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* D,
                              bf16* dqkv, int B, int T, int H, int hs, DevState* st, cudaStream_t s) {
     if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
     if (((uintptr_t)qkv & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15))
         return cudaErrorInvalidValue;
-    CUtensorMap mq, md;
+    CUtensorMap mq, md, mo;
     memset(&mq, 0, sizeof mq);
     memset(&md, 0, sizeof md);
-    if (!make_qkv_map(&mq, qkv, B, T, H * hs) || !make_do_map(&md, dout, B, T, H * hs))
+    memset(&mo, 0, sizeof mo);
+    if (!make_qkv_map(&mq, qkv, B, T, H * hs) || !make_do_map(&md, dout, B, T, H * hs) ||
+        !make_dqkv_map(&mo, dqkv, B, T, H * hs))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -992,9 +1034,9 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
-    fa_tc_bwd_dkv_kernel<<<grid, AT_THREADS, KV_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, B * H, st);
+    fa_tc_bwd_dkv_kernel<<<grid, BW_THREADS, KV_SMEM, s>>>(mq, md, mo, lse, D, T, H, B * H, st);
     CUDA_OK(cudaGetLastError());
-    fa_tc_bwd_dq_kernel<<<grid, AT_THREADS, DQ_SMEM, s>>>(mq, md, lse, D, dqkv, T, H, B * H, st);
+    fa_tc_bwd_dq_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, md, mo, lse, D, T, H, B * H, st);
     return cudaGetLastError();
 }
 
