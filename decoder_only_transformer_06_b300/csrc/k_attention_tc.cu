@@ -421,7 +421,8 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
 
 namespace {
 
-constexpr int BW_THREADS = 224;                 // 4 softmax warps, producer, two MMA issuers
+constexpr int BW_THREADS = 352;                 // 8 softmax warps, producer, two MMA issuers
+constexpr int BW_PRODUCER = 8, BW_ISSUE_A = 9, BW_ISSUE_B = 10;
 constexpr int BW_SLOTS = 3;
 constexpr int OUT_SLAB = 32 * AT_HS * 2;          // one warp's 32 output rows, 4 KB
 // dK/dV kernel: K and V double buffered per item, Q and dO in a 3-slot ring,
@@ -430,7 +431,7 @@ constexpr int KV_OFF_K = 0;                                  // [2]
 constexpr int KV_OFF_V = KV_OFF_K + 2 * AT_TILE;             // [2]
 constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [3]
 constexpr int KV_OFF_DO = KV_OFF_Q + BW_SLOTS * AT_TILE;     // [3]
-constexpr int KV_OFF_OUT = KV_OFF_DO + BW_SLOTS * AT_TILE;   // [4 warps][dK, dV] slabs
+constexpr int KV_OFF_OUT = KV_OFF_DO + BW_SLOTS * AT_TILE;   // [8 warps] dK or dV slab
 constexpr int KV_OFF_LD = KV_OFF_OUT + 8 * OUT_SLAB;         // lse2[2][128], D[2][128]
 constexpr int KV_OFF_BAR = KV_OFF_LD + 4 * 128 * 4;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
@@ -439,7 +440,7 @@ constexpr int DQ_OFF_Q = 0;                                  // [2]
 constexpr int DQ_OFF_DO = DQ_OFF_Q + 2 * AT_TILE;            // [2]
 constexpr int DQ_OFF_K = DQ_OFF_DO + 2 * AT_TILE;            // [3]
 constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;      // [3]
-constexpr int DQ_OFF_OUT = DQ_OFF_V + BW_SLOTS * AT_TILE;    // [4 warps] dQ slabs
+constexpr int DQ_OFF_OUT = DQ_OFF_V + BW_SLOTS * AT_TILE;    // [4 quarters] dQ slabs
 constexpr int DQ_OFF_BAR = DQ_OFF_OUT + 4 * OUT_SLAB;
 constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
 // TMEM columns. dK/dV: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383,
@@ -466,8 +467,10 @@ __device__ __forceinline__ void stage_out_slab(uint8_t* slab, int lane, const ui
 
 // Persistent like the forward: work items (key block kb, b, h), fewest key
 // blocks last (kb = w / (B*H)); g counts query blocks over all items, `it`
-// counts items. Warp 5 issues S^T = K Q^T and dP^T = V dO^T, warp 6 the
-// accumulating dV += P^T dO and dK += dS^T Q with P^T, dS^T read from TMEM.
+// counts items. Warp 9 issues S^T = K Q^T and dP^T = V dO^T, warp 10 the
+// accumulating dV += P^T dO and dK += dS^T Q with P^T, dS^T read from TMEM;
+// warp 8 loads; warps 0..7 compute P^T and dS^T, two warps per TMEM lane
+// quarter (no row reductions are needed here, so the columns split freely).
 __global__ void __launch_bounds__(BW_THREADS, 1)
 fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
@@ -506,7 +509,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         for (int i = 0; i < 2; i++) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
-            mbar_init(&ld_full[i], 4);
+            mbar_init(&ld_full[i], 8);
             mbar_init(&drain[i], 1);
         }
         for (int s = 0; s < BW_SLOTS; s++) {
@@ -514,21 +517,21 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             mbar_init(&qd_empty[s], 1);
         }
         mbar_init(st_full, 1);
-        mbar_init(st_free, 4);
-        mbar_init(ps_full, 4);
+        mbar_init(st_free, 8);
+        mbar_init(ps_full, 8);
         mbar_init(ps_free, 1);
         mbar_init(acc_full, 1);
-        mbar_init(acc_free, 4);
+        mbar_init(acc_free, 8);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    if (warp == BW_ISSUE_A) tmem_alloc(tmem_slot, AT_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == BW_PRODUCER) {
         if (lane == 0) {
             // ---------------- TMA producer
             int g = 0, it = 0, nkvl = 0, nql = 0;
@@ -558,7 +561,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                     wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == BW_ISSUE_A) {
         if (lane == 0) {
             // ---------------- S^T = K Q^T, dP^T = V dO^T (M = keys, N = queries, K = head dim)
             constexpr uint32_t id_s = make_idesc(AT_BK, AT_BQ, false, false);
@@ -593,7 +596,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                 wait_bounded(&drain[0], 0);
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == BW_ISSUE_B) {
         if (lane == 0) {
             // ---------------- dV += P^T dO, dK += dS^T Q (A from TMEM; dO, Q read MN-major)
             constexpr uint32_t id_a = make_idesc(AT_BK, AT_HS, false, true);
@@ -629,11 +632,28 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             }
         }
     } else {
-        // ---------------- warps 0..3: thread r owns key row r (TMEM lane r)
-        const int r = threadIdx.x;
+        // ---------------- warps 0..7: warp w reads TMEM lane quarter w % 4 (thread
+        // row r = its lane there: key row r) and query columns 64*(w/4)..+63
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = q4 * 32 + lane;
         const float sl2 = LOG2E_F * 0.125f;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
-        uint8_t* slab = sOut + warp * 2 * OUT_SLAB;        // [dK, dV] of this warp's 32 rows
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
+        uint8_t* slab = sOut + warp * OUT_SLAB;            // dK (hf 0) or dV (hf 1) of these 32 rows
+        // lse (log2 units) and D of query q0 + r of the block after the current one,
+        // loaded one block ahead so that their latency hides behind a block's work
+        auto fetch_ld = [&](int w_, int i_, float& l_, float& d_) {
+            l_ = INFINITY;
+            d_ = 0.f;
+            if (w_ < items) {
+                const int kb_ = w_ / BH, bh_ = w_ % BH, q_ = (kb_ + i_) * AT_BQ + r;
+                if (q_ < T) {
+                    l_ = lse[(int64_t)bh_ * T + q_] * LOG2E_F;
+                    d_ = Dg[(int64_t)bh_ * T + q_];
+                }
+            }
+        };
+        float nl, nd;
+        fetch_ld(blockIdx.x, 0, nl, nd);
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -641,16 +661,18 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             const int n = nb - kb;
             for (int i = 0; i < n; i++) {
                 const int G = g + i, ls = G & 1;
-                const int q0 = (kb + i) * AT_BQ;
-                {
-                    const int q = q0 + r;
-                    sL[ls * 128 + r] = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
-                    sD[ls * 128 + r] = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+                if (hf == 0) {
+                    sL[ls * 128 + r] = nl;
+                    sD[ls * 128 + r] = nd;
                 }
-                // every warp has staged its 32 rows (and, having passed the previous
-                // block's wait, every warp is done reading this slot's old values)
+                // the lower-half warps have staged their 32 rows; every warp, having
+                // passed the previous block's wait, is done reading this slot's old values
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ld_full[ls]);
+                if (hf == 0) {
+                    if (i + 1 < n) fetch_ld(w, i + 1, nl, nd);
+                    else fetch_ld(w + gridDim.x, 0, nl, nd);
+                }
                 ok = mbar_wait(&ld_full[ls], (uint32_t)((G >> 1) & 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
@@ -662,30 +684,35 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                 const float* L = sL + ls * 128;
                 const float* Dq = sD + ls * 128;
 #pragma unroll 1
-                for (int c = 0; c < 4; c++) {
+                for (int c = 2 * hf; c < 2 * hf + 2; c++) {
                     uint32_t sr[32], dr[32];
                     tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
                     tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
                     tmem_wait_ld();
-                    if (c == 3) {
+                    if (c == 2 * hf + 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(st_free);
                     }
                     uint32_t pp[16], pd[16];
 #pragma unroll
-                    for (int t = 0; t < 16; t++) {
-                        float p[2], d[2];
+                    for (int t4 = 0; t4 < 8; t4++) {
+                        const float4 l4 = *(const float4*)&L[32 * c + 4 * t4];     // broadcast reads
+                        const float4 d4 = *(const float4*)&Dq[32 * c + 4 * t4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float p[4], d[4];
 #pragma unroll
-                        for (int u = 0; u < 2; u++) {
-                            const int qq = 32 * c + 2 * t + u;
-                            float e = ex2f(fmaf(__uint_as_float(sr[2 * t + u]), sl2, -L[qq]));
+                        for (int u = 0; u < 4; u++) {
+                            const int qq = 32 * c + 4 * t4 + u;
+                            float e = ex2f(fmaf(__uint_as_float(sr[4 * t4 + u]), sl2, -lv[u]));
                             if (i == 0 && qq < r) e = 0.f;          // query before key: masked
                             p[u] = e;
-                            d[u] = e * (__uint_as_float(dr[2 * t + u]) - Dq[qq]);
+                            d[u] = e * (__uint_as_float(dr[4 * t4 + u]) - dv4[u]);
                         }
-                        pp[t] = pack2_bf16(p[0], p[1]);
-                        pd[t] = pack2_bf16(d[0], d[1]);
+                        pp[2 * t4] = pack2_bf16(p[0], p[1]);
+                        pp[2 * t4 + 1] = pack2_bf16(p[2], p[3]);
+                        pd[2 * t4] = pack2_bf16(d[0], d[1]);
+                        pd[2 * t4 + 1] = pack2_bf16(d[2], d[3]);
                     }
                     tmem_st16(lane_base + TM_PT + 16 * c, pp);
                     tmem_st16(lane_base + TM_DST + 16 * c, pd);
@@ -700,27 +727,23 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
             ok = mbar_wait(acc_full, (uint32_t)(it & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            uint32_t dv[64], dk[64];
-            tmem_ld32_nowait(lane_base + TM_ACC, dv);
-            tmem_ld32_nowait(lane_base + TM_ACC + 32, dv + 32);
-            tmem_ld32_nowait(lane_base + TM_ACC + 64, dk);
-            tmem_ld32_nowait(lane_base + TM_ACC + 96, dk + 32);
+            // lower-half warps take dK (TMEM columns 320..383), upper-half ones dV (256..319)
+            uint32_t acc[64];
+            const uint32_t tacc = lane_base + TM_ACC + (hf == 0 ? AT_HS : 0);
+            tmem_ld32_nowait(tacc, acc);
+            tmem_ld32_nowait(tacc + 32, acc + 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free);
-            if (lane == 0) tma_wait_read<0>();               // the previous item's stores have read the slabs
+            if (lane == 0) tma_wait_read<0>();               // the previous item's store has read the slab
             __syncwarp();
-            stage_out_slab(slab, lane, dk, 0.125f);
-            stage_out_slab(slab + OUT_SLAB, lane, dv, 1.f);
+            stage_out_slab(slab, lane, acc, hf == 0 ? 0.125f : 1.f);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                const int row0 = kb * AT_BK + warp * 32;
-                if (row0 < T) {
-                    tma_store_3d(&tm_out, slab, C + h * AT_HS, row0, b);
-                    tma_store_3d(&tm_out, slab + OUT_SLAB, 2 * C + h * AT_HS, row0, b);
-                }
+                const int row0 = kb * AT_BK + q4 * 32;
+                if (row0 < T) tma_store_3d(&tm_out, slab, (hf == 0 ? C : 2 * C) + h * AT_HS, row0, b);
                 tma_commit();
             }
             g += n;
@@ -732,14 +755,15 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         atomicOr(&st->err, ERR_TIMEOUT);
         st->timeout_site = 4;
     }
-    if (warp == 5) {
+    if (warp == BW_ISSUE_A) {
         tc_fence_after();
         tmem_dealloc(tmem_base, AT_TMEM_COLS);
     }
 }
 
-// Persistent: work items (query block qb, b, h), heaviest first. Warp 5 issues
-// S = Q K^T and dP = dO V^T, warp 6 the accumulating dQ += dS K (dS from TMEM).
+// Persistent: work items (query block qb, b, h), heaviest first. Warp 9 issues
+// S = Q K^T and dP = dO V^T, warp 10 the accumulating dQ += dS K (dS from
+// TMEM); warp 8 loads; warps 0..7 compute dS, two per TMEM lane quarter.
 __global__ void __launch_bounds__(BW_THREADS, 1)
 fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
@@ -776,7 +800,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             mbar_init(&qd_full[i], 1);
             mbar_init(&qd_empty[i], 1);
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_free[i], 4);
+            mbar_init(&acc_free[i], 8);
             mbar_init(&drain[i], 1);
         }
         for (int s = 0; s < BW_SLOTS; s++) {
@@ -784,19 +808,19 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             mbar_init(&kv_empty[s], 1);
         }
         mbar_init(st_full, 1);
-        mbar_init(st_free, 4);
-        mbar_init(ds_full, 4);
+        mbar_init(st_free, 8);
+        mbar_init(ds_full, 8);
         mbar_init(ds_free, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    if (warp == BW_ISSUE_A) tmem_alloc(tmem_slot, AT_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == BW_PRODUCER) {
         if (lane == 0) {
             // ---------------- TMA producer
             int g = 0, it = 0, nql = 0, nkvl = 0;
@@ -826,7 +850,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                     wait_bounded(&kv_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == BW_ISSUE_A) {
         if (lane == 0) {
             // ---------------- S = Q K^T, dP = dO V^T (M = queries, N = keys, K = head dim)
             constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
@@ -861,7 +885,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                 wait_bounded(&drain[0], 0);
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == BW_ISSUE_B) {
         if (lane == 0) {
             // ---------------- dQ += dS K (A = dS from TMEM, K read MN-major)
             constexpr uint32_t id_a = make_idesc(AT_BQ, AT_HS, false, true);
@@ -895,11 +919,27 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             }
         }
     } else {
-        // ---------------- warps 0..3: thread r owns query row r (TMEM lane r)
-        const int r = threadIdx.x;
+        // ---------------- warps 0..7: warp w reads TMEM lane quarter w % 4 (thread
+        // row r = its lane there: query row r) and key columns 64*(w/4)..+63
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = q4 * 32 + lane;
         const float sl2 = LOG2E_F * 0.125f;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
-        uint8_t* slab = sOut + warp * OUT_SLAB;
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
+        uint8_t* slab = sOut + q4 * OUT_SLAB;
+        // this row's lse (log2 units) and D for an item, loaded one item ahead
+        auto fetch_ld = [&](int w_, float& l_, float& d_) {
+            l_ = INFINITY;
+            d_ = 0.f;
+            if (w_ < items) {
+                const int qb_ = nqb - 1 - w_ / BH, bh_ = w_ % BH, q_ = qb_ * AT_BQ + r;
+                if (q_ < T) {
+                    l_ = lse[(int64_t)bh_ * T + q_] * LOG2E_F;
+                    d_ = Dg[(int64_t)bh_ * T + q_];
+                }
+            }
+        };
+        float nl, nd;
+        fetch_ld(blockIdx.x, nl, nd);
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -907,8 +947,8 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             const int nkv = qb + 1;
             const int q = qb * AT_BQ + r;
             const int ab = it & 1;
-            const float lse2 = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
-            const float Dq = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+            const float lse2 = nl, Dq = nd;
+            fetch_ld(w + gridDim.x, nl, nd);
             for (int j = 0; j < nkv; j++) {
                 const int G = g + j;
                 ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
@@ -919,12 +959,12 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                 const int key0 = j * AT_BK;
                 const bool edge = (j == qb) || (key0 + AT_BK > T);
 #pragma unroll 1
-                for (int c = 0; c < 4; c++) {
+                for (int c = 2 * hf; c < 2 * hf + 2; c++) {
                     uint32_t sr[32], dr[32];
                     tmem_ld32_nowait(lane_base + TM_S + 32 * c, sr);
                     tmem_ld32_nowait(lane_base + TM_DP + 32 * c, dr);
                     tmem_wait_ld();
-                    if (c == 3) {
+                    if (c == 2 * hf + 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(st_free);
@@ -953,22 +993,27 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
             ok = mbar_wait(&acc_full[ab], (uint32_t)((it >> 1) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
+            // the lower-half warp of each quarter writes the dQ rows
             uint32_t dq[64];
-            tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS, dq);
-            tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS + 32, dq + 32);
-            tmem_wait_ld();
+            if (hf == 0) {
+                tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS, dq);
+                tmem_ld32_nowait(lane_base + TM_ACC + ab * AT_HS + 32, dq + 32);
+                tmem_wait_ld();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_free[ab]);
-            if (lane == 0) tma_wait_read<0>();
-            __syncwarp();
-            stage_out_slab(slab, lane, dq, 0.125f);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                const int row0 = qb * AT_BQ + warp * 32;
-                if (row0 < T) tma_store_3d(&tm_out, slab, h * AT_HS, row0, b);
-                tma_commit();
+            if (hf == 0) {
+                if (lane == 0) tma_wait_read<0>();
+                __syncwarp();
+                stage_out_slab(slab, lane, dq, 0.125f);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int row0 = qb * AT_BQ + q4 * 32;
+                    if (row0 < T) tma_store_3d(&tm_out, slab, h * AT_HS, row0, b);
+                    tma_commit();
+                }
             }
             g += nkv;
         }
@@ -979,7 +1024,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
         atomicOr(&st->err, ERR_TIMEOUT);
         st->timeout_site = 5;
     }
-    if (warp == 5) {
+    if (warp == BW_ISSUE_A) {
         tc_fence_after();
         tmem_dealloc(tmem_base, AT_TMEM_COLS);
     }
