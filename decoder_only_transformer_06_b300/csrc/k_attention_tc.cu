@@ -432,8 +432,8 @@ constexpr int KV_OFF_V = KV_OFF_K + 2 * AT_TILE;             // [2]
 constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [3]
 constexpr int KV_OFF_DO = KV_OFF_Q + BW_SLOTS * AT_TILE;     // [3]
 constexpr int KV_OFF_OUT = KV_OFF_DO + BW_SLOTS * AT_TILE;   // [8 warps] dK or dV slab
-constexpr int KV_OFF_LD = KV_OFF_OUT + 8 * OUT_SLAB;         // lse2[2][128], D[2][128]
-constexpr int KV_OFF_BAR = KV_OFF_LD + 4 * 128 * 4;
+constexpr int KV_OFF_LD = KV_OFF_OUT + 8 * OUT_SLAB;         // [3 slots] lse2[128], D[128]
+constexpr int KV_OFF_BAR = KV_OFF_LD + BW_SLOTS * 2 * 128 * 4;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256 + 1024;
 // dQ kernel: Q and dO double buffered per item, K and V in a 3-slot ring
 constexpr int DQ_OFF_Q = 0;                                  // [2]
@@ -482,8 +482,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     uint8_t* sQ = smem + KV_OFF_Q;
     uint8_t* sDO = smem + KV_OFF_DO;
     uint8_t* sOut = smem + KV_OFF_OUT;
-    float* sL = (float*)(smem + KV_OFF_LD);          // [2][128] lse in log2 units
-    float* sD = sL + 256;                              // [2][128]
+    float* sLD = (float*)(smem + KV_OFF_LD);         // [3][lse (log2 units) 128, D 128]
     uint64_t* bars = (uint64_t*)(smem + KV_OFF_BAR);
     uint64_t* kv_full = bars;                          // [2]
     uint64_t* kv_empty = bars + 2;                     // [2]
@@ -495,9 +494,9 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     uint64_t* ps_free = bars + 13;
     uint64_t* acc_full = bars + 14;
     uint64_t* acc_free = bars + 15;
-    uint64_t* ld_full = bars + 16;                     // [2]
-    uint64_t* drain = bars + 18;                       // [2]
-    uint32_t* tmem_slot = (uint32_t*)(bars + 20);
+    uint64_t* ld_full = bars + 16;                     // [3] lse/D of the Q/dO slot staged
+    uint64_t* drain = bars + 19;                       // [2]
+    uint32_t* tmem_slot = (uint32_t*)(bars + 21);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nb = (T + AT_BK - 1) / AT_BK;
@@ -509,12 +508,12 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         for (int i = 0; i < 2; i++) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
-            mbar_init(&ld_full[i], 8);
             mbar_init(&drain[i], 1);
         }
         for (int s = 0; s < BW_SLOTS; s++) {
             mbar_init(&qd_full[s], 1);
             mbar_init(&qd_empty[s], 1);
+            mbar_init(&ld_full[s], 1);
         }
         mbar_init(st_full, 1);
         mbar_init(st_free, 8);
@@ -532,34 +531,51 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == BW_PRODUCER) {
-        if (lane == 0) {
-            // ---------------- TMA producer
-            int g = 0, it = 0, nkvl = 0, nql = 0;
-            bool ok = true;
-            for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
-                const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
-                const int n = nb - kb;
-                const int ks = it & 1;
-                if (!mbar_wait(&kv_empty[ks], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&kv_full[ks], 2 * AT_TILE);
-                tma_load_3d(sK + ks * AT_TILE, &tm_qkv, &kv_full[ks], C + h * AT_HS, kb * AT_BK, b);
-                tma_load_3d(sV + ks * AT_TILE, &tm_qkv, &kv_full[ks], 2 * C + h * AT_HS, kb * AT_BK, b);
-                nkvl++;
-                for (int i = 0; i < n; i++) {
-                    const int G = g + i, qs = G % BW_SLOTS;
-                    if (!mbar_wait(&qd_empty[qs], (uint32_t)(((G / BW_SLOTS) & 1) ^ 1), abort_flag)) { ok = false; break; }
+        // ---------------- producer warp: lane 0 issues the TMA copies; all lanes stage
+        // the lse (log2 units) and D values of each query block beside its Q/dO slot
+        int g = 0, it = 0, nkvl = 0, nql = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
+            const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
+            const int n = nb - kb;
+            const int ks = it & 1;
+            if (lane == 0) {
+                ok = mbar_wait(&kv_empty[ks], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag);
+                if (ok) {
+                    mbar_arrive_expect_tx(&kv_full[ks], 2 * AT_TILE);
+                    tma_load_3d(sK + ks * AT_TILE, &tm_qkv, &kv_full[ks], C + h * AT_HS, kb * AT_BK, b);
+                    tma_load_3d(sV + ks * AT_TILE, &tm_qkv, &kv_full[ks], 2 * C + h * AT_HS, kb * AT_BK, b);
+                    nkvl++;
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+            for (int i = 0; i < n; i++) {
+                const int G = g + i, qs = G % BW_SLOTS;
+                const int q0 = (kb + i) * AT_BQ;
+                ok = mbar_wait(&qd_empty[qs], (uint32_t)(((G / BW_SLOTS) & 1) ^ 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                if (lane == 0) {
                     mbar_arrive_expect_tx(&qd_full[qs], 2 * AT_TILE);
-                    tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
-                    tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, (kb + i) * AT_BQ, b);
+                    tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, q0, b);
+                    tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, q0, b);
                     nql++;
                 }
-                g += n;
+                float* ldst = sLD + qs * 256;
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const int qq = u * 32 + lane, q = q0 + qq;
+                    ldst[qq] = q < T ? lse[(int64_t)bh * T + q] * LOG2E_F : INFINITY;
+                    ldst[128 + qq] = q < T ? Dg[(int64_t)bh * T + q] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ld_full[qs]);
             }
-            if (!ok || *abort_flag) {
-                for (int i = (nkvl > 2 ? nkvl - 2 : 0); i < nkvl; i++) wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1));
-                for (int i = (nql > BW_SLOTS ? nql - BW_SLOTS : 0); i < nql; i++)
-                    wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
-            }
+            g += n;
+        }
+        if (lane == 0 && (!ok || *abort_flag)) {
+            for (int i = (nkvl > 2 ? nkvl - 2 : 0); i < nkvl; i++) wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1));
+            for (int i = (nql > BW_SLOTS ? nql - BW_SLOTS : 0); i < nql; i++)
+                wait_bounded(&qd_full[i % BW_SLOTS], (uint32_t)((i / BW_SLOTS) & 1));
         }
     } else if (warp == BW_ISSUE_A) {
         if (lane == 0) {
@@ -639,41 +655,14 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         const float sl2 = LOG2E_F * 0.125f;
         const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
         uint8_t* slab = sOut + warp * OUT_SLAB;            // dK (hf 0) or dV (hf 1) of these 32 rows
-        // lse (log2 units) and D of query q0 + r of the block after the current one,
-        // loaded one block ahead so that their latency hides behind a block's work
-        auto fetch_ld = [&](int w_, int i_, float& l_, float& d_) {
-            l_ = INFINITY;
-            d_ = 0.f;
-            if (w_ < items) {
-                const int kb_ = w_ / BH, bh_ = w_ % BH, q_ = (kb_ + i_) * AT_BQ + r;
-                if (q_ < T) {
-                    l_ = lse[(int64_t)bh_ * T + q_] * LOG2E_F;
-                    d_ = Dg[(int64_t)bh_ * T + q_];
-                }
-            }
-        };
-        float nl, nd;
-        fetch_ld(blockIdx.x, 0, nl, nd);
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
             const int kb = w / BH, bh = w % BH, h = bh % H, b = bh / H;
             const int n = nb - kb;
             for (int i = 0; i < n; i++) {
-                const int G = g + i, ls = G & 1;
-                if (hf == 0) {
-                    sL[ls * 128 + r] = nl;
-                    sD[ls * 128 + r] = nd;
-                }
-                // the lower-half warps have staged their 32 rows; every warp, having
-                // passed the previous block's wait, is done reading this slot's old values
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ld_full[ls]);
-                if (hf == 0) {
-                    if (i + 1 < n) fetch_ld(w, i + 1, nl, nd);
-                    else fetch_ld(w + gridDim.x, 0, nl, nd);
-                }
-                ok = mbar_wait(&ld_full[ls], (uint32_t)((G >> 1) & 1), abort_flag);
+                const int G = g + i, qs = G % BW_SLOTS;
+                ok = mbar_wait(&ld_full[qs], (uint32_t)((G / BW_SLOTS) & 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -681,8 +670,8 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
                 ok = mbar_wait(ps_free, (uint32_t)((G & 1) ^ 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                const float* L = sL + ls * 128;
-                const float* Dq = sD + ls * 128;
+                const float* L = sLD + qs * 256;
+                const float* Dq = L + 128;
 #pragma unroll 1
                 for (int c = 2 * hf; c < 2 * hf + 2; c++) {
                     uint32_t sr[32], dr[32];
