@@ -162,12 +162,13 @@ cudaError_t attention_bwd_f32(const float* qkv, const float* out, const float* l
 // tcgen05 flash attention (head size 64); bounded waits report into st
 cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
                                DevState* st, cudaStream_t s);
-// D = rowsum(dout * out) into Dbuf [B,H,T] (scratch), then the tcgen05 backward
+// the tcgen05 backward; Dbuf [B,H,T] (scratch) receives rowsum(dout * out)
 cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* lse,
                                const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,
                                int hs, DevState* st, cudaStream_t s);
-cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* D,
-                             bf16* dqkv, int B, int T, int H, int hs, DevState* st, cudaStream_t s);
+cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* out, const bf16* dout, const float* lse,
+                             float* D, bf16* dqkv, int B, int T, int H, int hs, DevState* st,
+                             cudaStream_t s);
 bool attention_bf16_supported(int T, int hs);
 
 // GEMMs

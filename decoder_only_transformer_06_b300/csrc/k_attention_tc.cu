@@ -409,7 +409,8 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
 
 // ------------------------------------------------------------------ backward
 // Deterministic (no atomics) backward in two kernels; the probabilities are
-// recomputed from the forward's lse, D = rowsum(dO * O) comes from a pre-pass.
+// recomputed from the forward's lse; the dQ kernel (run first) also computes
+// D = rowsum(dO * O) per query row and stores it for the dK/dV kernel.
 // With s the raw score q.k, p = exp(s/sqrt(hs) - lse), dP = dO V^T,
 // dS = P * (dP - D) (the gradient of the scaled scores):
 //   dK = dS^T Q / sqrt(hs), dV = P^T dO   (work item: one 128-key block)
@@ -441,7 +442,8 @@ constexpr int DQ_OFF_DO = DQ_OFF_Q + 2 * AT_TILE;            // [2]
 constexpr int DQ_OFF_K = DQ_OFF_DO + 2 * AT_TILE;            // [3]
 constexpr int DQ_OFF_V = DQ_OFF_K + BW_SLOTS * AT_TILE;      // [3]
 constexpr int DQ_OFF_OUT = DQ_OFF_V + BW_SLOTS * AT_TILE;    // [4 quarters] dQ slabs
-constexpr int DQ_OFF_BAR = DQ_OFF_OUT + 4 * OUT_SLAB;
+constexpr int DQ_OFF_O = DQ_OFF_OUT + 4 * OUT_SLAB;          // [2] forward output tile (for D)
+constexpr int DQ_OFF_BAR = DQ_OFF_O + 2 * AT_TILE;
 constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
 // TMEM columns. dK/dV: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383,
 // P^T 384..447 and dS^T 448..511 (bf16 pairs, the A operands of dV and dK).
@@ -755,8 +757,9 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
 // TMEM); warp 8 loads; warps 0..7 compute dS, two per TMEM lane quarter.
 __global__ void __launch_bounds__(BW_THREADS, 1)
 fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ lse,
-                    const float* __restrict__ Dg, int T, int H, int BH, DevState* st) {
+                    const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_o,
+                    const float* __restrict__ lse, float* __restrict__ Dg, int T, int H, int BH,
+                    DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = smem + DQ_OFF_Q;
@@ -764,6 +767,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     uint8_t* sK = smem + DQ_OFF_K;
     uint8_t* sV = smem + DQ_OFF_V;
     uint8_t* sOut = smem + DQ_OFF_OUT;
+    uint8_t* sO = smem + DQ_OFF_O;
     uint64_t* bars = (uint64_t*)(smem + DQ_OFF_BAR);
     uint64_t* qd_full = bars;                          // [2]
     uint64_t* qd_empty = bars + 2;                     // [2]
@@ -787,7 +791,9 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; i++) {
             mbar_init(&qd_full[i], 1);
-            mbar_init(&qd_empty[i], 1);
+            // released by the item's last S/dP products and by the eight softmax
+            // warps once they have read their dO rows (for D)
+            mbar_init(&qd_empty[i], 9);
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_free[i], 8);
             mbar_init(&drain[i], 1);
@@ -819,9 +825,10 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
                 const int nkv = qb + 1;
                 const int qs = it & 1;
                 if (!mbar_wait(&qd_empty[qs], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(&qd_full[qs], 2 * AT_TILE);
+                mbar_arrive_expect_tx(&qd_full[qs], 3 * AT_TILE);
                 tma_load_3d(sQ + qs * AT_TILE, &tm_qkv, &qd_full[qs], h * AT_HS, qb * AT_BQ, b);
                 tma_load_3d(sDO + qs * AT_TILE, &tm_do, &qd_full[qs], h * AT_HS, qb * AT_BQ, b);
+                tma_load_3d(sO + qs * AT_TILE, &tm_o, &qd_full[qs], h * AT_HS, qb * AT_BQ, b);
                 nql++;
                 for (int j = 0; j < nkv; j++) {
                     const int G = g + j, s = G % BW_SLOTS;
@@ -916,28 +923,50 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
         const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
         uint8_t* slab = sOut + q4 * OUT_SLAB;
         // this row's lse (log2 units) and D for an item, loaded one item ahead
-        auto fetch_ld = [&](int w_, float& l_, float& d_) {
+        // this row's lse (log2 units) for an item, loaded one item ahead
+        auto fetch = [&](int w_, float& l_) {
             l_ = INFINITY;
-            d_ = 0.f;
             if (w_ < items) {
                 const int qb_ = nqb - 1 - w_ / BH, bh_ = w_ % BH, q_ = qb_ * AT_BQ + r;
-                if (q_ < T) {
-                    l_ = lse[(int64_t)bh_ * T + q_] * LOG2E_F;
-                    d_ = Dg[(int64_t)bh_ * T + q_];
-                }
+                if (q_ < T) l_ = lse[(int64_t)bh_ * T + q_] * LOG2E_F;
             }
         };
-        float nl, nd;
-        fetch_ld(blockIdx.x, nl, nd);
+        float nl;
+        fetch(blockIdx.x, nl);
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
             const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
             const int nkv = qb + 1;
             const int q = qb * AT_BQ + r;
-            const int ab = it & 1;
-            const float lse2 = nl, Dq = nd;
-            fetch_ld(w + gridDim.x, nl, nd);
+            const int ab = it & 1, qs = it & 1;
+            const float lse2 = nl;
+            fetch(w + gridDim.x, nl);
+            // D = rowsum(dO * O) from this row of the dO and O tiles (128B-swizzled);
+            // written once for the dK/dV kernel
+            ok = mbar_wait(&qd_full[qs], (uint32_t)((it >> 1) & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            float Dq = 0.f;
+            {
+                const uint8_t* drow = sDO + qs * AT_TILE + r * 128;
+                const uint8_t* orow = sO + qs * AT_TILE + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint4 dv = *(const uint4*)(drow + ((c ^ (r & 7)) << 4));
+                    const uint4 ov = *(const uint4*)(orow + ((c ^ (r & 7)) << 4));
+                    const uint32_t du[4] = {dv.x, dv.y, dv.z, dv.w};
+                    const uint32_t ou[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; k2++) {
+                        const float2 a2 = __bfloat1622float2(*(const __nv_bfloat162*)&du[k2]);
+                        const float2 o2 = __bfloat1622float2(*(const __nv_bfloat162*)&ou[k2]);
+                        Dq = fmaf(a2.x, o2.x, fmaf(a2.y, o2.y, Dq));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qd_empty[qs]);
+            if (hf == 0 && q < T) Dg[(int64_t)bh * T + q] = Dq;
             for (int j = 0; j < nkv; j++) {
                 const int G = g + j;
                 ok = mbar_wait(st_full, (uint32_t)(G & 1), abort_flag);
@@ -1019,7 +1048,8 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
     }
 }
 
-// dout [B, T, C] bf16 as a 3-D map {C, T, B}, boxes 64 x 128 x 1, 128B swizzle.
+// dout (or the forward output) [B, T, C] bf16 as a 3-D map {C, T, B}, boxes
+// 64 x 128 x 1, 128B swizzle.
 static bool make_do_map(CUtensorMap* map, const bf16* dout, int B, int T, int C) {
     EncodeTiledFnA enc = encode_fn();
     if (!enc) return false;
@@ -1046,17 +1076,19 @@ static bool make_dqkv_map(CUtensorMap* map, bf16* dqkv, int B, int T, int C) {
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* D,
-                             bf16* dqkv, int B, int T, int H, int hs, DevState* st, cudaStream_t s) {
+cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* out, const bf16* dout, const float* lse,
+                             float* D, bf16* dqkv, int B, int T, int H, int hs, DevState* st,
+                             cudaStream_t s) {
     if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
-    if (((uintptr_t)qkv & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15))
+    if (((uintptr_t)qkv & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15) || ((uintptr_t)out & 15))
         return cudaErrorInvalidValue;
-    CUtensorMap mq, md, mo;
+    CUtensorMap mq, md, mo, mf;
     memset(&mq, 0, sizeof mq);
     memset(&md, 0, sizeof md);
     memset(&mo, 0, sizeof mo);
+    memset(&mf, 0, sizeof mf);
     if (!make_qkv_map(&mq, qkv, B, T, H * hs) || !make_do_map(&md, dout, B, T, H * hs) ||
-        !make_dqkv_map(&mo, dqkv, B, T, H * hs))
+        !make_dqkv_map(&mo, dqkv, B, T, H * hs) || !make_do_map(&mf, out, B, T, H * hs))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -1068,37 +1100,11 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
-    fa_tc_bwd_dkv_kernel<<<grid, BW_THREADS, KV_SMEM, s>>>(mq, md, mo, lse, D, T, H, B * H, st);
+    // the dQ kernel also computes D = rowsum(dO * O), which the dK/dV kernel reads
+    fa_tc_bwd_dq_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, md, mo, mf, lse, D, T, H, B * H, st);
     CUDA_OK(cudaGetLastError());
-    fa_tc_bwd_dq_kernel<<<grid, BW_THREADS, DQ_SMEM, s>>>(mq, md, mo, lse, D, T, H, B * H, st);
+    fa_tc_bwd_dkv_kernel<<<grid, BW_THREADS, KV_SMEM, s>>>(mq, md, mo, lse, D, T, H, B * H, st);
     return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ D pre-pass
-// D[b,h,i] = sum_c dO[i, h*64+c] * O[i, h*64+c]; one thread per (row, head).
-__global__ void fa_bwd_d_kernel(const bf16* __restrict__ out, const bf16* __restrict__ dout,
-                                float* __restrict__ D, int B, int T, int H) {
-    int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (int64_t)B * T * H) return;
-    int h = (int)(idx % H);
-    int64_t row = idx / H;             // b*T + t
-    int64_t b = row / T, tt = row % T;
-    const int C = H * AT_HS;
-    const uint4* o4 = (const uint4*)(out + row * C + h * AT_HS);
-    const uint4* d4 = (const uint4*)(dout + row * C + h * AT_HS);
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-        uint4 a = o4[q], c = d4[q];
-        const __nv_bfloat162* ha = (const __nv_bfloat162*)&a;
-        const __nv_bfloat162* hc = (const __nv_bfloat162*)&c;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            float2 fa = __bfloat1622float2(ha[j]), fc = __bfloat1622float2(hc[j]);
-            s += fa.x * fc.x + fa.y * fc.y;
-        }
-    }
-    D[(b * H + h) * T + tt] = s;
 }
 
 bool attention_bf16_supported(int T, int hs) { return hs == AT_HS && T >= 1; }
@@ -1107,10 +1113,7 @@ cudaError_t attention_bwd_bf16(const bf16* qkv, const bf16* out, const float* ls
                                const bf16* dout, bf16* dqkv, float* Dbuf, int B, int T, int H,
                                int hs, DevState* st, cudaStream_t s) {
     if (!attention_bf16_supported(T, hs)) return cudaErrorInvalidValue;
-    int64_t n = (int64_t)B * T * H;
-    fa_bwd_d_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(out, dout, Dbuf, B, T, H);
-    CUDA_OK(cudaGetLastError());
-    return attention_bwd_tc(qkv, dout, lse, Dbuf, dqkv, B, T, H, hs, st, s);
+    return attention_bwd_tc(qkv, out, dout, lse, Dbuf, dqkv, B, T, H, hs, st, s);
 }
 
 }  // namespace k
