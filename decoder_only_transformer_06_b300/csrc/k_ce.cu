@@ -140,10 +140,10 @@ ce_kernel(Act* __restrict__ logits, const int32_t* __restrict__ tgt, float* __re
 
 
 // ------------------------------------------------------------------ bf16 rows
-// Persistent variant for bf16 logits whose row fits twice in shared memory
-// (Vp <= 55296): one CTA per SM walks rows blockIdx.x, +gridDim.x, ...; row
-// i+1 is fetched by one TMA bulk copy while row i is processed, and the
-// gradient row is written back by one TMA bulk store. Per row:
+// Persistent variant for bf16 logits whose row fits in shared memory (Vp <=
+// 110000): two CTAs per SM, each walking rows blockIdx.x, +gridDim.x, ...
+// with one row buffer: a row arrives by one TMA bulk copy and the gradient row
+// leaves by one bulk store, while the other CTA on the SM computes. Per row:
 //   pass 1  max over j < V (packed bf16x2 max);
 //   pass 2  e_j = exp(z_j - max) in fp32, sum in fp32, e_j kept as bf16 in place;
 //   pass 3  dz_j = (e_j / sum - [j == y]) * scale, 0 on pad columns.
@@ -162,48 +162,37 @@ __device__ __forceinline__ float block_reduce_n(float v, bool is_max, float* sm)
     return r;
 }
 
-__global__ void __launch_bounds__(CEB_THREADS, 1)
+__global__ void __launch_bounds__(CEB_THREADS, 2)
 ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
                float* __restrict__ row_loss, int M, int V, int Vp, DevState* st) {
     extern __shared__ __align__(128) uint8_t ce_smem[];
     const uint32_t rowbytes = (uint32_t)Vp * 2;
     const uint32_t padbytes = (rowbytes + 127) & ~127u;
-    bf16* bufs[2] = {(bf16*)ce_smem, (bf16*)(ce_smem + padbytes)};
-    uint64_t* bar = (uint64_t*)(ce_smem + 2 * padbytes);
-    float* red = (float*)(bar + 2);
+    bf16* cur = (bf16*)ce_smem;
+    uint64_t* bar = (uint64_t*)(ce_smem + padbytes);
+    float* red = (float*)(bar + 1);
     const int tid = threadIdx.x;
     if (tid == 0) {
-        ptx::mbar_init(&bar[0], 1);
-        ptx::mbar_init(&bar[1], 1);
+        ptx::mbar_init(bar, 1);
         ptx::fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0 && (int)blockIdx.x < M) {
-        ptx::mbar_arrive_expect_tx(&bar[0], rowbytes);
-        ptx::bulk_g2s(bufs[0], logits + (int64_t)blockIdx.x * Vp, rowbytes, &bar[0]);
-    }
     const int nvec = Vp / 8;          // 16-byte chunks per row
     const int nfull = V / 8;          // chunks entirely below V
     const float L2E = 1.4426950408889634f;
     const float scale_valid = st->inv_count;
-    int i = 0;
-    for (int row = blockIdx.x; row < M; row += gridDim.x, i++) {
-        const int b = i & 1;
-        const uint32_t par = (uint32_t)((i >> 1) & 1);
-        bf16* cur = bufs[b];
-        const int next = row + gridDim.x;
-        if (tid == 0 && next < M) {
-            ptx::bulk_wait_read_all();            // previous store out of bufs[b^1] has read it
-            ptx::mbar_arrive_expect_tx(&bar[b ^ 1], rowbytes);
-            ptx::bulk_g2s(bufs[b ^ 1], logits + (int64_t)next * Vp, rowbytes, &bar[b ^ 1]);
+    uint32_t par = 0;
+    for (int row = blockIdx.x; row < M; row += gridDim.x, par ^= 1) {
+        if (tid == 0) {
+            ptx::bulk_wait_read_all();            // the previous row's store has read the buffer
+            ptx::mbar_arrive_expect_tx(bar, rowbytes);
+            ptx::bulk_g2s(cur, logits + (int64_t)row * Vp, rowbytes, bar);
         }
-        const bool ok = ptx::mbar_wait_bounded(&bar[b], par);
+        const bool ok = ptx::mbar_wait_bounded(bar, par);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 atomicOr(&st->err, ERR_TIMEOUT);
                 st->timeout_site = 2;
-                // drain (bounded) the prefetch this thread may have issued
-                if (next < M) ptx::mbar_wait_bounded(&bar[b ^ 1], (uint32_t)(((i + 1) >> 1) & 1));
             }
             break;
         }
@@ -214,6 +203,7 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
         const uint4* cv = (const uint4*)cur;
         // pass 1: max
         __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll 4
         for (int vi = tid; vi < nfull; vi += CEB_THREADS) {
             uint4 w = cv[vi];
             const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
@@ -227,6 +217,7 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
         const float mxl = mx * L2E;
         // pass 2: e = exp(z - max), sum; e kept in place as bf16
         float sum = 0.f;
+#pragma unroll 2
         for (int vi = tid; vi < nfull; vi += CEB_THREADS) {
             uint4 w = cv[vi];
             const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
@@ -253,6 +244,7 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
         const float inv = 1.0f / sum;
         const float scale = ignore ? 0.f : scale_valid;
         // pass 3: gradient in place
+#pragma unroll 2
         for (int vi = tid; vi < nvec; vi += CEB_THREADS) {
             uint4 o;
             uint32_t* op = (uint32_t*)&o;
@@ -299,11 +291,13 @@ cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int 
     if (Vp % VEC) return cudaErrorInvalidValue;
     if constexpr (sizeof(Act) == 2) {
         const size_t pad = ((size_t)Vp * 2 + 127) & ~(size_t)127;
-        const size_t smem = 2 * pad + 16 + CEB_THREADS / 32 * sizeof(float);
-        if (Vp >= 1024 && smem <= 227 * 1024) {
+        const size_t smem = pad + 16 + CEB_THREADS / 32 * sizeof(float);
+        if (Vp >= 1024 && smem <= 110 * 1024) {
             CUDA_OK(cudaFuncSetAttribute(ce_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem));
-            int grid = M < num_sms() ? M : num_sms();
+            CUDA_OK(cudaFuncSetAttribute(ce_bulk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         100));
+            int grid = M < 2 * num_sms() ? M : 2 * num_sms();
             ce_bulk_kernel<<<grid, CEB_THREADS, smem, s>>>((bf16*)logits, tgt, row_loss, M, V, Vp, st);
             return cudaGetLastError();
         }
