@@ -117,11 +117,15 @@ __device__ __forceinline__ void unstage_bf16(const uint8_t* tile, int lane, floa
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN>
+// PAIR: the tile is 256 x BN and is shared by a cluster of two CTAs (one
+// tcgen05.mma with cta_group::2 covers both): each CTA stages its own 128 rows
+// of A and half (BN/2 rows) of B, and holds its own 128 x BN accumulator.
+template <int BN, bool PAIR>
 struct TcCfg {
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
-    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int B_BYTES = B_ROWS * TC_BK * 2;
+    static constexpr int STAGES = (A_BYTES + B_BYTES) == 32768 ? 6 : (BN == 256 ? 4 : 6);
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
@@ -134,12 +138,12 @@ struct EpiMaps {
     CUtensorMap o1, o2, aux;
 };
 
-template <int BN, bool A_MN, bool B_MN, int KIND>
+template <int BN, bool A_MN, bool B_MN, int KIND, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ EpiMaps maps, int M, int N, int K, int splits,
                const float* __restrict__ bias, DevState* st) {
-    using Cfg = TcCfg<BN>;
+    using Cfg = TcCfg<BN, PAIR>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -156,6 +160,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // pair: rank 0 issues the MMAs; its full[] barriers count both CTAs'
+    // operand bytes and its tempty[] barriers both CTAs' epilogue warps
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(&full[s], 1);
@@ -163,20 +171,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], EPI_WARPS);
+            mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
         for (int i = 0; i < EPI_WARPS; i++) mbar_init(&auxbar[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR) tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        else tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync();      // the peer's barriers exist before any remote arrive
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // work is dealt per pair: both CTAs of a cluster walk the same tile list
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr int TILE_M = PAIR ? 2 * TC_BM : TC_BM;
 
-    const int num_m = (M + TC_BM - 1) / TC_BM;
+    const int num_m = (M + TILE_M - 1) / TILE_M;
     const int num_n = (N + BN - 1) / BN;
     const int tiles = num_m * num_n;
     const int kblocks = (K + TC_BK - 1) / TC_BK;
@@ -190,34 +206,57 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            // the barrier that counts this CTA's bytes: its own, or the leader's
+            const uint32_t full0 = PAIR ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
+            for (int w = unit; w < total && ok; w += units) {
                 int split = w / tiles, mt, nt;
                 tile_coords(w - split * tiles, num_m, num_n, mt, nt);
+                const int m_row = mt * TILE_M + (int)rank * TC_BM;
+                const int n_row = nt * BN + (int)rank * Cfg::B_ROWS;
                 int kb0 = split * kpb, kb1 = min(kb0 + kpb, kblocks);
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], (PAIR ? 2 : 1) * Cfg::STAGE_BYTES);
                     uint8_t* a = sA + stage * Cfg::A_BYTES;
                     uint8_t* b = sB + stage * Cfg::B_BYTES;
                     const int k0 = kb * TC_BK;
-                    if (!A_MN) {
-                        tma_load_2d(a, &tmA, &full[stage], k0, mt * TC_BM);
-                    } else {
-                        tma_load_2d(a, &tmA, &full[stage], mt * TC_BM, k0);
-                        tma_load_2d(a + 8192, &tmA, &full[stage], mt * TC_BM + 64, k0);
-                    }
-                    if (!B_MN) {
-                        tma_load_2d(b, &tmB, &full[stage], k0, nt * BN);
-                    } else {
+                    if constexpr (PAIR) {
+                        const uint32_t fb = full0 + (uint32_t)stage * 8u;
+                        if (!A_MN) {
+                            tma_load_2d_pair(a, &tmA, fb, k0, m_row);
+                        } else {
+                            tma_load_2d_pair(a, &tmA, fb, m_row, k0);
+                            tma_load_2d_pair(a + 8192, &tmA, fb, m_row + 64, k0);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d_pair(b, &tmB, fb, k0, n_row);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; j++)
-                            tma_load_2d(b + j * 8192, &tmB, &full[stage], nt * BN + 64 * j, k0);
+                            for (int j = 0; j < Cfg::B_ROWS / 64; j++)
+                                tma_load_2d_pair(b + j * 8192, &tmB, fb, n_row + 64 * j, k0);
+                        }
+                    } else {
+                        if (!A_MN) {
+                            tma_load_2d(a, &tmA, &full[stage], k0, m_row);
+                        } else {
+                            tma_load_2d(a, &tmA, &full[stage], m_row, k0);
+                            tma_load_2d(a + 8192, &tmA, &full[stage], m_row + 64, k0);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d(b, &tmB, &full[stage], k0, n_row);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; j++)
+                                tma_load_2d(b + j * 8192, &tmB, &full[stage], n_row + 64 * j, k0);
+                        }
                     }
                     issued++;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok || *abort_flag) {
+            // the peer's copies complete on the leader's barriers, which the
+            // leader's MMA issuer waits for; only the leader drains here
+            if (leader && (!ok || *abort_flag)) {
                 // drain: wait (bounded, ignoring the abort flag) for our last copies
                 long first = issued > STAGES ? issued - STAGES : 0;
                 for (long i = first; i < issued; i++) {
@@ -229,9 +268,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = make_idesc(TC_BM, BN, A_MN, B_MN);
+            constexpr uint32_t idesc = make_idesc(TILE_M, BN, A_MN, B_MN);
             constexpr uint32_t A_LBO = A_MN ? 8192 : 16, B_LBO = B_MN ? 8192 : 16;
             constexpr uint32_t KSTEP_A = A_MN ? 2048 : 32, KSTEP_B = B_MN ? 2048 : 32;
             const uint64_t dA0 = smem_desc(smem_u32(sA), A_LBO, 1024);
@@ -242,10 +281,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int w = unit; w < total && ok; w += units) {
                 int split = w / tiles;
                 int kb0 = split * kpb, kb1 = min(kb0 + kpb, kblocks);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!(PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1, abort_flag)
+                           : mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -254,23 +294,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint64_t ad = desc_adv(dA0, stage * Cfg::A_BYTES);
                     const uint64_t bd = desc_adv(dB0, stage * Cfg::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < TC_BK / 16; kk++)
-                        mma_bf16(d_tmem, desc_adv(ad, kk * KSTEP_A), desc_adv(bd, kk * KSTEP_B), idesc,
-                                 (kb > kb0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < TC_BK / 16; kk++) {
+                        if constexpr (PAIR)
+                            mma_bf16_pair(d_tmem, desc_adv(ad, kk * KSTEP_A), desc_adv(bd, kk * KSTEP_B),
+                                          idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        else
+                            mma_bf16(d_tmem, desc_adv(ad, kk * KSTEP_A), desc_adv(bd, kk * KSTEP_B), idesc,
+                                     (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
                     any = true;
-                    mma_commit(&empty[stage]);
+                    if constexpr (PAIR) mma_commit_pair(&empty[stage], 3);
+                    else mma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                mma_commit(&tfull[acc]);
+                if constexpr (PAIR) mma_commit_pair(&tfull[acc], 3);
+                else mma_commit(&tfull[acc]);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
-            if (any) {
+            if constexpr (PAIR) {
+                // every MMA of the pair completes (in both CTAs' TMEM and
+                // shared memory) before either CTA releases them
+                mma_commit_pair(drain, 3);
+            } else if (any) {
                 // all MMAs of this CTA complete before TMEM is released
                 mma_commit(drain);
                 const long long t0 = wait_clock();
                 while (!mbar_try_wait(drain, 0) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
             }
+        }
+        if (PAIR && lane == 0) {
+            const long long t0 = wait_clock();
+            while (!mbar_try_wait_cluster(drain, 0) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
         }
     } else {
         // ---------------- epilogue warps 2..9: TMEM lane quarter q4 = warp % 4
@@ -293,10 +348,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc_phase = 0;
         uint32_t seq = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        // the MMA issuer's tempty[] barriers (the leader's, in a pair)
+        const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
+        for (int w = unit; w < total && ok; w += units) {
             int split = w / tiles, mt, nt;
             tile_coords(w - split * tiles, num_m, num_n, mt, nt);
-            const int m_base = mt * TC_BM + q4 * 32;
+            const int m_base = mt * TILE_M + (int)rank * TC_BM + q4 * 32;
             const int n_half = nt * BN + half * (BN / 2);
             // lane j holds bias[n_half + 32c + j] for chunk c; broadcast by shuffle
             float bz[NCH];
@@ -324,7 +381,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // the accumulator is free for the MMA once its last chunk is in registers
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                    if (lane == 0) {
+                        if constexpr (PAIR) mbar_arrive_cluster(tempty0 + (uint32_t)acc * 8u);
+                        else mbar_arrive(&tempty[acc]);
+                    }
                 }
                 float v[32];
                 if (bias != nullptr) {
@@ -395,14 +455,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     }
-    __syncthreads();
+    // pair: no remote arrive or copy may still target a CTA that has exited
+    tc_fence_before();
+    if constexpr (PAIR) cluster_sync();
+    else __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) {
         atomicOr(&st->err, ERR_TIMEOUT);
         st->timeout_site = 1;
     }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -480,15 +544,37 @@ bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, c
     return true;
 }
 
-template <int BN, bool A_MN, bool B_MN, int KIND>
+// Clusters of two 1-CTA-per-SM GEMM CTAs that can be resident at once.
+template <typename Kern>
+static int max_pairs(Kern kern, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int BN, bool A_MN, bool B_MN, int KIND, bool PAIR>
 static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                              int splits, DevState* st, cudaStream_t s) {
-    using Cfg = TcCfg<BN>;
+    using Cfg = TcCfg<BN, PAIR>;
     CUtensorMap ta, tb;
     bool ok = A_MN ? make_operand_map(&ta, A.ptr, (uint64_t)M, (uint64_t)K, A.ld, 64, 64)
                    : make_operand_map(&ta, A.ptr, (uint64_t)K, (uint64_t)M, A.ld, 64, TC_BM);
     ok = ok && (B_MN ? make_operand_map(&tb, B.ptr, (uint64_t)N, (uint64_t)K, B.ld, 64, 64)
-                     : make_operand_map(&tb, B.ptr, (uint64_t)K, (uint64_t)N, B.ld, 64, BN));
+                     : make_operand_map(&tb, B.ptr, (uint64_t)K, (uint64_t)N, B.ld, 64, Cfg::B_ROWS));
     EpiMaps maps;
     memset(&maps, 0, sizeof maps);
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -505,29 +591,51 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     if (KIND == EPI_GELU_BWD)
         ok = ok && make_map(&maps.aux, epi.aux, BF, 2, N, M, epi.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return cudaErrorInvalidValue;
+    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, KIND, PAIR>;
     static bool attr_set = false;
+    static int pairs = 0;
     if (!attr_set) {
-        CUDA_OK(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN, KIND>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM));
+        CUDA_OK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM));
+        if (PAIR) {
+            pairs = max_pairs(kern, Cfg::SMEM);
+            if (pairs < 1) return cudaErrorInvalidConfiguration;
+        }
         attr_set = true;
     }
-    const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N + BN - 1) / BN);
+    constexpr int TILE_M = PAIR ? 2 * TC_BM : TC_BM;
+    const int tiles = ((M + TILE_M - 1) / TILE_M) * ((N + BN - 1) / BN);
     const int total = tiles * splits;
-    const int grid = total < num_sms() ? total : num_sms();
-    gemm_tc_kernel<BN, A_MN, B_MN, KIND><<<grid, TC_THREADS, Cfg::SMEM, s>>>(
-        ta, tb, maps, M, N, K, splits, epi.bias, st);
-    return cudaGetLastError();
+    if (!PAIR) {
+        const int grid = total < num_sms() ? total : num_sms();
+        kern<<<grid, TC_THREADS, Cfg::SMEM, s>>>(ta, tb, maps, M, N, K, splits, epi.bias, st);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (total < pairs ? total : pairs), 1, 1);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, M, N, K, splits, epi.bias, st);
 }
 
+// BN = 256 tiles run as CTA pairs (cta_group::2); BN = 128 as single CTAs.
 template <int BN, bool A_MN, bool B_MN>
 static cudaError_t launch_kind(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                                int splits, DevState* st, cudaStream_t s) {
+    constexpr bool P = (BN == 256);
     switch (epi.kind) {
-        case EPI_STORE_ACT: return launch_tc<BN, A_MN, B_MN, EPI_STORE_ACT>(M, N, K, A, B, epi, splits, st, s);
-        case EPI_GELU: return launch_tc<BN, A_MN, B_MN, EPI_GELU>(M, N, K, A, B, epi, splits, st, s);
-        case EPI_GELU_BWD: return launch_tc<BN, A_MN, B_MN, EPI_GELU_BWD>(M, N, K, A, B, epi, splits, st, s);
-        case EPI_STORE_F32: return launch_tc<BN, A_MN, B_MN, EPI_STORE_F32>(M, N, K, A, B, epi, splits, st, s);
-        case EPI_ACCUM_F32: return launch_tc<BN, A_MN, B_MN, EPI_ACCUM_F32>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_STORE_ACT: return launch_tc<BN, A_MN, B_MN, EPI_STORE_ACT, P>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_GELU: return launch_tc<BN, A_MN, B_MN, EPI_GELU, P>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_GELU_BWD: return launch_tc<BN, A_MN, B_MN, EPI_GELU_BWD, P>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_STORE_F32: return launch_tc<BN, A_MN, B_MN, EPI_STORE_F32, P>(M, N, K, A, B, epi, splits, st, s);
+        case EPI_ACCUM_F32: return launch_tc<BN, A_MN, B_MN, EPI_ACCUM_F32, P>(M, N, K, A, B, epi, splits, st, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -42,10 +42,13 @@ def test_gemm_bf16_fp32_out(M, N, K, ak, bk):
     assert np.abs(got - ref).max() <= 1e-4 * math.sqrt(K) * 4, (M, N, K, ak, bk)
 
 
+# N = 384 runs 128-wide single-CTA tiles, N = 768 256-wide tiles on CTA pairs
+# (M = 320 leaves the second pair tile more than half empty)
+@pytest.mark.parametrize("N", [384, 768])
 @pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 0)])
-def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk):
-    M, N, K = 320, 384, 256
-    a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, 5)
+def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk, N):
+    M, K = 320, 256
+    a, lda, b, ldb, ref = _gemm_case(M, N, K, ak, bk, 5 + N)
     bias = torch.randn(N, dtype=torch.float32).cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     gpt2.op_gemm_bf16(M, N, K, a, lda, ak, b, ldb, bk, bias=bias, out_bf16=out)
