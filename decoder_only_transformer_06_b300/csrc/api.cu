@@ -55,6 +55,12 @@ struct gpt2_model {
     bool use_bf16 = false;
     size_t act_bytes = 4;
     cudaStream_t stream = nullptr;
+    // Weight-gradient work of the backward (dW GEMMs, their split-K reduce,
+    // bias column sums) runs here, forked from and joined back to `stream`
+    // by events, so that it fills the SMs the main chain leaves idle.
+    cudaStream_t side = nullptr;
+    std::vector<cudaEvent_t> xev;
+    int xev_next = 0;
 
     std::vector<TensorRec> tensors;
     int64_t n_arena = 0, decay_end = 0;
@@ -372,6 +378,7 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     CK(m, cudaMemset(m->adam_v, 0, nb));
     CK(m, cudaMemset(m->st, 0, sizeof(DevState)));
     if (m->use_bf16) CK(m, k::f32_to_bf16(m->params, m->pbf, m->decay_end, nullptr));
+    CK(m, cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking));
     CK(m, cudaDeviceSynchronize());
     return GPT2_OK;
 }
@@ -462,14 +469,14 @@ struct Op {
     }
     // dW[N_out, K_in] += dY^T X, dY [M, N_out] (ld ldy), X [M, K_in] (ld ldx).
     int gemm_dw(const char* site, int n_out, int k_in, const void* dy, int64_t ldy, const void* x,
-                int64_t ldx, float* dW) {
+                int64_t ldx, float* dW, cudaStream_t s) {
         GemmOperand A{dy, ldy, false}, B{x, ldx, false};
         const int M = m->M;
         const double flops = 2.0 * n_out * k_in * (double)M;
         const double bytes = m->act_bytes * (double)M * (n_out + k_in) + 8.0 * n_out * k_in;
         if (!m->use_bf16) {
             GemmEpi e{EPI_ACCUM_F32, nullptr, dW, k_in, nullptr, 0, nullptr, 0};
-            RUN(m, site, 1, flops, bytes, k::gemm_f32(n_out, k_in, M, A, B, e, m->stream));
+            RUN(m, site, 1, flops, bytes, k::gemm_f32(n_out, k_in, M, A, B, e, s));
             return GPT2_OK;
         }
         const int bn = (k_in % 256 == 0 || k_in > 2048) ? 256 : 128;
@@ -484,16 +491,35 @@ struct Op {
             int kpb = (kblocks + splits - 1) / splits;
             int eff = (kblocks + kpb - 1) / kpb;
             RUN(m, site, 1, flops, bytes - 8.0 * n_out * k_in + 4.0 * eff * n_out * k_in,
-                k::gemm_bf16_tc(n_out, k_in, M, A, B, e, splits, m->st, m->stream));
+                k::gemm_bf16_tc(n_out, k_in, M, A, B, e, splits, m->st, s));
             RUN(m, "splitk_reduce", 1, 0.0, 4.0 * (eff + 2) * n_out * (double)k_in,
-                k::splitk_reduce_add(m->splitk_ws, eff, (int64_t)n_out * k_in, dW, m->stream));
+                k::splitk_reduce_add(m->splitk_ws, eff, (int64_t)n_out * k_in, dW, s));
             return GPT2_OK;
         }
         GemmEpi e{EPI_ACCUM_F32, nullptr, dW, k_in, nullptr, 0, nullptr, 0};
-        RUN(m, site, 1, flops, bytes, k::gemm_bf16_tc(n_out, k_in, M, A, B, e, 1, m->st, m->stream));
+        RUN(m, site, 1, flops, bytes, k::gemm_bf16_tc(n_out, k_in, M, A, B, e, 1, m->st, s));
         return GPT2_OK;
     }
 };
+
+// Cross-stream ordering: mark() records an event on `s` (the work enqueued
+// there so far); after(s, e) makes later work on `s` wait for it. Events come
+// from a pool that each backward pass reuses from the start: a wait binds to
+// the record that precedes it, so re-recording later does not disturb it.
+static int xmark(gpt2_model* m, cudaStream_t s, cudaEvent_t* out) {
+    if (m->xev_next == (int)m->xev.size()) {
+        cudaEvent_t e;
+        CK(m, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        m->xev.push_back(e);
+    }
+    *out = m->xev[m->xev_next++];
+    CK(m, cudaEventRecord(*out, s));
+    return GPT2_OK;
+}
+static int xafter(gpt2_model* m, cudaStream_t s, cudaEvent_t e) {
+    if (e) CK(m, cudaStreamWaitEvent(s, e, 0));
+    return GPT2_OK;
+}
 
 #define OPR(expr)                 \
     do {                          \
@@ -588,11 +614,31 @@ static int backward_impl(gpt2_model* m) {
     Op op{m};
     // LN backward: read du, x, read+write dres (first call writes only), write dres_act
     auto ln_bytes = [&](bool acc) { return MC * (A + 4 + (acc ? 8 : 4) + (m->use_bf16 ? A : 0)); };
+    // Weight-gradient work goes to the side stream (the main one when
+    // profiling, so that every site is timed alone). The main chain waits
+    // for the side only where a buffer the side still reads is overwritten:
+    // dres_act (read by the dW of the two residual projections), dh (dW and
+    // bias of fc), dqkv (dW and bias of the qkv projection).
+    const bool fork = m->side && !m->prof_on;
+    cudaStream_t s2 = fork ? m->side : s;
+    m->xev_next = 0;
+    cudaEvent_t ev = nullptr, dh_free = nullptr, dqkv_free = nullptr, dres_free = nullptr;
+    auto to_side = [&]() -> int {            // side waits for everything on main so far
+        if (!fork) return GPT2_OK;
+        OPR(xmark(m, s, &ev));
+        return xafter(m, s2, ev);
+    };
+    auto side_done = [&](cudaEvent_t* e) -> int {
+        if (!fork) return GPT2_OK;
+        return xmark(m, s2, e);
+    };
+    auto main_after = [&](cudaEvent_t e) -> int { return fork ? xafter(m, s, e) : GPT2_OK; };
     // LM head: du = dz wte ; dwte += dz^T uf
     {
         GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
+        OPR(to_side());
+        OPR(op.gemm_dw("gemm_lmhead_dw", Vp, C, m->logits, Vp, m->uf, C, m->G(0), s2));
         OPR(op.gemm("gemm_lmhead_dx", M, C, Vp, {m->logits, Vp, true}, {m->W(0), C, false}, e));
-        OPR(op.gemm_dw("gemm_lmhead_dw", Vp, C, m->logits, Vp, m->uf, C, m->G(0)));
     }
     // the new dres is the output gradient of the last MLP projection: its
     // column sums (that projection's bias gradient) come out of the same pass
@@ -605,19 +651,26 @@ static int backward_impl(gpt2_model* m) {
         // MLP projection: x_out = x_mid + hgel W_mp^T + b_mp
         {
             GemmEpi e{EPI_GELU_BWD, nullptr, m->dh, 4 * C, nullptr, 0, a.hpre, 4 * C};
+            OPR(to_side());
+            OPR(op.gemm_dw("gemm_mlpproj_dw", C, 4 * C, m->dres_act, C, a.hgel, 4 * C,
+                           m->G(m->lt(l, T_MPW)), s2));
+            OPR(side_done(&dres_free));
+            OPR(main_after(dh_free));
             OPR(op.gemm("gemm_mlpproj_dx", M, 4 * C, C, {m->dres_act, C, true},
                         {m->W(m->lt(l, T_MPW)), 4 * C, false}, e));
-            OPR(op.gemm_dw("gemm_mlpproj_dw", C, 4 * C, m->dres_act, C, a.hgel, 4 * C, m->G(m->lt(l, T_MPW))));
         }
         // fc: hpre = u2 W_fc^T + b_fc
         {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
-            OPR(op.gemm("gemm_fc_dx", M, C, 4 * C, {m->dh, 4 * C, true}, {m->W(m->lt(l, T_FCW)), C, false}, e));
-            OPR(op.gemm_dw("gemm_fc_dw", 4 * C, C, m->dh, 4 * C, a.u2, C, m->G(m->lt(l, T_FCW))));
+            OPR(to_side());
+            OPR(op.gemm_dw("gemm_fc_dw", 4 * C, C, m->dh, 4 * C, a.u2, C, m->G(m->lt(l, T_FCW)), s2));
             RUN(m, "bias_colsum", 2, 0, 4.0 * MC * A,
                 k::colsum_add<Act>((const Act*)m->dh, 4 * C, M, 4 * C, m->G(m->lt(l, T_FCB)),
-                                   m->cs_partial, s));
+                                   m->cs_partial, s2));
+            OPR(side_done(&dh_free));
+            OPR(op.gemm("gemm_fc_dx", M, C, 4 * C, {m->dh, 4 * C, true}, {m->W(m->lt(l, T_FCW)), C, false}, e));
         }
+        OPR(main_after(dres_free));
         RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
             k::layernorm_bwd<Act>((const Act*)m->du, a.x_mid, m->P(m->lt(l, T_LN2G)), a.mu2, a.rs2,
                                   m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN2G)),
@@ -626,9 +679,12 @@ static int backward_impl(gpt2_model* m) {
         // attention projection: x_mid = x_in + att W_ap^T + b_ap
         {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->datt, C, nullptr, 0, nullptr, 0};
+            OPR(to_side());
+            OPR(op.gemm_dw("gemm_attproj_dw", C, C, m->dres_act, C, a.att, C, m->G(m->lt(l, T_APW)), s2));
+            OPR(side_done(&dres_free));
             OPR(op.gemm("gemm_attproj_dx", M, C, C, {m->dres_act, C, true}, {m->W(m->lt(l, T_APW)), C, false}, e));
-            OPR(op.gemm_dw("gemm_attproj_dw", C, C, m->dres_act, C, a.att, C, m->G(m->lt(l, T_APW))));
         }
+        OPR(main_after(dqkv_free));
         if (m->use_bf16)
             RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
                 k::attention_bwd_bf16((const bf16*)a.qkv, (const bf16*)a.att, a.lse, (const bf16*)m->datt,
@@ -640,18 +696,26 @@ static int backward_impl(gpt2_model* m) {
         // qkv: qkv = u1 W_attn^T + b_attn
         {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
-            OPR(op.gemm("gemm_qkv_dx", M, C, 3 * C, {m->dqkv, 3 * C, true}, {m->W(m->lt(l, T_ATTW)), C, false}, e));
-            OPR(op.gemm_dw("gemm_qkv_dw", 3 * C, C, m->dqkv, 3 * C, a.u1, C, m->G(m->lt(l, T_ATTW))));
+            OPR(to_side());
+            OPR(op.gemm_dw("gemm_qkv_dw", 3 * C, C, m->dqkv, 3 * C, a.u1, C, m->G(m->lt(l, T_ATTW)), s2));
             RUN(m, "bias_colsum", 2, 0, 3.0 * MC * A,
                 k::colsum_add<Act>((const Act*)m->dqkv, 3 * C, M, 3 * C, m->G(m->lt(l, T_ATTB)),
-                                   m->cs_partial, s));
+                                   m->cs_partial, s2));
+            OPR(side_done(&dqkv_free));
+            OPR(op.gemm("gemm_qkv_dx", M, C, 3 * C, {m->dqkv, 3 * C, true}, {m->W(m->lt(l, T_ATTW)), C, false}, e));
         }
+        OPR(main_after(dres_free));
         RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
             k::layernorm_bwd<Act>((const Act*)m->du, a.x_in, m->P(m->lt(l, T_LN1G)), a.mu1, a.rs1,
                                   m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN1G)),
                                   m->G(m->lt(l, T_LN1B)),
                                   l > 0 ? m->G(m->lt(l - 1, T_MPB)) : nullptr, M, C,
                                   m->ln_partial, s));
+    }
+    // join: the tied embedding's gradient also receives the LM head's dW
+    if (fork) {
+        OPR(xmark(m, s2, &ev));
+        OPR(xafter(m, s, ev));
     }
     RUN(m, "embed_bwd", 4, 0, 4.0 * M + 8.0 * MC,
         k::embed_bwd(m->last_tok, m->dres, m->G(0), m->G(1), M, T, C, m->V, m->emb_ws, s));
@@ -704,6 +768,8 @@ void gpt2_destroy(gpt2_model* m) {
     if (!m) return;
     cudaDeviceSynchronize();
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    for (cudaEvent_t e : m->xev) cudaEventDestroy(e);
+    if (m->side) cudaStreamDestroy(m->side);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
 }

@@ -100,7 +100,11 @@ int gpt2_create(const gpt2_config* cfg, uint64_t seed, gpt2_model** out);
 void gpt2_destroy(gpt2_model* model);
 
 /* Enqueue all later work on cuda_stream (a cudaStream_t; NULL = legacy
- * default stream). The caller keeps ownership of the stream. */
+ * default stream). The caller keeps ownership of the stream. Inside
+ * gpt2_backward the weight-gradient work (dW GEMMs, bias gradients) runs on a
+ * second stream that the library owns; it is forked from and joined back to
+ * this stream by events before gpt2_backward returns, so the caller sees one
+ * ordered stream (and a stream capture records both branches). */
 int gpt2_set_stream(gpt2_model* model, void* cuda_stream);
 
 /*
@@ -208,7 +212,8 @@ const char* gpt2_last_error(const gpt2_model* model);
  * operands and results must move at least once. With profiling on, CUDA events
  * are also recorded on the model's stream around each site and their elapsed
  * times summed (adds one event pair per site; for measurement, not the timed
- * training loop).
+ * training loop). While event timing is on, the backward's weight-gradient
+ * work stays on the model's stream so that every site is timed alone.
  *   gpt2_profile(model, on): fold pending timings, clear every entry, set
  *     event timing on/off. Counting is always on.
  *   gpt2_profile_count: synchronise, fold pending timings, return the number
