@@ -686,7 +686,7 @@ static int backward_impl(gpt2_model* m) {
         }
         OPR(main_after(dqkv_free));
         if (m->use_bf16)
-            RUN(m, "attention_bwd", 3, attn_flops(m, 5), MC * A * 8,
+            RUN(m, "attention_bwd", 2, attn_flops(m, 5), MC * A * 8,
                 k::attention_bwd_bf16((const bf16*)a.qkv, (const bf16*)a.att, a.lse, (const bf16*)m->datt,
                                       (bf16*)m->dqkv, m->Dbuf, B, T, H, m->hs, m->st, s));
         else
@@ -1000,6 +1000,27 @@ int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kma
         e = GemmEpi{EPI_ACCUM_F32, nullptr, out_f32, ldd, nullptr, 0, nullptr, 0};
     } else {
         e = GemmEpi{EPI_STORE_F32, bias, out_f32, ldd, nullptr, 0, nullptr, 0};
+    }
+    GemmOperand a{A, lda, a_kmajor != 0}, b{B, ldb, b_kmajor != 0};
+    if (!k::gemm_bf16_tc_supported(M, N, K, a, b, e))
+        return fail(nullptr, GPT2_EINVAL, "unsupported GEMM shape/alignment");
+    DevState* st = op_state();
+    if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
+    cudaError_t r = k::gemm_bf16_tc(M, N, K, a, b, e, 1, st, (cudaStream_t)stream);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "gemm_bf16_tc", r);
+    return GPT2_OK;
+}
+
+int gpt2_op_gemm_bf16_gelu(int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
+                           const void* B, int64_t ldb, int b_kmajor, const float* bias,
+                           int backward, void* out, void* out2_or_aux, int64_t ldd, void* stream) {
+    if (!A || !B || !out || !out2_or_aux) return fail(nullptr, GPT2_EINVAL, "NULL operand");
+    GemmEpi e{};
+    if (backward) {
+        if (bias) return fail(nullptr, GPT2_EINVAL, "bias with the GELU backward epilogue");
+        e = GemmEpi{EPI_GELU_BWD, nullptr, out, ldd, nullptr, 0, out2_or_aux, ldd};
+    } else {
+        e = GemmEpi{EPI_GELU, bias, out, ldd, out2_or_aux, ldd, nullptr, 0};
     }
     GemmOperand a{A, lda, a_kmajor != 0}, b{B, ldb, b_kmajor != 0};
     if (!k::gemm_bf16_tc_supported(M, N, K, a, b, e))

@@ -15,7 +15,9 @@
 //               whose bandwidth the S and P V operand reads and the K/V
 //               copies already use up), rescales the O row in TMEM when the max grew
 //               by more than 2^8 (otherwise P may exceed 1 by up to 2^8, which
-//               the final division by the row sum absorbs exactly).
+//               the final division by the row sum absorbs exactly). The item's
+//               O / l leaves through a 4 KB shared-memory slab per warp and one
+//               TMA store (per-lane row stores cost 14% of the kernel).
 //   warp 4      TMA producer: Q once per item, then K and V of each block of
 //               128 keys into one slot of a three-slot ring.
 //   warp 5      allocates 512 TMEM columns (S double buffer, O double buffer,
@@ -46,7 +48,9 @@ constexpr int FW_THREADS = 224;                // forward: 4 softmax warps, prod
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
-constexpr int OFF_BAR = OFF_V + AT_SLOTS * AT_TILE;
+constexpr int OUT_SLAB = 32 * AT_HS * 2;       // one warp's 32 output rows, 4 KB
+constexpr int OFF_OUT = OFF_V + AT_SLOTS * AT_TILE;   // [4 softmax warps] O slabs
+constexpr int OFF_BAR = OFF_OUT + 4 * OUT_SLAB;
 constexpr size_t AT_SMEM = OFF_BAR + 256 + 1024;
 // forward TMEM columns: S[0] 0..127, S[1] 128..255, O[0] 256..319, O[1]
 // 320..383, P[0] 384..447, P[1] 448..511 (P: bf16 pairs, the A operand of P V)
@@ -67,6 +71,25 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
     const long long t0 = wait_clock();
     while (!mbar_try_wait(bar, parity) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
 }
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 family)
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// A warp's 32 rows x 64 columns of an output tile (fp32 accumulator values
+// times `scale`) as bf16 into a 128B-swizzled 4 KB slab: lane = row, 16-byte
+// piece q of row r at r*128 + ((q ^ (r & 7)) << 4), the layout the TMA store
+// of a 64 x 32 box expects.
+__device__ __forceinline__ void stage_out_slab(uint8_t* slab, int lane, const uint32_t (&a)[64], float scale) {
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        const float* f = (const float*)&a[8 * q];
+        *(uint4*)(slab + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(pack2_bf16(f[0] * scale, f[1] * scale), pack2_bf16(f[2] * scale, f[3] * scale),
+                       pack2_bf16(f[4] * scale, f[5] * scale), pack2_bf16(f[6] * scale, f[7] * scale));
+    }
+}
 
 }  // namespace
 
@@ -79,7 +102,7 @@ __device__ __forceinline__ void wait_bounded(uint64_t* bar, uint32_t parity) {
 // tensor-core work, one the S products and one the P V products, so that
 // neither chain of barrier waits delays the other.
 __global__ void __launch_bounds__(FW_THREADS, 1)
-fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ out,
+fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
                  float* __restrict__ lse, int T, int H, int BH, DevState* st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -231,6 +254,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
         const int r = threadIdx.x;
         const float sl2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
         const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
+        uint8_t* slab = smem + OFF_OUT + warp * OUT_SLAB;
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -264,7 +288,12 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
 #pragma unroll
                 for (int t = 0; t < 8; t++) pm[t] = __uint_as_float(sr[t]);
 #pragma unroll
-                for (int i = 8; i < 128; i++) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(sr[i]));
+                for (int i = 8; i < 120; i += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; t++)
+                        pm[t] = fmax3f(pm[t], __uint_as_float(sr[i + t]), __uint_as_float(sr[i + 8 + t]));
+#pragma unroll
+                for (int t = 0; t < 8; t++) pm[t] = fmaxf(pm[t], __uint_as_float(sr[120 + t]));
                 const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                        fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl2;
                 const float m_new = fmaxf(m_run, mx);
@@ -328,20 +357,23 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* __restrict__ 
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&o_free[ob]);
-            if (q < T) {
-                const float inv = 1.f / l_run;
-                uint4* orow = (uint4*)(out + ((int64_t)b * T + q) * C + h * AT_HS);
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const float* f = (const float*)&o[8 * c];
-                    orow[c] = make_uint4(pack2_bf16(f[0] * inv, f[1] * inv), pack2_bf16(f[2] * inv, f[3] * inv),
-                                         pack2_bf16(f[4] * inv, f[5] * inv), pack2_bf16(f[6] * inv, f[7] * inv));
-                }
-                lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
+            if (lane == 0) {
+                mbar_arrive(&o_free[ob]);
+                tma_wait_read<0>();             // the previous item's store has read the slab
             }
+            __syncwarp();
+            // O / l through this warp's slab and one TMA store (rows beyond T clipped)
+            stage_out_slab(slab, lane, o, 1.f / l_run);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&tm_out, slab, h * AT_HS, qb * AT_BQ + warp * 32, b);
+                tma_commit();
+            }
+            if (q < T) lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
             g += nkv;
         }
+        if (lane == 0) tma_wait_all();
     }
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) {
@@ -388,13 +420,29 @@ static bool make_qkv_map(CUtensorMap* map, const bf16* qkv, int B, int T, int C)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [B, T, width] bf16 tensor as the target of per-warp output stores: 3-D map
+// {width, T, B}, boxes of 64 x 32 x 1 with 128B swizzle (rows beyond T clipped).
+static bool make_rows_out_map(CUtensorMap* map, bf16* ptr, int B, int T, int width) {
+    EncodeTiledFnA enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)width * 2 * T};
+    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, int T, int H, int hs,
                                DevState* st, cudaStream_t s) {
     if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
     if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
-    CUtensorMap map;
+    CUtensorMap map, omap;
     memset(&map, 0, sizeof map);
-    if (!make_qkv_map(&map, qkv, B, T, H * hs)) return cudaErrorInvalidValue;
+    memset(&omap, 0, sizeof omap);
+    if (!make_qkv_map(&map, qkv, B, T, H * hs) || !make_rows_out_map(&omap, out, B, T, H * hs))
+        return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
         CUDA_OK(cudaFuncSetAttribute(fa_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -403,7 +451,7 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
-    fa_tc_fwd_kernel<<<grid, FW_THREADS, AT_SMEM, s>>>(map, out, lse, T, H, B * H, st);
+    fa_tc_fwd_kernel<<<grid, FW_THREADS, AT_SMEM, s>>>(map, omap, lse, T, H, B * H, st);
     return cudaGetLastError();
 }
 
@@ -425,7 +473,6 @@ namespace {
 constexpr int BW_THREADS = 352;                 // 8 softmax warps, producer, two MMA issuers
 constexpr int BW_PRODUCER = 8, BW_ISSUE_A = 9, BW_ISSUE_B = 10;
 constexpr int BW_SLOTS = 3;
-constexpr int OUT_SLAB = 32 * AT_HS * 2;          // one warp's 32 output rows, 4 KB
 // dK/dV kernel: K and V double buffered per item, Q and dO in a 3-slot ring,
 // per-warp staging of the dK and dV rows for their TMA stores
 constexpr int KV_OFF_K = 0;                                  // [2]
@@ -451,19 +498,6 @@ constexpr size_t DQ_SMEM = DQ_OFF_BAR + 256 + 1024;
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC = 256, TM_PT = 384, TM_DST = 448;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
-// A warp's 32 rows x 64 columns of an output tile (fp32 accumulator values
-// times `scale`) as bf16 into a 128B-swizzled 4 KB slab: lane = row, 16-byte
-// piece q of row r at r*128 + ((q ^ (r & 7)) << 4), the layout the TMA store
-// of a 64 x 32 box expects.
-__device__ __forceinline__ void stage_out_slab(uint8_t* slab, int lane, const uint32_t (&a)[64], float scale) {
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-        const float* f = (const float*)&a[8 * q];
-        *(uint4*)(slab + lane * 128 + ((q ^ (lane & 7)) << 4)) =
-            make_uint4(pack2_bf16(f[0] * scale, f[1] * scale), pack2_bf16(f[2] * scale, f[3] * scale),
-                       pack2_bf16(f[4] * scale, f[5] * scale), pack2_bf16(f[6] * scale, f[7] * scale));
-    }
-}
 
 }  // namespace
 

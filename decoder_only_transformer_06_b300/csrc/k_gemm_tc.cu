@@ -41,7 +41,6 @@ using namespace tc;
 static constexpr int TC_BM = 128, TC_BK = 64;
 static constexpr int EPI_WARPS = 8;
 static constexpr int TC_THREADS = 32 * (2 + EPI_WARPS);
-static constexpr int EPI_WARP_BYTES = 4096;                 // one 32x32 fp32 tile per warp
 
 // Grouped tile order: 16 m-tiles per group, m fastest inside a group, so a
 // wave of CTAs shares A and B tiles through L2.
@@ -68,12 +67,18 @@ __device__ __forceinline__ float tanh_hw(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// gelu(x) and gelu'(x) from one tanh
+// gelu(x) = 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), and
+// gelu'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) du/dx from one tanh, written as
+// ten fp32 operations (the epilogue of the fc Linear is bound by them).
 __device__ __forceinline__ void gelu_and_grad_hw(float x, float& g, float& dg) {
-    const float a = 0.7978845608028654f, c = 0.044715f;
-    const float t = tanh_hw(a * (x + c * x * x * x));
-    g = 0.5f * x * (1.0f + t);
-    dg = 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * a * (1.0f + 3.0f * c * x * x);
+    const float k0 = 0.7978845608028654f;              // sqrt(2/pi)
+    const float k1 = 0.7978845608028654f * 0.044715f;
+    const float x2 = x * x;
+    const float t = tanh_hw(x * fmaf(k1, x2, k0));
+    const float hx = 0.5f * x;
+    g = fmaf(hx, t, hx);
+    const float dudx = fmaf(3.0f * k1, x2, k0);
+    dg = fmaf(hx * fmaf(-t, t, 1.0f), dudx, fmaf(0.5f, t, 0.5f));
 }
 
 // Staging tiles are laid out as the TMA expects them with swizzling, which
@@ -120,16 +125,25 @@ __device__ __forceinline__ void unstage_bf16(const uint8_t* tile, int lane, floa
 // PAIR: the tile is 256 x BN and is shared by a cluster of two CTAs (one
 // tcgen05.mma with cta_group::2 covers both): each CTA stages its own 128 rows
 // of A and half (BN/2 rows) of B, and holds its own 128 x BN accumulator.
-template <int BN, bool PAIR>
+// The GELU epilogue (two outputs) gets 8 KB of staging per warp instead of 4 KB,
+// paid for by one operand stage: its GEMM has K = d_model, where five stages
+// still cover the copy latency. (The GELU-backward epilogue measured slower
+// with the same trade and a deeper prefetch of its extra operand, so it keeps
+// six stages and prefetches that operand one chunk ahead.)
+template <int BN, bool PAIR, int KIND>
 struct TcCfg {
+    static constexpr bool WIDE_EPI = (KIND == EPI_GELU);
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;
     static constexpr int B_BYTES = B_ROWS * TC_BK * 2;
-    static constexpr int STAGES = (A_BYTES + B_BYTES) == 32768 ? 6 : (BN == 256 ? 4 : 6);
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = STAGE_BYTES == 32768 ? (WIDE_EPI ? 5 : 6) : (WIDE_EPI ? 3 : 4);
     static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int EPI_WARP_BYTES = WIDE_EPI ? 8192 : 4096;
     static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 256;
+    static constexpr int AUX_RING = 1;            // GELU-derivative chunks in flight per warp
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + 512;
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // Tensor maps of the epilogue: o1 (bf16 out / fp32 out / fp32 reduce target /
@@ -143,7 +157,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ EpiMaps maps, int M, int N, int K, int splits,
                const float* __restrict__ bias, DevState* st) {
-    using Cfg = TcCfg<BN, PAIR>;
+    using Cfg = TcCfg<BN, PAIR, KIND>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -154,8 +168,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
-    uint64_t* auxbar = tempty + 2;              // [EPI_WARPS]
-    uint64_t* drain = auxbar + EPI_WARPS;
+    uint64_t* auxbar = tempty + 2;              // [EPI_WARPS][AUX_RING]
+    uint64_t* drain = auxbar + EPI_WARPS * Cfg::AUX_RING;
     uint32_t* tmem_slot = (uint32_t*)(drain + 1);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -173,7 +187,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
-        for (int i = 0; i < EPI_WARPS; i++) mbar_init(&auxbar[i], 1);
+        for (int i = 0; i < EPI_WARPS * Cfg::AUX_RING; i++) mbar_init(&auxbar[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -331,19 +345,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---------------- epilogue warps 2..9: TMEM lane quarter q4 = warp % 4
         // (the hardware's access rule), i.e. rows q4*32..q4*32+31 of the tile;
         // the two warps of a quarter take the left and right half of the columns.
-        // Each warp stages through its own 4 KB: a bf16 result in one 2 KB half
-        // (alternating halves for a single output, so that one TMA store can
-        // still be reading while the next chunk is written), the GELU outputs or
-        // the GELU derivative operand in both halves, an fp32 result in all 4 KB.
+        // Each warp stages through its own 4 KB (8 KB for GELU):
+        //   STORE_ACT  bf16 result in alternating 2 KB halves, so that one TMA
+        //              store can still be reading while the next chunk is written
+        //   GELU       gelu'(pre) and gelu(pre), 2 KB each, in alternating 4 KB sets
+        //   GELU_BWD   the bf16 result in 2 KB, then AUX_RING 2 KB slots of the
+        //              GELU derivative operand, loaded by TMA AUX_RING chunks
+        //              ahead (across tile boundaries)
+        //   fp32 kinds one 32x32 fp32 tile in all 4 KB
         const int ew = warp - 2;
         const int q4 = warp & 3;
         const int half = ew >> 2;
         constexpr int NCH = BN / 64;                 // 32-column chunks per warp per tile
-        constexpr bool ALT = (KIND == EPI_STORE_ACT);
-        uint8_t* wbuf = sEpi + ew * EPI_WARP_BYTES;
-        uint64_t* abar = auxbar + ew;
-        uint32_t aphase = 0u;
-        bool aux_inflight = false;
+        constexpr int NA = Cfg::AUX_RING;
+        constexpr bool ALT = (KIND == EPI_STORE_ACT || KIND == EPI_GELU);
+        constexpr uint32_t ALT_BYTES = KIND == EPI_GELU ? 4096u : 2048u;
+        uint8_t* wbuf = sEpi + ew * Cfg::EPI_WARP_BYTES;
+        uint8_t* aring = wbuf + 2048;
+        uint64_t* abar = auxbar + ew * NA;
+        const bool bias_vec = bias != nullptr && ((uintptr_t)bias & 15) == 0;
+        // The GELU derivative chunks of this warp, in the order the epilogue uses
+        // them (tile by tile, NCH chunks each), go into ring slot q % NA. The
+        // next chunk to load is chunk a_c of tile a_w, whose corner is (a_x, a_y).
+        long a_issued = 0, a_used = 0;
+        int a_w = unit, a_c = 0, a_x = 0, a_y = 0;
+        auto aux_tile = [&]() {
+            if (a_w >= total) return;
+            const int split = a_w / tiles;
+            int mt, nt;
+            tile_coords(a_w - split * tiles, num_m, num_n, mt, nt);
+            a_x = nt * BN + half * (BN / 2);
+            a_y = mt * TILE_M + (int)rank * TC_BM + q4 * 32;
+        };
+        auto issue_aux = [&]() {
+            if (a_w >= total) return;
+            const int slot = (int)(a_issued % NA);
+            mbar_arrive_expect_tx(&abar[slot], 2048);
+            tma_load_2d(aring + slot * 2048, &maps.aux, &abar[slot], a_x + 32 * a_c, a_y);
+            a_issued++;
+            if (++a_c == NCH) {
+                a_c = 0;
+                a_w += units;
+                aux_tile();
+            }
+        };
+        if (KIND == EPI_GELU_BWD && lane == 0) {
+            aux_tile();
+            for (int q = 0; q < NA; q++) issue_aux();
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t seq = 0;
@@ -355,25 +404,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tile_coords(w - split * tiles, num_m, num_n, mt, nt);
             const int m_base = mt * TILE_M + (int)rank * TC_BM + q4 * 32;
             const int n_half = nt * BN + half * (BN / 2);
-            // lane j holds bias[n_half + 32c + j] for chunk c; broadcast by shuffle
-            float bz[NCH];
-#pragma unroll
-            for (int c = 0; c < NCH; c++) {
-                const int n = n_half + 32 * c + lane;
-                bz[c] = (bias != nullptr && n < N) ? __ldg(bias + n) : 0.f;
-            }
-            if (KIND == EPI_GELU_BWD && lane == 0) {
-                mbar_arrive_expect_tx(abar, 2048);
-                tma_load_2d(wbuf + 2048, &maps.aux, abar, n_half, m_base);
-                aux_inflight = true;
-            }
             ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < NCH; c++, seq++) {
                 const int n0 = n_half + 32 * c;
-                uint8_t* sbuf = wbuf + (ALT ? (seq & 1) * 2048 : 0);
+                uint8_t* sbuf = wbuf + (ALT ? (seq & 1) * ALT_BYTES : 0);
+                // bias of columns n0..n0+31, the same for every lane (broadcast loads)
+                float bv[32];
+                if (bias != nullptr) {
+                    if (bias_vec && n0 + 32 <= N) {
+                        const float4* bp = (const float4*)(bias + n0);
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            const float4 t = __ldg(bp + q);
+                            bv[4 * q] = t.x;
+                            bv[4 * q + 1] = t.y;
+                            bv[4 * q + 2] = t.z;
+                            bv[4 * q + 3] = t.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) bv[j] = n0 + j < N ? __ldg(bias + n0 + j) : 0.f;
+                    }
+                }
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) +
                               (uint32_t)(acc * BN + half * (BN / 2) + c * 32), r);
@@ -387,29 +442,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 float v[32];
-                if (bias != nullptr) {
 #pragma unroll
-                    for (int j = 0; j < 32; j++)
-                        v[j] = __uint_as_float(r[j]) + __shfl_sync(0xffffffffu, bz[c], j);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
-                }
+                for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) + (bias != nullptr ? bv[j] : 0.f);
                 if (KIND == EPI_GELU_BWD) {
-                    ok = mbar_wait(abar, aphase, abort_flag);
+                    const long q = a_used;
+                    const int slot = (int)(q % NA);
+                    ok = mbar_wait(&abar[slot], (uint32_t)((q / NA) & 1), abort_flag);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    aphase ^= 1u;
-                    aux_inflight = false;
+                    a_used = q + 1;
                     float dg[32];
-                    unstage_bf16(wbuf + 2048, lane, dg);
+                    unstage_bf16(aring + slot * 2048, lane, dg);
 #pragma unroll
                     for (int j = 0; j < 32; j++) v[j] *= dg[j];
-                    __syncwarp();                        // every lane has read the operand
-                    if (lane == 0 && c + 1 < NCH) {      // prefetch the next chunk's operand
-                        mbar_arrive_expect_tx(abar, 2048);
-                        tma_load_2d(wbuf + 2048, &maps.aux, abar, n0 + 32, m_base);
-                        aux_inflight = true;
-                    }
+                    __syncwarp();                        // every lane has read the slot
+                    if (lane == 0) issue_aux();          // refill it NA chunks ahead
                 }
                 // the TMA store that last read this staging area is done
                 if (lane == 0) {
@@ -447,11 +493,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (lane == 0) {
             tma_wait_all();
-            // after an abort a prefetch of the GELU derivative may still be in
-            // flight: wait for it (bounded) before the CTA exits
-            if (KIND == EPI_GELU_BWD && aux_inflight) {
-                const long long t0 = wait_clock();
-                while (!mbar_try_wait(abar, aphase) && wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
+            // after an abort, prefetches of the GELU derivative may still be in
+            // flight: wait for them (bounded) before the CTA exits
+            if (KIND == EPI_GELU_BWD) {
+                for (long q = a_used; q < a_issued; q++) {
+                    const long long t0 = wait_clock();
+                    while (!mbar_try_wait(&abar[q % NA], (uint32_t)((q / NA) & 1)) &&
+                           wait_clock() - t0 < WAIT_LIMIT_CYCLES) {}
+                }
             }
         }
     }
@@ -569,7 +618,7 @@ static int max_pairs(Kern kern, size_t smem) {
 template <int BN, bool A_MN, bool B_MN, int KIND, bool PAIR>
 static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                              int splits, DevState* st, cudaStream_t s) {
-    using Cfg = TcCfg<BN, PAIR>;
+    using Cfg = TcCfg<BN, PAIR, KIND>;
     CUtensorMap ta, tb;
     bool ok = A_MN ? make_operand_map(&ta, A.ptr, (uint64_t)M, (uint64_t)K, A.ld, 64, 64)
                    : make_operand_map(&ta, A.ptr, (uint64_t)K, (uint64_t)M, A.ld, 64, TC_BM);

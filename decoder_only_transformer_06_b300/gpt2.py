@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_last_error": (ctypes.c_char_p, [P]),
         "gpt2_version": (ctypes.c_char_p, []),
         "gpt2_op_gemm_bf16": (I, [I, I, I, P, I64, I, P, I64, I, P, P, P, I64, I, P]),
+        "gpt2_op_gemm_bf16_gelu": (I, [I, I, I, P, I64, I, P, I64, I, P, I, P, P, I64, P]),
         "gpt2_op_sync": (I, [P]),
         "gpt2_op_attention_fwd": (I, [I, I, I, I, I, P, P, P, P]),
         "gpt2_op_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
@@ -294,6 +295,17 @@ def op_gemm_bf16(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, bias=None, out_bf1
     _check(_lib.gpt2_op_gemm_bf16(M, N, K, ptr(A), lda, int(a_kmajor), ptr(B), ldb, int(b_kmajor),
                                   ptr(bias), ptr(out_bf16), ptr(out_f32), ldd, int(accumulate),
                                   _stream_ptr(stream)))
+
+
+def op_gemm_bf16_gelu(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, out, out2_or_aux, bias=None,
+                      backward=False, ldd=None, stream=None):
+    """GELU epilogues: backward=False writes out = gelu'(A B^T + bias) and
+    out2_or_aux = gelu(A B^T + bias); backward=True writes out = (A B^T) * aux."""
+    ldd = N if ldd is None else ldd
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    _check(_lib.gpt2_op_gemm_bf16_gelu(M, N, K, ptr(A), lda, int(a_kmajor), ptr(B), ldb,
+                                       int(b_kmajor), ptr(bias), int(backward), ptr(out),
+                                       ptr(out2_or_aux), ldd, _stream_ptr(stream)))
 
 
 def op_sync(stream=None):

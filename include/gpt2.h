@@ -245,6 +245,24 @@ int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kma
                       void* out_bf16, float* out_f32, int64_t ldd, int accumulate,
                       void* stream);
 
+/* The two GELU epilogues of the MLP's GEMMs (nanoGPT guide Deep dive 1, the
+ * MLP block c_fc -> GELU(tanh) -> c_proj; "Let's reproduce GPT-2" on the tanh
+ * approximation), same operand conventions as gpt2_op_gemm_bf16, all outputs
+ * bf16 [M, N] with row stride ldd:
+ *   backward == 0: pre = A B^T + bias (bias fp32 [N] or NULL);
+ *                  out = gelu'(pre), out2_or_aux = gelu(pre)
+ *                  (the forward of c_fc, saving the derivative for the backward)
+ *   backward != 0: out = (A B^T) * aux with aux = out2_or_aux (bf16 [M, N], the
+ *                  saved gelu'(pre)); bias must be NULL
+ *                  (the input gradient of c_proj carried through the GELU)
+ * tanh is the hardware approximation (absolute error about 2^-11).
+ * EINVAL for NULL pointers, a bias with backward != 0, or shapes/alignments
+ * gpt2_op_gemm_bf16 rejects. */
+int gpt2_op_gemm_bf16_gelu(int M, int N, int K, const void* A, int64_t lda, int a_kmajor,
+                           const void* B, int64_t ldb, int b_kmajor, const float* bias,
+                           int backward, void* out, void* out2_or_aux, int64_t ldd,
+                           void* stream);
+
 /* Synchronise `stream` and report device-side conditions raised by the
  * op-level calls above since the previous gpt2_op_sync: GPT2_ETIMEOUT if a
  * bounded wait inside a kernel expired (the kernel then skipped its remaining

@@ -61,6 +61,58 @@ def test_gemm_bf16_bias_bf16_out_and_accumulate(ak, bk, N):
     assert np.abs(acc.cpu().double().numpy() - (ref + 1.0)).max() <= 4e-4 * math.sqrt(K)
 
 
+def _gelu_bound(pre, ref, deriv):
+    """Per-element bound for the GELU epilogues: bf16 rounding of the output
+    (2^-9 relative, 2^-8 allowed), fp32 accumulation of the products (K * 2^-24
+    relative to sum |a b|, below 1e-5 here) and the hardware tanh (absolute
+    error e = 2^-10.9 in t): gelu = 0.5 x (1 + t) moves by 0.5 |x| e, and
+    gelu' = 0.5 (1 + t) + 0.5 x (1 - t^2) u' by 0.5 e + |x| |t| e u', with
+    u' = sqrt(2/pi) (1 + 3 * 0.044715 x^2)."""
+    e = 2.0 ** -10.9
+    hx = 0.5 * np.abs(pre)
+    if deriv:
+        up = 0.7978845608028654 * (1.0 + 3.0 * 0.044715 * pre * pre)
+        t = np.tanh(0.7978845608028654 * (pre + 0.044715 * pre ** 3))
+        ta = 0.5 * e + 2.0 * hx * np.abs(t) * e * up
+    else:
+        ta = hx * e
+    return 2.0 ** -8 * np.abs(ref) + ta + 1e-5
+
+
+# N = 768 runs on CTA pairs, N = 384 on single CTAs; M = 320 leaves the last
+# tile partly empty; K-major and MN-major B (the forward and the dX layouts)
+@pytest.mark.parametrize("N", [384, 768])
+@pytest.mark.parametrize("bk", [1, 0])
+def test_gemm_gelu_epilogues(N, bk):
+    M, K = 320, 256
+    g = torch.Generator().manual_seed(N + bk)
+    A = torch.randn(M, K, generator=g, dtype=torch.float32).bfloat16()
+    # weights of std 0.1 keep pre-activations around N(0, 1.6^2): the range
+    # where GELU bends
+    Bw = (0.1 * torch.randn(N, K, generator=g, dtype=torch.float32)).bfloat16()
+    bias = (0.5 * torch.randn(N, generator=g, dtype=torch.float32))
+    b_mem = Bw if bk else Bw.t().contiguous()
+    ldb = K if bk else N
+    pre = A.double().numpy() @ Bw.double().numpy().T
+    # forward: out = gelu'(pre + bias), out2 = gelu(pre + bias)
+    d = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    h = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gpt2.op_gemm_bf16_gelu(M, N, K, A.cuda(), K, 1, b_mem.cuda(), ldb, bk, d, h, bias=bias.cuda())
+    # backward: out = pre * aux, with an arbitrary bf16 aux
+    aux = torch.randn(M, N, generator=g, dtype=torch.float32).bfloat16()
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gpt2.op_gemm_bf16_gelu(M, N, K, A.cuda(), K, 1, b_mem.cuda(), ldb, bk, y, aux.cuda(), backward=True)
+    gpt2.op_sync()
+    x = pre + bias.double().numpy()[None, :]
+    ref_h, ref_d = O.gelu_tanh(x), O.gelu_tanh_grad(x)
+    got_h, got_d = h.cpu().double().numpy(), d.cpu().double().numpy()
+    assert np.all(np.abs(got_h - ref_h) <= _gelu_bound(x, ref_h, False)), (N, bk)
+    assert np.all(np.abs(got_d - ref_d) <= _gelu_bound(x, ref_d, True)), (N, bk)
+    ref_y = pre * aux.double().numpy()
+    got_y = y.cpu().double().numpy()
+    assert np.all(np.abs(got_y - ref_y) <= 2.0 ** -8 * np.abs(ref_y) + 1e-5 * np.abs(aux.double().numpy()) * math.sqrt(K)), (N, bk)
+
+
 def _attn_inputs(B, T, H, hs, seed, dtype):
     g = torch.Generator().manual_seed(seed)
     qkv = torch.randn(B * T, 3 * H * hs, generator=g, dtype=torch.float32)
