@@ -347,7 +347,8 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     ALLOC(m, m->yproj, M * C * A);
     ALLOC(m, m->dh, M * 4 * C * A);
     ALLOC(m, m->Dbuf, M * m->H * 4);
-    ALLOC(m, m->ln_partial, k::layernorm_bwd_partial_floats(m->M, m->C) * 4);
+    // two buffers: the side stream reduces one while the next row pass fills the other
+    ALLOC(m, m->ln_partial, 2 * k::layernorm_bwd_partial_floats(m->M, m->C) * 4);
     size_t cs = k::colsum_partial_floats(m->M, 4 * m->C);
     ALLOC(m, m->cs_partial, cs * 4);
     ALLOC(m, m->emb_ws, k::embed_bwd_workspace(m->M, m->C));
@@ -633,19 +634,38 @@ static int backward_impl(gpt2_model* m) {
         return xmark(m, s2, e);
     };
     auto main_after = [&](cudaEvent_t e) -> int { return fork ? xafter(m, s, e) : GPT2_OK; };
-    // LM head: du = dz wte ; dwte += dz^T uf
+    // LayerNorm backward: the row pass on the main chain; the reduction of its
+    // per-block partials into dgamma, dbeta and the preceding projection's bias
+    // gradient on the side, from one of two alternating partials buffers
+    const size_t ln_pf = k::layernorm_bwd_partial_floats(M, C);
+    cudaEvent_t ln_free[2] = {nullptr, nullptr};
+    int ln_iter = 0;
+    auto ln_bwd = [&](const float* x, int gi, const float* mu, const float* rs, bool acc,
+                      float* dsum) -> int {
+        float* part = m->ln_partial + (size_t)(ln_iter & 1) * ln_pf;
+        OPR(main_after(ln_free[ln_iter & 1]));
+        RUN(m, "layernorm_bwd", 1, 0, ln_bytes(acc),
+            k::layernorm_bwd_rows<Act>((const Act*)m->du, x, m->P(gi), mu, rs, m->dres, (Act*)m->dres_act,
+                                       acc, dsum != nullptr, M, C, part, s));
+        OPR(to_side());
+        RUN(m, "ln_param_reduce", 1, 0, 4.0 * ln_pf + 12.0 * C,
+            k::layernorm_bwd_params(part, M, C, m->G(gi), m->G(gi + 1), dsum, s2));
+        OPR(side_done(&ln_free[ln_iter & 1]));
+        ln_iter++;
+        return GPT2_OK;
+    };
+    // LM head: du = dz wte ; dwte += dz^T uf. The side also sorts the token ids
+    // for the embedding backward (they depend on nothing else).
     {
         GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
         OPR(to_side());
+        RUN(m, "embed_bwd", 1, 0, 8.0 * M, k::embed_bwd_sort(m->last_tok, M, m->V, m->emb_ws, s2));
         OPR(op.gemm_dw("gemm_lmhead_dw", Vp, C, m->logits, Vp, m->uf, C, m->G(0), s2));
         OPR(op.gemm("gemm_lmhead_dx", M, C, Vp, {m->logits, Vp, true}, {m->W(0), C, false}, e));
     }
     // the new dres is the output gradient of the last MLP projection: its
     // column sums (that projection's bias gradient) come out of the same pass
-    RUN(m, "layernorm_bwd", 2, 0, ln_bytes(false),
-        k::layernorm_bwd<Act>((const Act*)m->du, m->x_final, m->P(m->lnf_g()), m->muf, m->rsf, m->dres,
-                              (Act*)m->dres_act, false, m->G(m->lnf_g()), m->G(m->lnf_g() + 1),
-                              m->G(m->lt(L - 1, T_MPB)), M, C, m->ln_partial, s));
+    OPR(ln_bwd(m->x_final, m->lnf_g(), m->muf, m->rsf, false, m->G(m->lt(L - 1, T_MPB))));
     for (int l = L - 1; l >= 0; l--) {
         LayerActs& a = m->la[l];
         // MLP projection: x_out = x_mid + hgel W_mp^T + b_mp
@@ -671,11 +691,7 @@ static int backward_impl(gpt2_model* m) {
             OPR(op.gemm("gemm_fc_dx", M, C, 4 * C, {m->dh, 4 * C, true}, {m->W(m->lt(l, T_FCW)), C, false}, e));
         }
         OPR(main_after(dres_free));
-        RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
-            k::layernorm_bwd<Act>((const Act*)m->du, a.x_mid, m->P(m->lt(l, T_LN2G)), a.mu2, a.rs2,
-                                  m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN2G)),
-                                  m->G(m->lt(l, T_LN2B)), m->G(m->lt(l, T_APB)), M, C,
-                                  m->ln_partial, s));
+        OPR(ln_bwd(a.x_mid, m->lt(l, T_LN2G), a.mu2, a.rs2, true, m->G(m->lt(l, T_APB))));
         // attention projection: x_mid = x_in + att W_ap^T + b_ap
         {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->datt, C, nullptr, 0, nullptr, 0};
@@ -705,20 +721,16 @@ static int backward_impl(gpt2_model* m) {
             OPR(op.gemm("gemm_qkv_dx", M, C, 3 * C, {m->dqkv, 3 * C, true}, {m->W(m->lt(l, T_ATTW)), C, false}, e));
         }
         OPR(main_after(dres_free));
-        RUN(m, "layernorm_bwd", 2, 0, ln_bytes(true),
-            k::layernorm_bwd<Act>((const Act*)m->du, a.x_in, m->P(m->lt(l, T_LN1G)), a.mu1, a.rs1,
-                                  m->dres, (Act*)m->dres_act, true, m->G(m->lt(l, T_LN1G)),
-                                  m->G(m->lt(l, T_LN1B)),
-                                  l > 0 ? m->G(m->lt(l - 1, T_MPB)) : nullptr, M, C,
-                                  m->ln_partial, s));
+        OPR(ln_bwd(a.x_in, m->lt(l, T_LN1G), a.mu1, a.rs1, true,
+                   l > 0 ? m->G(m->lt(l - 1, T_MPB)) : nullptr));
     }
     // join: the tied embedding's gradient also receives the LM head's dW
     if (fork) {
         OPR(xmark(m, s2, &ev));
         OPR(xafter(m, s, ev));
     }
-    RUN(m, "embed_bwd", 4, 0, 4.0 * M + 8.0 * MC,
-        k::embed_bwd(m->last_tok, m->dres, m->G(0), m->G(1), M, T, C, m->V, m->emb_ws, s));
+    RUN(m, "embed_bwd", 3, 0, 8.0 * MC,
+        k::embed_bwd_apply(m->dres, m->G(0), m->G(1), M, T, C, m->emb_ws, s));
     return GPT2_OK;
 }
 

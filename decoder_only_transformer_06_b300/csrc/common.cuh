@@ -115,6 +115,11 @@ cudaError_t embed_fwd(const int32_t* tok, const float* wte, const float* wpe, fl
 size_t embed_bwd_workspace(int M, int C);
 cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
                       int C, int V, void* workspace, cudaStream_t s);
+// embed_bwd in its two parts: the sort of the token ids (depends on the tokens
+// only) and the segmented sums of dx rows that use it.
+cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cudaStream_t s);
+cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, int T, int C,
+                            void* workspace, cudaStream_t s);
 
 // u = LN(x') with x' = x, or x' = x + y written to x_out when y != nullptr
 // (the residual add of the preceding branch fused into the LayerNorm).
@@ -131,6 +136,16 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
                           const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
                           float* db, float* dsum, int M, int C, float* partial, cudaStream_t s);
 size_t layernorm_bwd_partial_floats(int M, int C);
+// layernorm_bwd in its two parts: the row pass (dres, dres_act, and the
+// per-block partials of dg, db and, with want_dsum, dsum into `partial`), and
+// the fixed-order reduction of those partials (which may run on another stream
+// once the row pass is done).
+template <typename Act>
+cudaError_t layernorm_bwd_rows(const Act* du, const float* x, const float* g, const float* mu,
+                               const float* rstd, float* dres, Act* dres_act, bool accumulate,
+                               bool want_dsum, int M, int C, float* partial, cudaStream_t s);
+cudaError_t layernorm_bwd_params(const float* partial, int M, int C, float* dg, float* db, float* dsum,
+                                 cudaStream_t s);
 
 // db[n] += sum_m dy[m, n]; fixed-order two-stage reduction.
 template <typename T>

@@ -370,14 +370,20 @@ cudaError_t layernorm_fwd(const float* x, const Act* y, float* x_out, const floa
     return cudaErrorInvalidValue;
 }
 
+cudaError_t layernorm_bwd_params(const float* partial, int M, int C, float* dg, float* db, float* dsum,
+                                 cudaStream_t s) {
+    ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, ln_bwd_blocks(M), C, dg, db, dsum);
+    return cudaGetLastError();
+}
+
 template <typename Act>
-cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const float* mu,
-                          const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
-                          float* db, float* dsum, int M, int C, float* partial, cudaStream_t s) {
+cudaError_t layernorm_bwd_rows(const Act* du, const float* x, const float* g, const float* mu,
+                               const float* rstd, float* dres, Act* dres_act, bool accumulate,
+                               bool want_dsum, int M, int C, float* partial, cudaStream_t s) {
     int epl = (C + 31) / 32;
     int blocks = ln_bwd_blocks(M);
     size_t smem = (size_t)LN_WARPS * 3 * C * sizeof(float);
-    const int want_sum = dsum ? 1 : 0;
+    const int want_sum = want_dsum ? 1 : 0;
     cudaError_t e = cudaErrorInvalidValue;
     if (C % 128 == 0 && C <= 1024) {
         switch (C / 128) {
@@ -393,9 +399,7 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
             LBV(1) LBV(2) LBV(3) LBV(4) LBV(5) LBV(6) LBV(7) LBV(8)
 #undef LBV
         }
-        if (e != cudaSuccess) return e;
-        ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, blocks, C, dg, db, dsum);
-        return cudaGetLastError();
+        return e;
     }
 #define LNB(E)                                                                                  \
     do {                                                                                        \
@@ -415,9 +419,17 @@ cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const f
     else if (epl <= 48) LNB(48);
     else if (epl <= 64) LNB(64);
 #undef LNB
+    return e;
+}
+
+template <typename Act>
+cudaError_t layernorm_bwd(const Act* du, const float* x, const float* g, const float* mu,
+                          const float* rstd, float* dres, Act* dres_act, bool accumulate, float* dg,
+                          float* db, float* dsum, int M, int C, float* partial, cudaStream_t s) {
+    cudaError_t e = layernorm_bwd_rows<Act>(du, x, g, mu, rstd, dres, dres_act, accumulate,
+                                            dsum != nullptr, M, C, partial, s);
     if (e != cudaSuccess) return e;
-    ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, blocks, C, dg, db, dsum);
-    return cudaGetLastError();
+    return layernorm_bwd_params(partial, M, C, dg, db, dsum, s);
 }
 
 template cudaError_t layernorm_fwd<float>(const float*, const float*, float*, const float*,
@@ -426,6 +438,12 @@ template cudaError_t layernorm_fwd<float>(const float*, const float*, float*, co
 template cudaError_t layernorm_fwd<bf16>(const float*, const bf16*, float*, const float*,
                                          const float*, bf16*, float*, float*, int, int,
                                          cudaStream_t);
+template cudaError_t layernorm_bwd_rows<float>(const float*, const float*, const float*, const float*,
+                                               const float*, float*, float*, bool, bool, int, int,
+                                               float*, cudaStream_t);
+template cudaError_t layernorm_bwd_rows<bf16>(const bf16*, const float*, const float*, const float*,
+                                              const float*, float*, bf16*, bool, bool, int, int,
+                                              float*, cudaStream_t);
 template cudaError_t layernorm_bwd<float>(const float*, const float*, const float*, const float*,
                                           const float*, float*, float*, bool, float*, float*,
                                           float*, int, int, float*, cudaStream_t);

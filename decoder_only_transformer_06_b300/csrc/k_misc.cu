@@ -204,17 +204,28 @@ size_t embed_bwd_workspace(int M, int C) {
     return (size_t)2 * M * sizeof(int) + (size_t)M * C * sizeof(float) + 256;
 }
 
-cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
-                      int C, int V, void* workspace, cudaStream_t s) {
+cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cudaStream_t s) {
     int* s_tok = (int*)workspace;
     int* s_pos = s_tok + M;
-    float* carry = (float*)(((uintptr_t)(s_pos + M) + 255) & ~(uintptr_t)255);
     int P2 = pow2_at_least(M);
     size_t smem = (size_t)P2 * sizeof(uint32_t);
     CUDA_OK(cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem));
     embed_sort_kernel<<<1, 1024, smem, s>>>(tok, M, V, P2, s_tok, s_pos);
-    CUDA_OK(cudaGetLastError());
+    return cudaGetLastError();
+}
+
+cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
+                      int C, int V, void* workspace, cudaStream_t s) {
+    CUDA_OK(embed_bwd_sort(tok, M, V, workspace, s));
+    return embed_bwd_apply(dx, dwte, dwpe, M, T, C, workspace, s);
+}
+
+cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, int T, int C,
+                            void* workspace, cudaStream_t s) {
+    int* s_tok = (int*)workspace;
+    int* s_pos = s_tok + M;
+    float* carry = (float*)(((uintptr_t)(s_pos + M) + 255) & ~(uintptr_t)255);
     int C4 = C / 4;
     int chunks = (M + EMB_R - 1) / EMB_R;
     embed_chunk_kernel<<<chunks, C4, 0, s>>>(s_tok, s_pos, (const float4*)dx, (float4*)dwte,
