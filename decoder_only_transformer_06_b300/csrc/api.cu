@@ -3,6 +3,7 @@
 #include "gpt2.h"
 #include "common.cuh"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -61,6 +62,14 @@ struct gpt2_model {
     cudaStream_t side = nullptr;
     std::vector<cudaEvent_t> xev;
     int xev_next = 0;
+    // AdamW also runs on the side stream, in groups in the order the next
+    // forward reads the parameters (embeddings, layer 0..L-1, final
+    // LayerNorm); upd_ev[g] marks group g done. While upd_pending, the next
+    // forward waits for each group just before it uses it, and every other
+    // entry point first joins the side stream.
+    std::vector<cudaEvent_t> upd_ev;
+    bool upd_pending = false;
+    std::vector<std::vector<std::pair<int64_t, int64_t>>> upd_runs;   // [group] arena [begin, end)
 
     std::vector<TensorRec> tensors;
     int64_t n_arena = 0, decay_end = 0;
@@ -304,6 +313,27 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     m->tensors = p.t;
     m->n_arena = p.n_arena;
     m->decay_end = p.decay_end;
+    {
+        // AdamW groups in the order the forward reads them: 0 = wte, wpe;
+        // 1 + l = layer l; L + 1 = final LayerNorm. Each tensor's run extends to
+        // the next tensor's offset (covering its alignment padding); adjacent
+        // runs of one group merge.
+        const int G = m->L + 2;
+        m->upd_runs.assign(G, {});
+        std::vector<int> order(m->tensors.size());
+        for (size_t i = 0; i < order.size(); i++) order[i] = (int)i;
+        std::sort(order.begin(), order.end(),
+                  [&](int a, int b) { return m->tensors[a].offset < m->tensors[b].offset; });
+        for (size_t k = 0; k < order.size(); k++) {
+            const int i = order[k];
+            const int g = i < 2 ? 0 : (i < 2 + m->L * T_PER_LAYER ? 1 + (i - 2) / T_PER_LAYER : m->L + 1);
+            const int64_t b = m->tensors[i].offset;
+            const int64_t e = k + 1 < order.size() ? m->tensors[order[k + 1]].offset : m->n_arena;
+            auto& runs = m->upd_runs[g];
+            if (!runs.empty() && runs.back().second == b) runs.back().second = e;
+            else runs.push_back({b, e});
+        }
+    }
 
     const size_t nb = (size_t)m->n_arena * sizeof(float);
     ALLOC(m, m->params, nb);
@@ -521,6 +551,19 @@ static int xafter(gpt2_model* m, cudaStream_t s, cudaEvent_t e) {
     if (e) CK(m, cudaStreamWaitEvent(s, e, 0));
     return GPT2_OK;
 }
+// The model's stream waits for everything enqueued on the side stream.
+static int join_side(gpt2_model* m) {
+    if (!m->upd_pending) return GPT2_OK;
+    m->upd_pending = false;
+    cudaEvent_t e;
+    int r = xmark(m, m->side, &e);
+    if (r) return r;
+    return xafter(m, m->stream, e);
+}
+// Before the forward reads parameter group g: wait for its AdamW update.
+static int param_wait(gpt2_model* m, int g) {
+    return m->upd_pending ? xafter(m, m->stream, m->upd_ev[g]) : GPT2_OK;
+}
 
 #define OPR(expr)                 \
     do {                          \
@@ -543,11 +586,13 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
     const double A = m->act_bytes, MC = (double)M * C;
     Op op{m};
     RUN(m, "validate", 1, 0, 8.0 * M, k::validate_inputs(tok, tgt, M, m->V, m->st, m->accum, s));
+    OPR(param_wait(m, 0));
     RUN(m, "embed_fwd", 1, 0, 4.0 * M + 12.0 * MC,
         k::embed_fwd(tok, m->P(0), m->P(1), m->la[0].x_in, M, T, C, m->V, s));
     // LayerNorm: read x, write u, mu, rstd; fused residual add: also read y, write x
     const double ln_bytes = MC * (4 + A) + 8.0 * M;
     const double add_ln_bytes = ln_bytes + MC * (A + 4);
+    OPR(param_wait(m, 1));
     RUN(m, "layernorm_fwd", 1, 0, ln_bytes,
         k::layernorm_fwd<Act>(m->la[0].x_in, nullptr, nullptr, m->P(m->lt(0, T_LN1G)),
                               m->P(m->lt(0, T_LN1B)), (Act*)m->la[0].u1, m->la[0].mu1, m->la[0].rs1,
@@ -585,11 +630,14 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
         }
         if (l + 1 < L) {
             LayerActs& n = m->la[l + 1];
+            OPR(param_wait(m, l + 2));
             RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
                 k::layernorm_fwd<Act>(a.x_mid, (const Act*)m->yproj, n.x_in, m->P(m->lt(l + 1, T_LN1G)),
                                       m->P(m->lt(l + 1, T_LN1B)), (Act*)n.u1, n.mu1, n.rs1, M, C, s));
         }
     }
+    OPR(param_wait(m, L + 1));
+    m->upd_pending = false;      // every group has been waited for
     RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
         k::layernorm_fwd<Act>(m->la[L - 1].x_mid, (const Act*)m->yproj, m->x_final, m->P(m->lnf_g()),
                               m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf, m->rsf, M, C, s));
@@ -781,6 +829,7 @@ void gpt2_destroy(gpt2_model* m) {
     cudaDeviceSynchronize();
     for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
     for (cudaEvent_t e : m->xev) cudaEventDestroy(e);
+    for (cudaEvent_t e : m->upd_ev) cudaEventDestroy(e);
     if (m->side) cudaStreamDestroy(m->side);
     for (void* p : m->allocs) cudaFree(p);
     delete m;
@@ -788,6 +837,8 @@ void gpt2_destroy(gpt2_model* m) {
 
 int gpt2_set_stream(gpt2_model* m, void* stream) {
     if (!m) return GPT2_EINVAL;
+    int r = join_side(m);
+    if (r) return r;
     m->stream = (cudaStream_t)stream;
     return GPT2_OK;
 }
@@ -809,6 +860,10 @@ int gpt2_forward(gpt2_model* m, const int32_t* tok, const int32_t* tgt, float* h
 
 int gpt2_backward(gpt2_model* m) {
     if (!m) return GPT2_EINVAL;
+    {
+        int r = join_side(m);
+        if (r) return r;
+    }
     if (!m->have_targets) return fail(m, GPT2_ESTATE, "backward needs a forward with targets");
     m->have_targets = false;   // the logits buffer now holds consumed gradients
     return m->use_bf16 ? backward_impl<bf16>(m) : backward_impl<float>(m);
@@ -817,15 +872,48 @@ int gpt2_backward(gpt2_model* m) {
 int gpt2_step(gpt2_model* m, float lr, float beta1, float beta2, float eps, float weight_decay,
               float clip, float* h_grad_norm) {
     if (!m) return GPT2_EINVAL;
+    {
+        int r = join_side(m);
+        if (r) return r;
+    }
     cudaStream_t s = m->stream;
     const double n = (double)m->n_arena;
     RUN(m, "grad_norm", 1, 0, 4.0 * n,
         k::grad_norm(m->grads, m->n_arena, m->norm_partial, m->norm_parts, s));
     RUN(m, "step_finalize", 1, 0, 8.0 * m->norm_parts,
         k::step_finalize(m->norm_partial, m->norm_parts, clip, beta1, beta2, m->st, s));
-    RUN(m, "adamw", 1, 0, 28.0 * n + (m->use_bf16 ? 2.0 * m->decay_end : 0.0),
-        k::adamw(m->params, m->grads, m->adam_m, m->adam_v, m->pbf, m->n_arena, m->decay_end,
-                 m->decay_end, lr, beta1, beta2, eps, weight_decay, m->st, s));
+    bf16* pbf = m->use_bf16 ? m->pbf : nullptr;
+    if (!m->side || m->prof_on) {
+        RUN(m, "adamw", 1, 0, 28.0 * n + (m->use_bf16 ? 2.0 * m->decay_end : 0.0),
+            k::adamw(m->params, m->grads, m->adam_m, m->adam_v, pbf, m->n_arena, m->decay_end,
+                     m->decay_end, lr, beta1, beta2, eps, weight_decay, m->st, s));
+    } else {
+        // on the side stream, group by group (update_groups: contiguous arena
+        // runs of the embeddings, each layer, the final LayerNorm)
+        cudaEvent_t e;
+        int r = xmark(m, s, &e);
+        if (r) return r;
+        r = xafter(m, m->side, e);
+        if (r) return r;
+        const int G = m->L + 2;
+        while ((int)m->upd_ev.size() < G) {
+            cudaEvent_t u;
+            CK(m, cudaEventCreateWithFlags(&u, cudaEventDisableTiming));
+            m->upd_ev.push_back(u);
+        }
+        for (int g = 0; g < G; g++) {
+            for (const auto& run : m->upd_runs[g]) {
+                const int64_t a = run.first, cnt = run.second - run.first;
+                const int64_t dend = std::max<int64_t>(0, std::min<int64_t>(cnt, m->decay_end - a));
+                RUN(m, "adamw", 1, 0, 28.0 * cnt + (m->use_bf16 ? 2.0 * dend : 0.0),
+                    k::adamw(m->params + a, m->grads + a, m->adam_m + a, m->adam_v + a,
+                             pbf ? pbf + a : nullptr, cnt, dend, dend, lr, beta1, beta2, eps,
+                             weight_decay, m->st, m->side));
+            }
+            CK(m, cudaEventRecord(m->upd_ev[g], m->side));
+        }
+        m->upd_pending = true;
+    }
     if (h_grad_norm) {
         int r = check_device_status(m);
         if (r) return r;
@@ -839,8 +927,12 @@ int gpt2_step(gpt2_model* m, float lr, float beta1, float beta2, float eps, floa
 
 int gpt2_zero_grad(gpt2_model* m) {
     if (!m) return GPT2_EINVAL;
+    // behind a pending AdamW (which reads the gradients) on the side stream;
+    // the backward writes gradients only on the side stream, or on the model's
+    // stream after joining it
     RUN(m, "zero_grad", 0, 0, 4.0 * m->n_arena,
-        cudaMemsetAsync(m->grads, 0, (size_t)m->n_arena * sizeof(float), m->stream));
+        cudaMemsetAsync(m->grads, 0, (size_t)m->n_arena * sizeof(float),
+                        m->upd_pending ? m->side : m->stream));
     return GPT2_OK;
 }
 
@@ -853,11 +945,15 @@ double gpt2_lr_schedule(int64_t it, int64_t warmup, int64_t horizon, double lr_m
 
 int gpt2_sync(gpt2_model* m) {
     if (!m) return GPT2_EINVAL;
+    int r = join_side(m);
+    if (r) return r;
     return check_device_status(m);
 }
 
 int gpt2_get_loss(gpt2_model* m, float* h_loss) {
     if (!m || !h_loss) return GPT2_EINVAL;
+    // the loss comes from the forward on the model's stream: no need to wait
+    // for a pending parameter update on the side stream
     int r = check_device_status(m);
     if (r) return r;
     DevState st;
@@ -891,6 +987,7 @@ static float* buffer_of(gpt2_model* m, int which) {
 
 int gpt2_copy_tensor(gpt2_model* m, int i, int which, float* dst) {
     if (!m || !dst || i < 0 || i >= (int)m->tensors.size()) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     float* buf = buffer_of(m, which);
     if (!buf) return fail(m, GPT2_EINVAL, "unknown buffer selector");
     CK(m, cudaStreamSynchronize(m->stream));
@@ -901,6 +998,7 @@ int gpt2_copy_tensor(gpt2_model* m, int i, int which, float* dst) {
 
 int gpt2_set_tensor(gpt2_model* m, int i, int which, const float* src) {
     if (!m || !src || i < 0 || i >= (int)m->tensors.size()) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     float* buf = buffer_of(m, which);
     if (!buf) return fail(m, GPT2_EINVAL, "unknown buffer selector");
     CK(m, cudaStreamSynchronize(m->stream));
@@ -916,6 +1014,7 @@ int gpt2_set_tensor(gpt2_model* m, int i, int which, const float* src) {
 
 int gpt2_copy_logits(gpt2_model* m, int64_t row0, int64_t nrows, float* dst) {
     if (!m || !dst || row0 < 0 || nrows < 0 || row0 + nrows > m->M) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     CK(m, cudaStreamSynchronize(m->stream));
     const int Vp = m->Vp, V = m->V;
     if (!m->use_bf16) {
@@ -935,6 +1034,7 @@ int gpt2_copy_logits(gpt2_model* m, int64_t row0, int64_t nrows, float* dst) {
 
 int gpt2_copy_row_losses(gpt2_model* m, int64_t row0, int64_t nrows, float* dst) {
     if (!m || !dst || row0 < 0 || nrows < 0 || row0 + nrows > m->M) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     CK(m, cudaStreamSynchronize(m->stream));
     CK(m, cudaMemcpy(dst, m->row_loss + row0, nrows * sizeof(float), cudaMemcpyDeviceToHost));
     return GPT2_OK;
@@ -963,6 +1063,7 @@ int gpt2_host_init_tensor(const gpt2_config* cfg, uint64_t seed, int kidx, float
 
 int gpt2_profile(gpt2_model* m, int on) {
     if (!m) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     int r = prof_collect(m);
     if (r) return r;
     m->sites.clear();
@@ -972,6 +1073,7 @@ int gpt2_profile(gpt2_model* m, int on) {
 
 int gpt2_profile_count(gpt2_model* m) {
     if (!m) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
     int r = prof_collect(m);
     if (r) return r;
     return (int)m->sites.size();

@@ -510,7 +510,8 @@ cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* p_bf16, in
                   int64_t decay_end, int64_t bf16_end, float lr, float beta1, float beta2, float eps,
                   float wd, const DevState* st, cudaStream_t s) {
     int64_t n4 = n / 4;
-    int blocks = num_sms() * 4;
+    const int64_t want = (n4 + 511) / 512;
+    int blocks = want < num_sms() * 4 ? (int)(want > 0 ? want : 1) : num_sms() * 4;
     adamw_kernel<<<blocks, 512, 0, s>>>((float4*)p, (const float4*)g, (float4*)m, (float4*)v,
                                         (uint2*)p_bf16, n4, decay_end / 4,
                                         p_bf16 ? bf16_end / 4 : 0, lr, beta1, beta2, eps, wd, st);

@@ -104,7 +104,12 @@ void gpt2_destroy(gpt2_model* model);
  * gpt2_backward the weight-gradient work (dW GEMMs, bias gradients) runs on a
  * second stream that the library owns; it is forked from and joined back to
  * this stream by events before gpt2_backward returns, so the caller sees one
- * ordered stream (and a stream capture records both branches). */
+ * ordered stream (and a stream capture records both branches). gpt2_step's
+ * AdamW also runs there, group by group in the order the next gpt2_forward
+ * reads the parameters (which waits for each group just before using it), and
+ * gpt2_zero_grad queues behind it; every other call that touches model state
+ * (gpt2_sync, tensor copies, profiling, gpt2_set_stream) first makes this
+ * stream wait for it. gpt2_get_loss does not (the loss comes from the forward). */
 int gpt2_set_stream(gpt2_model* model, void* cuda_stream);
 
 /*
