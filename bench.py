@@ -251,6 +251,9 @@ def run_ours(args):
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
+    # the library counts its launches even with event timing off: clear the
+    # counters here and read them right after the timed region
+    model.profile(False)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -258,6 +261,7 @@ def run_ours(args):
         train_step(args.warmup + k, args.warmup + k)
     e1.record(stream)
     torch.cuda.synchronize()
+    launches_timed = sum(r["kernels"] for r in model.profile_report())
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
@@ -277,7 +281,6 @@ def run_ours(args):
     rep = model.profile_report()
     model.profile(False)
     per_step = {r["name"]: r for r in rep}
-    kernels_per_step = sum(r["kernels"] for r in rep) / psteps
     peaks = load_peaks()
     gemm = [r for r in rep if r["name"].startswith("gemm_")]
     g_ms = sum(r["ms"] for r in gemm)
@@ -359,7 +362,7 @@ def run_ours(args):
         "memory_bound_kernels": mem_kernels,
         "attention": attn,
         "site_ms_per_step": sites,
-        "gpu_launches": int(round(kernels_per_step * args.steps)),
+        "gpu_launches": int(launches_timed),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(2 * B * T * 4), "d2h_bytes_per_step": 4,
@@ -376,6 +379,46 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_op_workload(args):
+    """Four rounds of one block's op-level kernels at the workload's shapes,
+    for ncu captures of a single kernel (no timing, no JSON bench line):
+      attention  causal attention forward, then backward (dQ, then dK/dV)
+      mlp_gemms  the MLP's c_fc GEMM with the GELU epilogue, then the c_proj
+                 input-gradient GEMM with the GELU-backward epilogue"""
+    import torch
+    from decoder_only_transformer_06_b300 import gpt2
+    L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    if args.batch:
+        B = args.batch
+    M = B * T
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rnd = lambda *shape, scale=1.0: (scale * torch.randn(*shape, device="cuda", generator=g)).bfloat16()
+    if args.op_workload == "attention":
+        hs = C // H
+        qkv, dout = rnd(M, 3 * C), rnd(M, C)
+        out = torch.empty(M, C, dtype=torch.bfloat16, device="cuda")
+        dqkv = torch.empty(M, 3 * C, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B * H * T, device="cuda")
+        scratch = torch.empty(B * H * T, device="cuda")
+        for _ in range(4):
+            gpt2.op_attention_fwd(gpt2.GPT2_BF16, B, T, H, hs, qkv, out, lse)
+            gpt2.op_attention_bwd(gpt2.GPT2_BF16, B, T, H, hs, qkv, out, lse, dout, dqkv, scratch)
+    else:
+        F = 4 * C
+        u, w_fc, b_fc = rnd(M, C), rnd(F, C, scale=0.02), torch.zeros(F, device="cuda")
+        dy, w_mp = rnd(M, C), rnd(C, F, scale=0.02)
+        dgelu = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+        h = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+        dh = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+        for _ in range(4):
+            gpt2.op_gemm_bf16_gelu(M, F, C, u, C, 1, w_fc, C, 1, dgelu, h, bias=b_fc)
+            gpt2.op_gemm_bf16_gelu(M, F, C, dy, C, 1, w_mp, F, 0, dh, dgelu, backward=True)
+    torch.cuda.synchronize()
+    gpt2.op_sync()
+    print(json.dumps({"op_workload": args.op_workload, "workload": args.workload, "batch": B,
+                      "rounds": 4}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,7 +429,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (small profiling captures)")
+    ap.add_argument("--op-workload", choices=["attention", "mlp_gemms"], default=None,
+                    help="only run one block's op-level kernels (for ncu captures)")
     args = ap.parse_args()
+    if args.op_workload:
+        run_op_workload(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
