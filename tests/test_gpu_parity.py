@@ -171,6 +171,39 @@ def test_char_bf16_loss_trajectory():
         tr.step(lr=1e-3)
 
 
+def test_fp32_consecutive_steps_track_the_oracle():
+    """Three training steps in a row, zero_grad after each step. The library
+    runs each step's AdamW on its second stream while the next forward waits
+    for every parameter group just before using it, and queues zero_grad behind
+    that update: a layer that read a parameter before its update, or gradients
+    not cleared before the next backward, would move the next step's loss by far
+    more than the fp32 tolerance."""
+    c = CONFIGS["tiny"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=11)
+    tr = O.Trainer(c, 11)
+    for step in range(3):
+        x, y = synthdata.uniform_batch(65, c.batch_size, c.seq_len, 500 + step)
+        loss = m.forward(dev(x), dev(y))
+        lo, _ = tr.forward(x, y)
+        assert abs(loss - lo) / lo < 1e-4, (step, loss, lo)
+        m.backward()
+        tr.backward()
+        m.step(lr=3e-3)
+        tr.step(lr=3e-3)
+        m.zero_grad()
+        tr.zero_grad()
+    # after the last update: parameters (read through a copy, which waits for
+    # the pending update) close to the oracle's. An Adam step moves an element
+    # by about lr whatever |g|, so an element whose tiny gradient has the other
+    # sign may differ by up to 2 lr per step: 6 lr after three steps.
+    p = m.state(gpt2.GPT2_PARAM)
+    for n, a in tr.params.items():
+        assert float(np.abs(p[n] - a).max()) <= 6 * 3e-3, n
+        assert rel_l2(p[n], a) < 1e-2, (n, rel_l2(p[n], a))
+    g = m.state(gpt2.GPT2_GRAD)
+    assert all(not np.any(v) for v in g.values())
+
+
 def test_grad_accumulation_matches_one_big_batch():
     base = CONFIGS["tiny"]
     x, y = synthdata.uniform_batch(65, 8, base.seq_len, 9)
