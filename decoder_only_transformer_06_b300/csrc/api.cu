@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -1037,6 +1038,94 @@ int gpt2_copy_row_losses(gpt2_model* m, int64_t row0, int64_t nrows, float* dst)
     if (int r0 = join_side(m)) return r0;
     CK(m, cudaStreamSynchronize(m->stream));
     CK(m, cudaMemcpy(dst, m->row_loss + row0, nrows * sizeof(float), cudaMemcpyDeviceToHost));
+    return GPT2_OK;
+}
+
+// ------------------------------------------------------------------ checkpoint
+static const char CKPT_MAGIC[16] = {'G', 'P', 'T', '2', 'B', '3', '0', '0', 'C', 'K', 'P', 'T', 0, 'v', '1', 0};
+
+static void cfg_fields(const gpt2_config& c, int32_t f[10]) {
+    f[0] = c.n_layer; f[1] = c.n_head; f[2] = c.d_model; f[3] = c.vocab_size; f[4] = c.padded_vocab;
+    f[5] = c.block_size; f[6] = c.batch_size; f[7] = c.seq_len; f[8] = c.grad_accum_steps;
+    f[9] = c.precision;
+}
+
+int gpt2_save(gpt2_model* m, const char* path) {
+    if (!m || !path) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
+    CK(m, cudaStreamSynchronize(m->stream));
+    DevState st;
+    CK(m, cudaMemcpy(&st, m->st, sizeof st, cudaMemcpyDeviceToHost));
+    FILE* f = std::fopen(path, "wb");
+    if (!f) return fail(m, GPT2_EINVAL, std::string("cannot create checkpoint file ") + path);
+    int32_t fields[10];
+    cfg_fields(m->cfg, fields);
+    const int64_t n = m->n_arena;
+    const int32_t t = st.step_t;
+    bool ok = std::fwrite(CKPT_MAGIC, 1, 16, f) == 16 && std::fwrite(fields, 4, 10, f) == 10 &&
+              std::fwrite(&n, 8, 1, f) == 1 && std::fwrite(&t, 4, 1, f) == 1;
+    std::vector<float> host;
+    try {
+        host.resize((size_t)n);
+    } catch (...) {
+        std::fclose(f);
+        return fail(m, GPT2_ENOMEM, "host buffer for the checkpoint");
+    }
+    const float* bufs[3] = {m->params, m->adam_m, m->adam_v};
+    for (int b = 0; b < 3 && ok; b++) {
+        cudaError_t e = cudaMemcpy(host.data(), bufs[b], (size_t)n * 4, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) {
+            std::fclose(f);
+            return fail_cuda(m, "checkpoint read-back", e);
+        }
+        ok = std::fwrite(host.data(), 4, (size_t)n, f) == (size_t)n;
+    }
+    ok = (std::fclose(f) == 0) && ok;
+    if (!ok) return fail(m, GPT2_EINVAL, std::string("cannot write checkpoint file ") + path);
+    return GPT2_OK;
+}
+
+int gpt2_load(gpt2_model* m, const char* path) {
+    if (!m || !path) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
+    FILE* f = std::fopen(path, "rb");
+    if (!f) return fail(m, GPT2_EINVAL, std::string("cannot open checkpoint file ") + path);
+    char magic[16];
+    int32_t fields[10], mine[10];
+    int64_t n = 0;
+    int32_t t = 0;
+    bool ok = std::fread(magic, 1, 16, f) == 16 && std::memcmp(magic, CKPT_MAGIC, 16) == 0 &&
+              std::fread(fields, 4, 10, f) == 10 && std::fread(&n, 8, 1, f) == 1 &&
+              std::fread(&t, 4, 1, f) == 1;
+    cfg_fields(m->cfg, mine);
+    if (!ok || std::memcmp(fields, mine, sizeof mine) != 0 || n != m->n_arena || t < 0) {
+        std::fclose(f);
+        return fail(m, GPT2_EINVAL, std::string("not a checkpoint of this model configuration: ") + path);
+    }
+    std::vector<float> host;
+    try {
+        host.resize((size_t)n);
+    } catch (...) {
+        std::fclose(f);
+        return fail(m, GPT2_ENOMEM, "host buffer for the checkpoint");
+    }
+    CK(m, cudaStreamSynchronize(m->stream));
+    float* bufs[3] = {m->params, m->adam_m, m->adam_v};
+    for (int b = 0; b < 3; b++) {
+        if (std::fread(host.data(), 4, (size_t)n, f) != (size_t)n) {
+            std::fclose(f);
+            return fail(m, GPT2_EINVAL, std::string("truncated checkpoint file ") + path);
+        }
+        cudaError_t e = cudaMemcpy(bufs[b], host.data(), (size_t)n * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            std::fclose(f);
+            return fail_cuda(m, "checkpoint upload", e);
+        }
+    }
+    std::fclose(f);
+    CK(m, cudaMemcpy((char*)m->st + offsetof(DevState, step_t), &t, sizeof t, cudaMemcpyHostToDevice));
+    if (m->use_bf16) CK(m, k::f32_to_bf16(m->params, m->pbf, m->decay_end, m->stream));
+    CK(m, cudaStreamSynchronize(m->stream));
     return GPT2_OK;
 }
 

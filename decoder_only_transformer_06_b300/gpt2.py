@@ -73,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_copy_logits": (I, [P, I64, I64, FP]),
         "gpt2_copy_row_losses": (I, [P, I64, I64, FP]),
         "gpt2_num_params": (I64, [P, I, I]),
+        "gpt2_save": (I, [P, ctypes.c_char_p]),
+        "gpt2_load": (I, [P, ctypes.c_char_p]),
         "gpt2_host_init_tensor": (I, [ctypes.POINTER(gpt2_config), U64, I, FP]),
         "gpt2_profile": (I, [P, I]),
         "gpt2_profile_count": (I, [P]),
@@ -246,6 +248,14 @@ class GPT2:
 
     def state(self, which=GPT2_PARAM) -> dict:
         return {n: self.get(i, which) for i, n in enumerate(self.names)}
+
+    def save(self, path):
+        """Checkpoint: parameters, Adam moments and step counter (gpt2_save)."""
+        self._ck(_lib.gpt2_save(self.h, str(path).encode()))
+
+    def load(self, path):
+        """Resume from a checkpoint written by save() for the same config."""
+        self._ck(_lib.gpt2_load(self.h, str(path).encode()))
 
     def logits(self, row0=0, nrows=None) -> np.ndarray:
         M = self.cfg.batch_size * self.cfg.seq_len

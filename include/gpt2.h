@@ -197,6 +197,22 @@ int gpt2_copy_logits(gpt2_model* model, int64_t row0, int64_t nrows, float* h_ds
  * 0 for ignored rows). Synchronises. */
 int gpt2_copy_row_losses(gpt2_model* model, int64_t row0, int64_t nrows, float* h_dst);
 
+/* Checkpoint of the training state: the pages' ckpt.pt holds the model, the
+ * optimizer state and the iteration (nanoGPT guide, "train.py": saving and
+ * --init_from=resume). gpt2_save writes the configuration, the AdamW step
+ * counter and the fp32 parameter, first-moment and second-moment arenas to the
+ * file `path` (created or truncated). gpt2_load reads such a file into a model
+ * created with the same configuration (EINVAL otherwise, and for a file that is
+ * not a checkpoint of this library): it replaces parameters, moments and the
+ * step counter, rebuilds the bf16 weight copy from the fp32 parameters, and
+ * leaves the gradients as they are. Training resumed from a checkpoint is
+ * bit-identical to training that never stopped. Both synchronise; EINVAL also
+ * for I/O failures (the message names the file). Format: 16-byte magic
+ * "GPT2B300CKPT\0v1\0", the ten int32 fields of gpt2_config, int64 arena
+ * length n, int32 step counter, then three arrays of n little-endian fp32. */
+int gpt2_save(gpt2_model* model, const char* path);
+int gpt2_load(gpt2_model* model, const char* path);
+
 /* Parameter count; the tied matrix counted once (nanoGPT guide Deep dive 1).
  * include_wpe: count the position table; padded: count wte as Vp rows. */
 int64_t gpt2_num_params(const gpt2_model* model, int include_wpe, int padded);

@@ -311,3 +311,42 @@ def test_gpt2_124m_full_size_sampled_rows():
     assert math.isfinite(norm) and norm > 0
     loss2 = m.forward(dev(x), dev(y))
     assert loss2 < loss
+
+
+def test_checkpoint_resume_is_bit_exact(tmp_path):
+    """Three steps in one run against two steps, a checkpoint, a fresh model
+    (other seed) that loads it, and the third step: parameters, Adam moments
+    and the next loss identical bit for bit (the pages' ckpt.pt resume)."""
+    c = oracle_cfg(CONFIGS["char"], batch_size=2, n_layer=2)
+    batches = [synthdata.markov_batch(65, c.batch_size, c.seq_len, 700 + i) for i in range(3)]
+
+    def run(m, steps):
+        loss = None
+        for x, y in steps:
+            m.zero_grad()
+            loss = m.forward(dev(x), dev(y))
+            m.backward()
+            m.step(lr=2e-3)
+        return loss
+
+    for precision in (gpt2.GPT2_BF16, gpt2.GPT2_FP32):
+        a = gpt2.GPT2(gpu_cfg(c, precision), seed=21)
+        la = run(a, batches)
+        b = gpt2.GPT2(gpu_cfg(c, precision), seed=21)
+        run(b, batches[:2])
+        path = tmp_path / f"ckpt{precision}.bin"
+        b.save(path)
+        r = gpt2.GPT2(gpu_cfg(c, precision), seed=99)
+        r.load(path)
+        lr_ = run(r, batches[2:])
+        assert lr_ == la, (precision, lr_, la)
+        for which in (gpt2.GPT2_PARAM, gpt2.GPT2_ADAM_M, gpt2.GPT2_ADAM_V):
+            sa, sr = a.state(which), r.state(which)
+            for n in sa:
+                assert np.array_equal(sa[n], sr[n]), (precision, which, n)
+        # a checkpoint of another configuration is refused
+        other = gpt2.GPT2(gpu_cfg(oracle_cfg(c, n_layer=1), precision), seed=1)
+        with pytest.raises(gpt2.GPT2Error):
+            other.load(path)
+        for m in (a, b, r, other):
+            m.close()
