@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <atomic>
 
 typedef __nv_bfloat16 bf16;
 
@@ -195,6 +196,14 @@ cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, cons
                          int splits, DevState* st, cudaStream_t s);
 bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi);
 
-int num_sms();
+int num_sms();   // SM count of the current device
+// Bit of the current device in a per-device set-up mask: kernel attributes
+// (the dynamic shared-memory limit) and occupancy figures are per device, so
+// host code that caches them keeps one flag per device (devices 0..63).
+inline unsigned long long device_bit() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0) d = 0;
+    return 1ull << (d & 63);
+}
 
 }  // namespace k

@@ -443,11 +443,12 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     memset(&omap, 0, sizeof omap);
     if (!make_qkv_map(&map, qkv, B, T, H * hs) || !make_rows_out_map(&omap, out, B, T, H * hs))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr_done{0};   // per device
+    const unsigned long long dbit = device_bit();
+    if (!(attr_done.load() & dbit)) {
         CUDA_OK(cudaFuncSetAttribute(fa_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)AT_SMEM));
-        attr = true;
+        attr_done.fetch_or(dbit);
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
@@ -1124,13 +1125,14 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* out, const bf16* dout,
     if (!make_qkv_map(&mq, qkv, B, T, H * hs) || !make_do_map(&md, dout, B, T, H * hs) ||
         !make_dqkv_map(&mo, dqkv, B, T, H * hs) || !make_do_map(&mf, out, B, T, H * hs))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
+    static std::atomic<unsigned long long> attr_done{0};   // per device
+    const unsigned long long dbit = device_bit();
+    if (!(attr_done.load() & dbit)) {
         CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)KV_SMEM));
         CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)DQ_SMEM));
-        attr = true;
+        attr_done.fetch_or(dbit);
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();

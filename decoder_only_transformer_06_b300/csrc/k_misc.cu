@@ -6,12 +6,15 @@
 namespace k {
 
 int num_sms() {
-    static int n = 0;
+    static std::atomic<int> cached[64];     // per device; 0 = not queried yet
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+    std::atomic<int>& slot = cached[dev & 63];
+    int n = slot.load();
     if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        slot.store(n);
     }
     return n;
 }
