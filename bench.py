@@ -123,10 +123,13 @@ def dist_env():
 
 
 def barrier_max(x: float, world: int, torch):
+    """Max of x over the ranks (a barrier as a side effect); the tensor lives
+    where the process group's backend wants it (CUDA for NCCL, host for gloo)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

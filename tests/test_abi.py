@@ -117,4 +117,6 @@ def test_null_arguments_are_rejected():
     assert L.gpt2_backward(None) == gpt2.GPT2_EINVAL
     assert L.gpt2_step(None, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == gpt2.GPT2_EINVAL
     assert L.gpt2_zero_grad(None) == gpt2.GPT2_EINVAL
+    assert L.gpt2_save(None, b"/dev/null") == gpt2.GPT2_EINVAL
+    assert L.gpt2_load(None, b"/dev/null") == gpt2.GPT2_EINVAL
     L.gpt2_destroy(None)
