@@ -207,7 +207,10 @@ int gpt2_copy_row_losses(gpt2_model* model, int64_t row0, int64_t nrows, float* 
  * step counter, rebuilds the bf16 weight copy from the fp32 parameters, and
  * leaves the gradients as they are. Training resumed from a checkpoint is
  * bit-identical to training that never stopped. Both synchronise; EINVAL also
- * for I/O failures (the message names the file). Format: 16-byte magic
+ * for I/O failures (the message names the file). The header and configuration
+ * are checked before anything is overwritten; a file truncated inside the
+ * arrays leaves the model's parameters and moments partly replaced (load a
+ * good checkpoint, or recreate the model). Format: 16-byte magic
  * "GPT2B300CKPT\0v1\0", the ten int32 fields of gpt2_config, int64 arena
  * length n, int32 step counter, then three arrays of n little-endian fp32. */
 int gpt2_save(gpt2_model* model, const char* path);
