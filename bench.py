@@ -163,9 +163,20 @@ def cpu_oracle_time(workload: str, tokens: int, steps: int = 1):
     return times, cores, sample
 
 
+def workload_config(workload: str, B: int, world: int) -> dict:
+    """The bench line's `config`, the same for both arms."""
+    L, H, C, V, Vp, T, _, _ = WORKLOADS[workload]
+    return {"workload": workload, "global_batch": B * world, "seq_len": T,
+            "n_layer": L, "n_head": H, "d_model": C, "vocab": V, "padded_vocab": Vp,
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "l2": "inputs larger than L2: a step's weights, optimizer state and activations far exceed the 126 MB L2"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    if args.batch:
+        B = args.batch
     if rank != 0:
         return
     n = args.steps + args.warmup
@@ -186,8 +197,9 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * sec, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "global_batch": 1, "seq_len": tokens,
-                   "sample_of": f"B={B} T={T}"},
+        # the workload timed is ours; the oracle runs a bounded sample of it
+        # (cpu_baseline.sample says which)
+        "config": workload_config(args.workload, B, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -354,10 +366,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic Zipf(1.1) token ids (seeded), random-init weights",
-        "config": {"workload": args.workload, "global_batch": B * world, "seq_len": T,
-                   "n_layer": L, "n_head": H, "d_model": C, "vocab": V, "padded_vocab": Vp,
-                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": "working set (7+ GB of weights and activations) far larger than L2"},
+        "config": workload_config(args.workload, B, world),
         "mfu": {"flops_per_token": fpt, "achieved_tflops": achieved / 1e12,
                 "vs_nominal_2.25PF": achieved / NOMINAL_BF16_DENSE / world,
                 "vs_measured_burst": achieved / (peaks["bf16"] * 1e12) / world},
