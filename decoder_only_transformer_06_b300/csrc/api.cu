@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <mutex>
@@ -121,6 +122,7 @@ struct gpt2_model {
     std::vector<SiteAcc> sites;
     std::string err = "no error";
     std::vector<void*> allocs;
+    int allocs_tried = 0;       // device allocations attempted (fault injection)
 
     // --- helpers
     float* P(int i) const { return params + tensors[i].offset; }
@@ -277,8 +279,19 @@ static void host_init_tensor(const gpt2_config* c, const TensorRec& r, int k, ui
 }
 
 // ------------------------------------------------------------------ create
+// Fault injection for tests, on the host only: with GPT2_FAIL_ALLOC_AT=n in
+// the environment, the n-th device allocation of a gpt2_create (counting from
+// 0) fails as if the device had run out of memory, before any cudaMalloc.
 static int alloc_dev(gpt2_model* m, void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
+    const int attempt = m->allocs_tried++;
+    if (const char* env = std::getenv("GPT2_FAIL_ALLOC_AT")) {
+        char* end = nullptr;
+        const long at = std::strtol(env, &end, 10);
+        if (end != env && at == attempt)
+            return fail(m, GPT2_ENOMEM, "injected allocation failure at allocation " +
+                                            std::to_string(attempt) + " (GPT2_FAIL_ALLOC_AT)");
+    }
     cudaError_t e = cudaMalloc(p, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();

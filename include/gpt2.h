@@ -92,7 +92,10 @@ typedef struct gpt2_model gpt2_model;   /* opaque; owns all device memory */
  *   cfg: read only, copied. out: receives the new model (NULL on failure).
  * Errors: EINVAL (NULL, sizes <= 0, d_model % n_head != 0, seq_len >
  * block_size, padded_vocab < vocab_size, a shape the chosen precision does
- * not support), ENOMEM, ECUDA. Synchronises.
+ * not support), ENOMEM, ECUDA. Synchronises. On failure everything already
+ * allocated is freed. Testing hook: with GPT2_FAIL_ALLOC_AT=n in the
+ * environment, the n-th device allocation (from 0) fails with ENOMEM before
+ * any cudaMalloc (allocation 0 precedes every CUDA call of gpt2_create).
  */
 int gpt2_create(const gpt2_config* cfg, uint64_t seed, gpt2_model** out);
 

@@ -110,6 +110,18 @@ def test_create_rejects_bad_configs_without_touching_the_gpu(bad):
     assert gpt2.lib().gpt2_last_error(None)
 
 
+def test_injected_allocation_failure_is_reported(monkeypatch):
+    """Host-side fault injection: the first device allocation of gpt2_create
+    fails (before any CUDA call); the call returns ENOMEM with no model and a
+    message naming the injected failure."""
+    monkeypatch.setenv("GPT2_FAIL_ALLOC_AT", "0")
+    c = _cfg("tiny", precision=gpt2.GPT2_FP32).to_c()     # head size 16: the fp32-math path
+    h = ctypes.c_void_p()
+    r = gpt2.lib().gpt2_create(ctypes.byref(c), 1, ctypes.byref(h))
+    assert r == gpt2.GPT2_ENOMEM and not h.value
+    assert b"injected allocation failure at allocation 0" in gpt2.lib().gpt2_last_error(None)
+
+
 def test_null_arguments_are_rejected():
     L = gpt2.lib()
     assert L.gpt2_create(None, 1, None) == gpt2.GPT2_EINVAL
