@@ -368,6 +368,78 @@ def test_adamw_matches_torch_over_steps():
         assert np.allclose(b, tb.detach().numpy(), atol=1e-15, rtol=1e-13)
 
 
+def _torch_gpt_modules(cfg):
+    """The model's parameters held by real torch modules (nn.Embedding,
+    nn.Linear, nn.LayerNorm; the LM head is the token embedding, tied), keyed
+    by the oracle's names. Shapes come from the modules, not from the oracle."""
+    C, L = cfg.d_model, cfg.n_layer
+    mods = torch.nn.ModuleDict({"wte": torch.nn.Embedding(cfg.Vp, C),
+                                "wpe": torch.nn.Embedding(cfg.block_size, C)})
+    for l in range(L):
+        mods[f"h{l}_ln1"] = torch.nn.LayerNorm(C)
+        mods[f"h{l}_attn"] = torch.nn.Linear(C, 3 * C)
+        mods[f"h{l}_attn_proj"] = torch.nn.Linear(C, C)
+        mods[f"h{l}_ln2"] = torch.nn.LayerNorm(C)
+        mods[f"h{l}_fc"] = torch.nn.Linear(C, 4 * C)
+        mods[f"h{l}_mlp_proj"] = torch.nn.Linear(4 * C, C)
+    mods["lnf"] = torch.nn.LayerNorm(C)
+    named = {"wte": mods["wte"].weight, "wpe": mods["wpe"].weight,
+             "lnf.g": mods["lnf"].weight, "lnf.b": mods["lnf"].bias}
+    for l in range(L):
+        for part in ("ln1", "ln2"):
+            named[f"h{l}.{part}.g"] = mods[f"h{l}_{part}"].weight
+            named[f"h{l}.{part}.b"] = mods[f"h{l}_{part}"].bias
+        for part in ("attn", "attn_proj", "fc", "mlp_proj"):
+            named[f"h{l}.{part}.W"] = mods[f"h{l}_{part}"].weight
+            named[f"h{l}.{part}.b"] = mods[f"h{l}_{part}"].bias
+    return named
+
+
+def test_decay_groups_follow_configure_optimizers():
+    """Which tensors weight decay touches (nanoGPT guide, Deep dive 1
+    configure_optimizers: parameters of two or more dimensions decay, i.e. the
+    embeddings and every Linear weight; biases and LayerNorm gains/shifts do
+    not; sotaaz Section 3: decay on 2-D params only). Two pins:
+    (1) by category, as the pages list them: the oracle decays exactly wte,
+    wpe and the four Linear weights of each block;
+    (2) by the library optimizer: two clipped steps of torch AdamW with the
+    parameter groups built the pages' way over real torch modules match the
+    oracle's Trainer.step on the same gradients. Decaying a 1-D tensor, or
+    sparing wpe, fails both."""
+    cfg = CONFIGS["tiny"]
+    shapes = dict(O.param_shapes(cfg))
+    decayed = {n for n, s in shapes.items() if O.decays(n, s)}
+    linear_w = {f"h{l}.{p}.W" for l in range(cfg.n_layer)
+                for p in ("attn", "attn_proj", "fc", "mlp_proj")}
+    assert decayed == {"wte", "wpe"} | linear_w
+
+    named = _torch_gpt_modules(cfg)
+    assert set(named) == set(shapes)
+    for n, p in named.items():
+        assert tuple(p.shape) == tuple(shapes[n]), n
+    tr = O.Trainer(cfg, 5)
+    with torch.no_grad():
+        for n, p in named.items():
+            p.copy_(torch.tensor(tr.params[n]))
+    groups = [{"params": [p for p in named.values() if p.dim() >= 2], "weight_decay": 0.1},
+              {"params": [p for p in named.values() if p.dim() < 2], "weight_decay": 0.0}]
+    opt = torch.optim.AdamW(groups, lr=3e-3, betas=(0.9, 0.95), eps=1e-8)
+    for step in range(2):
+        x, y = synthdata.uniform_batch(65, cfg.batch_size, cfg.seq_len, 40 + step)
+        tr.zero_grad()
+        tr.forward(x, y)
+        tr.backward()
+        for n, p in named.items():
+            p.grad = torch.tensor(tr.grads[n]).clone()
+        tn = torch.nn.utils.clip_grad_norm_(list(named.values()), 1.0).item()
+        opt.step()
+        n_orc = tr.step(lr=3e-3, weight_decay=0.1, clip=1.0)
+        assert abs(n_orc - tn) <= 1e-12 * tn
+        for n, p in named.items():
+            d = float(np.abs(tr.params[n] - p.detach().numpy()).max())
+            assert d < 1e-14, (step, n, d)
+
+
 def test_adamw_first_step_closed_form():
     rng = np.random.default_rng(8)
     p0 = rng.normal(size=100); g = rng.normal(size=100)
