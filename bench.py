@@ -37,14 +37,22 @@ import numpy as np  # noqa: E402
 import synthdata  # noqa: E402
 
 METRIC = "tokens/s and MFU, GPT-2 124M fwd+bwd+AdamW step, B=16 T=1024, 1 B300"
-NOMINAL_BF16_DENSE = 2.25e15     # B300 dense bf16 tensor peak (NVIDIA nominal)
+# B300 dense bf16 tensor peak: NVIDIA's HGX B300 specification lists 36
+# PFLOPS FP16/BF16 for eight GPUs with 2:4 sparsity, i.e. 18 dense, 2.25 per GPU
+NOMINAL_BF16_DENSE = 2.25e15
 
 WORKLOADS = {
     # name: (n_layer, n_head, d_model, vocab, padded, T, B, stream kind)
     "gpt2_124m": (12, 12, 768, 50257, 50304, 1024, 16, "zipf"),
+    "gpt2_124m_accum32": (12, 12, 768, 50257, 50304, 1024, 16, "zipf"),
     "gpt2_24l_1024d": (24, 16, 1024, 50257, 50304, 1024, 8, "zipf"),
     "char": (6, 6, 384, 65, 0, 256, 64, "markov"),
 }
+# micro-steps per optimizer step (gradient accumulation; sotaaz Section 3:
+# 32 micro-batches of 16 x 1024 = 524,288 tokens per step)
+ACCUM = {"gpt2_124m_accum32": 32}
+# the oracle's bounded sample for both CPU arms: one sequence of this many tokens
+ORACLE_SAMPLE_TOKENS = 256
 
 
 def load_peaks():
@@ -53,8 +61,34 @@ def load_peaks():
         with open(p) as f:
             d = json.load(f)
         return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
-                    source="measured")
-    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+                    max_mhz=d.get("sm_max_mhz", 2032.0), source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, max_mhz=2032.0, source="fallback")
+
+
+def tensor_peak(peaks, clocks):
+    """The bf16 peak for a kernel timed at the clocks this run saw: the burst
+    figure (measured at full clock) when the run's median SM clock is within
+    5% of the maximum, else the burst figure scaled by median / maximum. The
+    sustained figure was taken at a lower clock under the power cap, so it
+    would overstate the fraction of a kernel that runs at full clock."""
+    mhz = (clocks or {}).get("sm_mhz")
+    mx = (clocks or {}).get("sm_max_mhz") or peaks["max_mhz"]
+    if mhz and mhz < 0.95 * mx:
+        return peaks["bf16"] * mhz / mx, (f"{peaks['source']} bf16_tflops (burst) x median SM clock "
+                                          f"{mhz:.0f} / {mx:.0f} MHz of this run")
+    return peaks["bf16"], (f"{peaks['source']} bf16_tflops (burst): this run's median SM clock "
+                           f"{mhz if mhz else 'unknown'} MHz is at the maximum")
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def flops_per_token(L, C, V_padded, T, block):
@@ -159,7 +193,8 @@ def cpu_oracle_time(workload: str, tokens: int, steps: int = 1):
     except Exception:
         cores = os.cpu_count()
     sample = (f"oracle (fp64 numpy) fwd+bwd+AdamW of the full {workload} model on 1 sequence x "
-              f"{tokens} tokens (of the {B}x{T} batch), {steps} step(s)")
+              f"{tokens} tokens (of the {B}x{T} batch), {steps} step(s); CPU {cpu_model()}, "
+              f"{os.cpu_count()} logical cores")
     return times, cores, sample
 
 
@@ -180,14 +215,9 @@ def run_reference(args):
     if rank != 0:
         return
     n = args.steps + args.warmup
-    # size the sample so that the whole run stays within ~3 minutes
-    budget = 180.0
-    tokens = 64
-    for cand in (1024, 512, 256, 128, 64):
-        est = 4.0 * (L / 12) + 25.0 * (L * C * C) / (12 * 768 * 768) * cand / 1024
-        if cand <= T and n * est <= budget:
-            tokens = cand
-            break
+    # the same bounded sample as the GPU arm's cpu_baseline (one sequence of
+    # ORACLE_SAMPLE_TOKENS tokens), one oracle step per bench step
+    tokens = min(T, ORACLE_SAMPLE_TOKENS)
     times, cores, sample = cpu_oracle_time(args.workload, tokens, n)
     timed = times[args.warmup:] if len(times) > args.warmup else times
     sec = sum(timed) / len(timed)
@@ -243,19 +273,27 @@ def run_ours(args):
     L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
     if args.batch:
         B = args.batch
+    accum = ACCUM.get(args.workload, 1)
     cfg = gpt2.Config(n_layer=L, n_head=H, d_model=C, vocab_size=V, padded_vocab=Vp,
-                      block_size=T, batch_size=B, seq_len=T, precision=gpt2.GPT2_BF16)
+                      block_size=T, batch_size=B, seq_len=T, grad_accum_steps=accum,
+                      precision=gpt2.GPT2_BF16)
     stream = torch.cuda.Stream()
     model = gpt2.GPT2(cfg, seed=1337, stream=stream)
-    nb = args.warmup + args.steps
+    # one synthetic batch per micro-step; with accumulation a bounded pool of
+    # distinct batches is cycled (the step's arithmetic does not depend on it)
+    nb = min((args.warmup + args.steps) * accum, 64)
     host = [synthdata.batch_for(kind, V, B, T, 1337 + 1000 * rank + i) for i in range(nb)]
     toks = [torch.from_numpy(x.reshape(-1)).cuda() for x, _ in host]
     tgts = [torch.from_numpy(y.reshape(-1)).cuda() for _, y in host]
     lr = lambda it: gpt2.lr_schedule(it, 715, 19073, 6e-4, 6e-5)
 
     def train_step(i, it):
-        model.forward(toks[i], tgts[i], sync_loss=False)
-        model.backward()
+        # one optimizer step: `accum` micro-steps of forward + backward, then
+        # clip + AdamW and zero_grad (nanoGPT guide Part IV Stages 4-5)
+        for a in range(accum):
+            j = (i * accum + a) % nb
+            model.forward(toks[j], tgts[j], sync_loss=False)
+            model.backward()
         model.step(lr(it), sync_norm=False)
         model.zero_grad()
 
@@ -274,6 +312,9 @@ def run_ours(args):
     e0.record(stream)
     for k in range(args.steps):
         train_step(args.warmup + k, args.warmup + k)
+    # the last step's AdamW and zero_grad run on the library's second stream:
+    # join it before the closing event
+    model.join()
     e1.record(stream)
     torch.cuda.synchronize()
     launches_timed = sum(r["kernels"] for r in model.profile_report())
@@ -284,7 +325,7 @@ def run_ours(args):
     model.sync()
     ms = barrier_max(ms, world, torch)
     ms_step = ms / args.steps
-    tokens_step = B * T * world
+    tokens_step = B * T * accum * world
     value = tokens_step / (ms_step / 1000.0)
 
     # ---- per-kernel measurement: CUDA events around every launch site, same
@@ -298,20 +339,27 @@ def run_ours(args):
     per_step = {r["name"]: r for r in rep}
     peaks = load_peaks()
     gemm = [r for r in rep if r["name"].startswith("gemm_")]
-    g_ms = sum(r["ms"] for r in gemm)
+    # the split-K reduce completes the weight-gradient GEMMs that write fp32
+    # partials: its time counts toward the GEMMs' (it adds no FLOPs)
+    reduce_ms = sum(r["ms"] for r in rep if r["name"] == "splitk_reduce")
+    g_ms = sum(r["ms"] for r in gemm) + reduce_ms
     g_flops = sum(r["flops"] for r in gemm)
     g_launch = sum(r["calls"] for r in gemm)
     achieved_tf = g_flops / (g_ms / 1000.0) / 1e12 if g_ms > 0 else None
     total_ms = sum(r["ms"] for r in rep)
     traffic = traffic_from_profiles(os.path.join(ROOT, "decoder_only_transformer_06_b300", "csrc",
                                                  "k_gemm_tc.cu"))
+    peak_tf, peak_src = tensor_peak(peaks, clk)
     roofline = {
-        "bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05; every Linear fwd/dX/dW)",
-        "achieved": achieved_tf, "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
-        "frac": (achieved_tf / peaks["bf16_sus"]) if achieved_tf else None,
+        "bound": "tensor",
+        "kernel": "gemm_tc_kernel (tcgen05; every Linear fwd/dX/dW) + splitk_reduce of its dW partials",
+        "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+        "frac": (achieved_tf / peak_tf) if achieved_tf else None,
         "traffic": traffic,
-        "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel timed inside the step)",
+        "peak_source": peak_src,
         "launches_per_step": g_launch / psteps,
+        "gemm_flops_per_step": g_flops / psteps,
+        "gemm_plus_reduce_ms_per_step": g_ms / psteps,
         "share_of_step": g_ms / total_ms if total_ms else None,
     }
     mem_kernels = {}
@@ -338,22 +386,27 @@ def run_ours(args):
     e2e_steps = max(2, min(args.steps, 10))
 
     def e2e_step(i, it):
-        with torch.cuda.stream(stream):
-            dt.copy_(pin_t[i], non_blocking=True)
-            dy.copy_(pin_y[i], non_blocking=True)
-        model.forward(dt, dy, sync_loss=False)
-        model.backward()
+        for a in range(accum):
+            j = (i * accum + a) % nb
+            with torch.cuda.stream(stream):
+                dt.copy_(pin_t[j], non_blocking=True)
+                dy.copy_(pin_y[j], non_blocking=True)
+            model.forward(dt, dy, sync_loss=False)
+            model.backward()
+        loss = model.loss()          # device -> host read of the step's (last micro-step's) loss
         model.step(lr(it), sync_norm=False)
         model.zero_grad()
-        return model.loss()          # device -> host read of the step's loss
+        return loss
 
     for i in range(2):
-        e2e_step(i % nb, i)
+        e2e_step(i, i)
+    model.sync()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for k in range(e2e_steps):
-        e2e_step(k % nb, k)
+        e2e_step(k, k)
+    model.sync()                     # the last step's update has landed
     e2e_s = barrier_max(time.perf_counter() - t0, world, torch)
     e2e_value = tokens_step * e2e_steps / e2e_s
 
@@ -377,12 +430,16 @@ def run_ours(args):
         "gpu_launches": int(launches_timed),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s",
-                "h2d_bytes_per_step": int(2 * B * T * 4), "d2h_bytes_per_step": 4,
+                "h2d_bytes_per_step": int(2 * B * T * 4 * accum), "d2h_bytes_per_step": 4,
                 "steps": e2e_steps},
     }
+    if accum > 1:
+        line["config"]["grad_accum_steps"] = accum
+        line["config"]["tokens_per_step"] = tokens_step
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times, cores, sample = cpu_oracle_time(args.workload, min(T, 1024), 1)
-        line["cpu_baseline"] = {"value": min(T, 1024) / times[0], "unit": "tokens/s",
+        tokens = min(T, ORACLE_SAMPLE_TOKENS)
+        times, cores, sample = cpu_oracle_time(args.workload, tokens, 3)
+        line["cpu_baseline"] = {"value": tokens / (sum(times) / len(times)), "unit": "tokens/s",
                                 "cores": cores, "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)

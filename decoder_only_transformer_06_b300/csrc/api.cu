@@ -964,6 +964,20 @@ int gpt2_sync(gpt2_model* m) {
     return check_device_status(m);
 }
 
+int gpt2_join(gpt2_model* m) {
+    if (!m) return GPT2_EINVAL;
+    return join_side(m);
+}
+
+int gpt2_set_wait_limit(gpt2_model* m, unsigned int cycles) {
+    if (!m) return GPT2_EINVAL;
+    if (int r0 = join_side(m)) return r0;
+    CK(m, cudaStreamSynchronize(m->stream));
+    CK(m, cudaMemcpy((char*)m->st + offsetof(DevState, wait_limit), &cycles, sizeof cycles,
+                     cudaMemcpyHostToDevice));
+    return GPT2_OK;
+}
+
 int gpt2_get_loss(gpt2_model* m, float* h_loss) {
     if (!m || !h_loss) return GPT2_EINVAL;
     // the loss comes from the forward on the model's stream: no need to wait
@@ -1195,14 +1209,104 @@ int gpt2_profile_entry(gpt2_model* m, int i, const char** name, int64_t* calls, 
 }
 
 // ------------------------------------------------------------------ op-level
-static DevState* op_state() {
-    static DevState* st = nullptr;
-    if (!st) {
-        if (cudaMalloc(&st, sizeof(DevState)) != cudaSuccess) return nullptr;
-        cudaMemset(st, 0, sizeof(DevState));
-    }
-    return st;
+}  // extern "C"
+
+// Status words of the op-level calls: bounded-wait expiries inside their
+// kernels are recorded in a DevState on the device the call ran on. The
+// allocating entry points use one word per device, allocated on first use;
+// the allocation-free attention backward uses a word compiled into the
+// library (below), so that neither it nor gpt2_op_sync has to allocate.
+namespace {
+
+constexpr int OP_MAX_DEVICES = 64;
+std::mutex g_op_mu;
+DevState* g_op_state[OP_MAX_DEVICES] = {};
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev >= 0 && dev < OP_MAX_DEVICES ? dev : -1;
 }
+
+// The current device's status word of the allocating op-level calls, created
+// (cudaMalloc) when `create` and it does not exist yet; nullptr otherwise.
+DevState* op_state_dev(bool create) {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_op_mu);
+    if (!g_op_state[dev] && create) {
+        DevState* st = nullptr;
+        if (cudaMalloc(&st, sizeof(DevState)) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (cudaMemset(st, 0, sizeof(DevState)) != cudaSuccess) {
+            cudaFree(st);
+            return nullptr;
+        }
+        g_op_state[dev] = st;
+    }
+    return g_op_state[dev];
+}
+DevState* op_state() { return op_state_dev(true); }
+
+// ---------------- the allocation-free attention backward's fixed device memory
+// Its rowsum scratch and its status word are file-scope device arrays: every
+// device that loads this library holds them until the process exits. Host code
+// must not use their names as addresses (on the host they are stand-in
+// symbols), so each device's addresses are looked up once, with that device
+// current, by cudaGetSymbolAddress.
+constexpr int64_t NOALLOC_ROWS_MAX = int64_t(1) << 20;   // B*H*T rows, 4 MiB of fp32
+__device__ __align__(256) float g_noalloc_rowsum[NOALLOC_ROWS_MAX];
+__device__ __align__(256) DevState g_noalloc_state;       // zero at load
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[OP_MAX_DEVICES] = {};
+DevState* g_noalloc_st[OP_MAX_DEVICES] = {};
+
+// Device addresses of g_noalloc_rowsum and g_noalloc_state on the current
+// device (looked up on the first call made on it; nothing is allocated).
+cudaError_t noalloc_scratch(float** out, DevState** st) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        void* q = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_rowsum);
+        if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress(&q, g_noalloc_state);
+        if (e != cudaSuccess) return e;
+        g_noalloc_st[dev] = (DevState*)q;
+        g_noalloc_ptr[dev] = (float*)p;
+    }
+    *out = g_noalloc_ptr[dev];
+    *st = g_noalloc_st[dev];
+    return cudaSuccess;
+}
+// The no-alloc status word of the current device if the allocation-free
+// entry point has run on it, else nullptr.
+DevState* noalloc_state_if_used() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    return g_noalloc_st[dev];
+}
+
+// Read a status word's error bits and clear them (the wait limit stays).
+cudaError_t take_status(DevState* st, unsigned int* err, unsigned int* site) {
+    DevState h;
+    cudaError_t r = cudaMemcpy(&h, st, sizeof h, cudaMemcpyDeviceToHost);
+    if (r != cudaSuccess) return r;
+    *err = h.err;
+    *site = h.timeout_site;
+    if (h.err) r = cudaMemset((char*)st + offsetof(DevState, err), 0, sizeof(unsigned int));
+    return r;
+}
+
+}  // namespace
+
+extern "C" {
 
 int gpt2_op_gemm_bf16(int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
                       int64_t ldb, int b_kmajor, const float* bias, void* out_bf16, float* out_f32,
@@ -1251,18 +1355,38 @@ int gpt2_op_gemm_bf16_gelu(int M, int N, int K, const void* A, int64_t lda, int 
 int gpt2_op_sync(void* stream) {
     cudaError_t r = cudaStreamSynchronize((cudaStream_t)stream);
     if (r != cudaSuccess) return fail_cuda(nullptr, "cudaStreamSynchronize", r);
+    // both status words of the current device; neither is created here, so
+    // this call allocates nothing
+    unsigned int err = 0, site = 0;
+    DevState* words[2] = {op_state_dev(false), noalloc_state_if_used()};
+    for (DevState* w : words) {
+        if (!w) continue;
+        unsigned int e = 0, s = 0;
+        r = take_status(w, &e, &s);
+        if (r != cudaSuccess) return fail_cuda(nullptr, "status read", r);
+        if (e && !err) site = s;
+        err |= e;
+    }
+    if (err & ERR_TIMEOUT)
+        return fail(nullptr, GPT2_ETIMEOUT,
+                    "a bounded device wait expired in an op-level call (site " +
+                        std::to_string(site) + ")");
+    return GPT2_OK;
+}
+
+int gpt2_op_set_wait_limit(unsigned int cycles) {
+    // testing hook: the allocating entry points' status word (created here if
+    // needed) and the allocation-free one of the current device
     DevState* st = op_state();
     if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
-    DevState h;
-    r = cudaMemcpy(&h, st, sizeof h, cudaMemcpyDeviceToHost);
-    if (r != cudaSuccess) return fail_cuda(nullptr, "status read", r);
-    if (h.err) {
-        const unsigned int err = h.err, site = h.timeout_site;
-        cudaMemset(st, 0, sizeof(DevState));
-        if (err & ERR_TIMEOUT)
-            return fail(nullptr, GPT2_ETIMEOUT,
-                        "a bounded device wait expired in an op-level call (site " +
-                            std::to_string(site) + ")");
+    float* scratch = nullptr;
+    DevState* nst = nullptr;
+    cudaError_t r = noalloc_scratch(&scratch, &nst);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "cudaGetSymbolAddress", r);
+    for (DevState* w : {st, nst}) {
+        r = cudaMemcpy((char*)w + offsetof(DevState, wait_limit), &cycles, sizeof cycles,
+                       cudaMemcpyHostToDevice);
+        if (r != cudaSuccess) return fail_cuda(nullptr, "wait limit write", r);
     }
     return GPT2_OK;
 }
@@ -1272,9 +1396,12 @@ int gpt2_op_attention_fwd(int precision, int B, int T, int H, int hs, const void
     if (!qkv || !out || !lse || B <= 0 || T <= 0 || H <= 0 || hs <= 0)
         return fail(nullptr, GPT2_EINVAL, "bad attention arguments");
     cudaError_t r;
-    if (precision == GPT2_BF16)
-        r = k::attention_fwd_bf16((const bf16*)qkv, (bf16*)out, lse, B, T, H, hs, op_state(),
+    if (precision == GPT2_BF16) {
+        DevState* st = op_state();
+        if (!st) return fail(nullptr, GPT2_ENOMEM, "status word allocation failed");
+        r = k::attention_fwd_bf16((const bf16*)qkv, (bf16*)out, lse, B, T, H, hs, st,
                                   (cudaStream_t)stream);
+    }
     else
         r = k::attention_fwd_f32((const float*)qkv, (float*)out, lse, B, T, H, hs, (cudaStream_t)stream);
     if (r == cudaErrorInvalidValue) return fail(nullptr, GPT2_EINVAL, "unsupported attention shape");
@@ -1306,52 +1433,12 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
 
 // ------------------------------------------------------- allocation-free variant
 // gpt2_op_attention_bwd_noalloc: the attention backward with its rowsum
-// scratch in a fixed, file-scope device array instead of a caller buffer, for
-// callers that cannot allocate device memory (a plugin inside a host that owns
-// the allocator and forbids cudaMalloc, code that runs while an allocator is
-// locked, or a host with a hard no-allocation policy after start-up).
-//
-// The array lives in every device that loads this library until the process
-// exits. Host code must not use its name as an address (on the host it is a
-// stand-in symbol), so each device's address is looked up once, with that
-// device current, by cudaGetSymbolAddress on the first call made on it.
-namespace {
-
-constexpr int64_t NOALLOC_ROWS_MAX = int64_t(1) << 20;   // B*H*T rows, 4 MiB of fp32
-__device__ __align__(256) float g_noalloc_rowsum[NOALLOC_ROWS_MAX];
-// status word of the kernels' bounded waits (zero at load; reported by gpt2_op_sync)
-__device__ __align__(256) DevState g_noalloc_state;
-
-constexpr int NOALLOC_MAX_DEVICES = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
-DevState* g_noalloc_st[NOALLOC_MAX_DEVICES] = {};
-
-// Device addresses of g_noalloc_rowsum and g_noalloc_state on the current
-// device (looked up once per device).
-cudaError_t noalloc_scratch(float** out, DevState** st) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        void* q = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_rowsum);
-        if (e != cudaSuccess) return e;
-        e = cudaGetSymbolAddress(&q, g_noalloc_state);
-        if (e != cudaSuccess) return e;
-        g_noalloc_st[dev] = (DevState*)q;
-        g_noalloc_ptr[dev] = (float*)p;
-    }
-    *out = g_noalloc_ptr[dev];
-    *st = g_noalloc_st[dev];
-    return cudaSuccess;
-}
-
-}  // namespace
-
+// scratch in the fixed, file-scope device array above instead of a caller
+// buffer, for callers that cannot allocate device memory (a plugin inside a
+// host that owns the allocator and forbids cudaMalloc, code that runs while an
+// allocator is locked, or a host with a hard no-allocation policy after
+// start-up). Its kernels' bounded-wait expiries go to the fixed status word
+// g_noalloc_state, which gpt2_op_sync reads.
 extern "C" int gpt2_op_attention_bwd_noalloc(int precision, int B, int T, int H, int hs,
                                              const void* qkv, const void* out, const float* lse,
                                              const void* dout, void* dqkv, void* stream) {

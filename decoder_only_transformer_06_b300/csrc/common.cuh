@@ -26,6 +26,8 @@ struct DevState {
     float bc1, bc2;      // 1 - beta1^t, 1 - beta2^t for the current step
     unsigned int err;    // ERR_* bits, sticky until read by the host
     unsigned int timeout_site;
+    unsigned int wait_limit;   // bounded-wait limit in SM cycles for single-CTA
+                               // kernels; 0 means WAIT_LIMIT_CYCLES
 };
 
 // A GEMM operand: element (row r, reduction index k) of the logical [R, K]
@@ -103,6 +105,17 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // it while a kernel runs, which would end a wait early.
 __device__ __forceinline__ long long wait_clock() { return clock64(); }
 #define WAIT_LIMIT_CYCLES 4000000000ll
+
+// The limit a kernel's pipeline waits use: DevState::wait_limit when set
+// (a test lowers it to make a wait run out), else WAIT_LIMIT_CYCLES. Kernels
+// keep it in the shared-memory word right after their abort flag. Waits that
+// drain in-flight copies after an abort always use WAIT_LIMIT_CYCLES, and so
+// does every wait of a CTA pair: the peer's copies complete on the leader's
+// barriers, so only a long wait covers them.
+__device__ __forceinline__ unsigned int wait_limit_of(const DevState* st) {
+    const unsigned int l = st ? st->wait_limit : 0u;
+    return l ? l : (unsigned int)WAIT_LIMIT_CYCLES;
+}
 
 // ------------------------------------------------------------------ launchers
 // All launchers return cudaSuccess or the launch error; `st` may be null.

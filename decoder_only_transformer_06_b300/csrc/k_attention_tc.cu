@@ -143,7 +143,8 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = (int)wait_limit_of(st);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
@@ -558,7 +559,8 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_co
         mbar_init(ps_free, 1);
         mbar_init(acc_full, 1);
         mbar_init(acc_free, 8);
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = (int)wait_limit_of(st);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == BW_ISSUE_A) tmem_alloc(tmem_slot, AT_TMEM_COLS);
@@ -841,7 +843,8 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_con
         mbar_init(st_free, 8);
         mbar_init(ds_full, 8);
         mbar_init(ds_free, 1);
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        abort_flag[1] = (int)wait_limit_of(st);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == BW_ISSUE_A) tmem_alloc(tmem_slot, AT_TMEM_COLS);

@@ -189,7 +189,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int i = 0; i < EPI_WARPS * Cfg::AUX_RING; i++) mbar_init(&auxbar[i], 1);
         mbar_init(drain, 1);
-        *abort_flag = 0;
+        abort_flag[0] = 0;
+        // a pair keeps the full limit (see wait_limit_of)
+        abort_flag[1] = (int)(PAIR ? (unsigned int)WAIT_LIMIT_CYCLES : wait_limit_of(st));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {

@@ -37,14 +37,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity. Returns false when the
 // CTA is aborting (another role timed out) or when this wait timed out.
+// abort_flag[0] is the CTA's abort flag, abort_flag[1] its wait limit in
+// cycles (wait_limit_of), both in shared memory.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = wait_clock();
+    const long long limit = (long long)(unsigned int)abort_flag[1];
+    // the clock is read every 64 polls, or every poll under a short limit
+    // (a test's), so that such a limit expires before a copy or product lands
+    const uint32_t every = limit < (1ll << 20) ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
+        if ((it & every) == 0) {
             if (*abort_flag) return false;
-            if (wait_clock() - t0 > WAIT_LIMIT_CYCLES) {
+            if (wait_clock() - t0 > limit) {
                 *abort_flag = 1;
                 return false;
             }

@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_lr_schedule": (D, [I64, I64, I64, D, D]),
         "gpt2_sync": (I, [P]),
         "gpt2_get_loss": (I, [P, FP]),
+        "gpt2_set_wait_limit": (I, [P, ctypes.c_uint]),
+        "gpt2_join": (I, [P]),
         "gpt2_num_tensors": (I, [P]),
         "gpt2_tensor_info": (I, [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(I),
                                  ctypes.POINTER(I64), ctypes.POINTER(I)]),
@@ -86,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_op_gemm_bf16": (I, [I, I, I, P, I64, I, P, I64, I, P, P, P, I64, I, P]),
         "gpt2_op_gemm_bf16_gelu": (I, [I, I, I, P, I64, I, P, I64, I, P, I, P, P, I64, P]),
         "gpt2_op_sync": (I, [P]),
+        "gpt2_op_set_wait_limit": (I, [ctypes.c_uint]),
         "gpt2_op_attention_fwd": (I, [I, I, I, I, I, P, P, P, P]),
         "gpt2_op_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
         "gpt2_op_attention_bwd_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P]),
@@ -214,6 +217,15 @@ class GPT2:
     def sync(self):
         self._ck(_lib.gpt2_sync(self.h))
 
+    def join(self):
+        """The model's stream waits for the library's second stream (no host sync)."""
+        self._ck(_lib.gpt2_join(self.h))
+
+    def set_wait_limit(self, cycles: int):
+        """Testing hook: bounded-wait limit (SM cycles; 0 = default) of the
+        model's single-CTA tensor-core kernels."""
+        self._ck(_lib.gpt2_set_wait_limit(self.h, int(cycles)))
+
     def loss(self) -> float:
         v = ctypes.c_float()
         self._ck(_lib.gpt2_get_loss(self.h, ctypes.byref(v)))
@@ -322,6 +334,12 @@ def op_sync(stream=None):
     """Synchronise the stream; raise GPT2Error(ETIMEOUT) if a bounded device
     wait expired in an op-level call since the last op_sync."""
     _check(_lib.gpt2_op_sync(_stream_ptr(stream)))
+
+
+def op_set_wait_limit(cycles: int):
+    """Testing hook: bounded-wait limit (SM cycles; 0 = default) of the
+    op-level calls' single-CTA kernels on the current device."""
+    _check(_lib.gpt2_op_set_wait_limit(int(cycles)))
 
 
 def op_attention_fwd(precision, B, T, H, hs, qkv, out, lse, stream=None):

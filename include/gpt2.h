@@ -170,8 +170,23 @@ double gpt2_lr_schedule(int64_t it, int64_t warmup, int64_t horizon, double lr_m
 /* Synchronise the stream and report any recorded device error. */
 int gpt2_sync(gpt2_model* model);
 
+/* Make the model's stream wait for everything the library queued on its
+ * second stream (a pending AdamW update and zero_grad), without synchronising
+ * the host: work the caller enqueues on the stream afterwards (an event, a
+ * copy of the parameters) sees the finished update. */
+int gpt2_join(gpt2_model* model);
+
 /* Mean loss of the last forward with targets (synchronises). */
 int gpt2_get_loss(gpt2_model* model, float* h_loss);
+
+/* Testing hook for failure detection (no counterpart on the pages). Every
+ * pipeline wait inside the library's single-CTA tensor-core kernels gives up
+ * after `cycles` SM cycles (0 restores the default, about two seconds), after
+ * which the kernel records ERR_TIMEOUT, drains its copies, frees its tensor
+ * memory and returns; the next synchronising call reports GPT2_ETIMEOUT and
+ * the model stays usable. CTA-pair GEMMs keep the default limit. A limit of a
+ * few hundred cycles makes waits expire on purpose. Synchronises. */
+int gpt2_set_wait_limit(gpt2_model* model, unsigned int cycles);
 
 /* Number of parameter tensors (canonical order: wte, wpe, per layer ln1.g,
  * ln1.b, attn.W, attn.b, attn_proj.W, attn_proj.b, ln2.g, ln2.b, fc.W, fc.b,
@@ -291,10 +306,17 @@ int gpt2_op_gemm_bf16_gelu(int M, int N, int K, const void* A, int64_t lda, int 
                            void* stream);
 
 /* Synchronise `stream` and report device-side conditions raised by the
- * op-level calls above since the previous gpt2_op_sync: GPT2_ETIMEOUT if a
- * bounded wait inside a kernel expired (the kernel then skipped its remaining
- * work, so its outputs are incomplete). Clears the recorded conditions. */
+ * op-level calls (including gpt2_op_attention_bwd_noalloc) on the current
+ * device since the previous gpt2_op_sync: GPT2_ETIMEOUT if a bounded wait
+ * inside a kernel expired (the kernel then skipped its remaining work, so its
+ * outputs are incomplete). Clears the recorded conditions. Allocates nothing. */
 int gpt2_op_sync(void* stream);
+
+/* Testing hook (no counterpart on the pages): the bounded-wait limit, in SM
+ * cycles, of the op-level calls' single-CTA kernels on the current device
+ * (0 = the default, about two seconds); see gpt2_set_wait_limit. Creates the
+ * status word of the allocating op-level calls if it does not exist yet. */
+int gpt2_op_set_wait_limit(unsigned int cycles);
 
 /* Causal attention forward on a fused qkv buffer [B*T, 3C] (bf16 when
  * precision == GPT2_BF16, else fp32): out [B*T, C], lse fp32 [B, H, T]
@@ -327,6 +349,8 @@ int gpt2_op_attention_bwd(int precision, int B, int T, int H, int hs, const void
  *    call's contents (each call rewrites every row it reads, so no clearing is
  *    needed). Calls that may overlap on the GPU (different streams, no ordering
  *    between them) race on it: order them on one stream or with events.
+ *  - A bounded-wait expiry inside its kernels is recorded in a status word
+ *    that is also compiled into the library, and reported by gpt2_op_sync.
  * Return codes as gpt2_op_attention_bwd. */
 int gpt2_op_attention_bwd_noalloc(int precision, int B, int T, int H, int hs, const void* qkv,
                                   const void* out, const float* lse, const void* dout,

@@ -152,23 +152,84 @@ def test_gpt2_124m_bf16_one_step_batch2():
     _pad_rows_zero(r)
 
 
+@pytest.mark.slow
 def test_char_bf16_loss_trajectory():
-    """Several AdamW steps at lr 1e-3 on fresh batches: the loss curve tracks
-    the oracle's."""
-    c = oracle_cfg(CONFIGS["char"], batch_size=4, n_layer=2)
+    """The character model of the pages' configuration (6 layers, 6 heads,
+    d=384, T=256, Markov-chain tokens) at B=16, 20 AdamW steps at lr 1e-3 on
+    fresh batches: the library's loss at every step stays within 5e-3
+    relative of the oracle's (fp64) loss at the same step."""
+    c = oracle_cfg(CONFIGS["char"], batch_size=16)
     m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_BF16), seed=3)
     tr = O.Trainer(c, 3)
-    for step in range(6):
+    worst = 0.0
+    for step in range(20):
         x, y = synthdata.markov_batch(65, c.batch_size, c.seq_len, 100 + step)
         m.zero_grad()
         tr.zero_grad()
         loss = m.forward(dev(x), dev(y))
         lo, _ = tr.forward(x, y)
-        assert abs(loss - lo) / lo < 5e-3 * (1 + step), (step, loss, lo)
+        rel = abs(loss - lo) / lo
+        worst = max(worst, rel)
+        assert rel < 5e-3, (step, loss, lo)
         m.backward()
         tr.backward()
         m.step(lr=1e-3)
         tr.step(lr=1e-3)
+    print(f"char bf16 20-step trajectory: worst relative loss difference {worst:.2e}")
+
+
+@pytest.mark.slow
+def test_gpt2_width_full_batch_bf16_gradients():
+    """The benchmark's batch shape (B=16, T=1024: 16,384 rows) at GPT-2 width
+    and full vocabulary with two layers: every gradient against the oracle.
+    Reaches the row-count-dependent paths at full size: cross-entropy over
+    16,384 rows of 50,304 columns, the token sort of the embedding backward
+    with the Zipf-hot ids, the attention work lists of 16 x 12 heads."""
+    c = oracle_cfg(CONFIGS["gpt2_124m"], n_layer=2)
+    r = _compare_step(c, gpt2.GPT2_BF16, "zipf", lr=6e-4)
+    _check_bf16(r)
+    _pad_rows_zero(r)
+
+
+@pytest.mark.slow
+def test_gpt2_medium_width_bf16_one_step():
+    """The 24-layer configuration's widths (d=1024, 16 heads of 64, MLP 4096,
+    vocabulary 50304) with two layers at B=2, T=1024: one full step."""
+    c = oracle_cfg(CONFIGS["gpt2_24l_1024d"], n_layer=2, batch_size=2)
+    r = _compare_step(c, gpt2.GPT2_BF16, "zipf", lr=6e-4)
+    _check_bf16(r)
+    _pad_rows_zero(r)
+
+
+@pytest.mark.parametrize("precision", [gpt2.GPT2_FP32, gpt2.GPT2_BF16])
+def test_grad_accumulation_matches_the_oracle(precision):
+    """Four micro-steps of B=2 with grad_accum_steps=4 (sotaaz Section 3:
+    each micro-batch loss divided by the micro-batch count; gradients add up
+    across backward calls) against the oracle's Trainer over the same four
+    micro-batches: accumulated gradients, the clipped norm and the update."""
+    base = oracle_cfg(CONFIGS["char"], n_layer=2, batch_size=2, grad_accum_steps=4)
+    m = gpt2.GPT2(gpu_cfg(base, precision), seed=8)
+    tr = O.Trainer(base, 8)
+    for i in range(4):
+        x, y = synthdata.markov_batch(65, base.batch_size, base.seq_len, 300 + i)
+        loss = m.forward(dev(x), dev(y))
+        lo, _ = tr.forward(x, y)
+        assert abs(loss - lo) / lo < (1e-4 if precision == gpt2.GPT2_FP32 else 5e-3), (i, loss, lo)
+        m.backward()
+        tr.backward()
+    g_gpu = m.state(gpt2.GPT2_GRAD)
+    g_orc = {n: a.copy() for n, a in tr.grads.items()}
+    p0 = {n: a.copy() for n, a in tr.params.items()}
+    norm = m.step(lr=1e-3)
+    tn = tr.step(lr=1e-3)
+    r = dict(loss=(loss, lo), norm=(norm, tn), g_gpu=g_gpu, g_orc=g_orc,
+             p_gpu=m.state(gpt2.GPT2_PARAM), p_orc=tr.params, V=base.vocab_size,
+             p_iso=oracle_adamw_on(p0, g_gpu, 1e-3))
+    if precision == gpt2.GPT2_FP32:
+        _check_fp32(r)
+    else:
+        _check_bf16(r)
+    _pad_rows_zero(r)
 
 
 def test_fp32_consecutive_steps_track_the_oracle():

@@ -18,8 +18,6 @@ import pytest
 
 from decoder_only_transformer_06_b300 import gpt2
 
-from gpu_helpers import rel_l2
-
 
 def _inputs(B, T, H, hs, seed, dtype):
     import torch
@@ -50,13 +48,49 @@ def _run(precision, B, T, H, hs, seed):
 @pytest.mark.gpu
 @pytest.mark.parametrize("precision", [gpt2.GPT2_BF16, gpt2.GPT2_FP32])
 def test_noalloc_attention_bwd_matches_the_allocating_entry_point(precision):
-    # two calls in a row on one device: a larger case, then a smaller ragged one
+    # two calls in a row on one device: a larger case, then a smaller ragged
+    # one; both entry points run the same kernels on the same inputs, so the
+    # outputs must be identical bit for bit
     for B, T, H, seed in ((4, 512, 3, 11), (2, 200, 2, 12)):
         got, ref = _run(precision, B, T, H, 64, seed)
         assert np.all(np.isfinite(got))
-        # the same kernels on the same inputs; the bound is the fp32 attention
-        # parity tolerance of the kernel tests
-        assert rel_l2(got, ref) <= 1e-5, (precision, B, T, H)
+        assert np.array_equal(got, ref), (precision, B, T, H)
+
+
+@pytest.mark.gpu
+def test_noalloc_attention_bwd_fills_its_scratch_to_the_limit():
+    """B*H*T exactly 2^20 rows: the last row of the fixed array is used."""
+    got, ref = _run(gpt2.GPT2_BF16, 1024, 1024, 1, 64, 13)
+    assert np.all(np.isfinite(got))
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.gpu
+def test_noalloc_attention_bwd_reports_an_expired_wait():
+    """The allocation-free path's kernels record a bounded-wait expiry in the
+    library's fixed status word; gpt2_op_sync reports it as ETIMEOUT (and
+    allocates nothing to do so). With the default limit back, the next call is
+    bit-identical to the allocating entry point."""
+    import torch
+    B, T, H, hs = 2, 512, 2, 64
+    qkv, dout = _inputs(B, T, H, hs, 14, torch.bfloat16)
+    C = H * hs
+    out = torch.empty(B * T, C, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
+    gpt2.op_attention_fwd(gpt2.GPT2_BF16, B, T, H, hs, qkv, out, lse)
+    got = torch.empty(B * T, 3 * C, dtype=torch.bfloat16, device="cuda")
+    gpt2.op_sync()
+    gpt2.op_set_wait_limit(200)
+    try:
+        gpt2.op_attention_bwd_noalloc(gpt2.GPT2_BF16, B, T, H, hs, qkv, out, lse, dout, got)
+        with pytest.raises(gpt2.GPT2Error) as e:
+            gpt2.op_sync()
+        assert e.value.code == gpt2.GPT2_ETIMEOUT
+    finally:
+        gpt2.op_set_wait_limit(0)
+    gpt2.op_sync()                      # the report cleared the status
+    got2, ref = _run(gpt2.GPT2_BF16, B, T, H, hs, 14)
+    assert np.array_equal(got2, ref)
 
 
 def test_noalloc_attention_bwd_rejects_sizes_beyond_its_scratch():
