@@ -156,26 +156,64 @@ def test_gpt2_124m_bf16_one_step_batch2():
 def test_char_bf16_loss_trajectory():
     """The character model of the pages' configuration (6 layers, 6 heads,
     d=384, T=256, Markov-chain tokens) at B=16, 20 AdamW steps at lr 1e-3 on
-    fresh batches: the library's loss at every step stays within 5e-3
-    relative of the oracle's (fp64) loss at the same step."""
+    fresh batches, every step checked on the same parameters: before each step
+    the oracle takes the library's current parameters, so the library's loss
+    is held to the stated one-step bound (5e-3 relative) at each of 20 points
+    along its own bf16 trajectory, its gradients to the bf16 gradient bounds
+    (every fifth step), and its clip + AdamW update, given its own gradients
+    and moments, to the oracle's update of them within 1e-6.
+
+    A free-running fp64 run from the same init is compared too, but only
+    reported: the two runs separate step by step (an Adam step moves every
+    element by about lr whatever |g|, so elements whose tiny gradient differs
+    in sign move apart by 2 lr per step; measured on B300 the curves differ by
+    about 6% after 17 steps), so the one-step bound does not apply to them."""
     c = oracle_cfg(CONFIGS["char"], batch_size=16)
     m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_BF16), seed=3)
-    tr = O.Trainer(c, 3)
-    worst = 0.0
+    synced = O.Trainer(c, 3)         # re-synced to the library's parameters each step
+    free = O.Trainer(c, 3)           # free-running fp64 trajectory (reported only)
+    worst_step, worst_curve = 0.0, 0.0
     for step in range(20):
         x, y = synthdata.markov_batch(65, c.batch_size, c.seq_len, 100 + step)
+        p0 = m.state(gpt2.GPT2_PARAM)
+        for n in synced.params:
+            synced.params[n] = p0[n].astype(np.float64)
         m.zero_grad()
-        tr.zero_grad()
+        synced.zero_grad()
+        free.zero_grad()
         loss = m.forward(dev(x), dev(y))
-        lo, _ = tr.forward(x, y)
+        lo, _ = synced.forward(x, y)
+        lf, _ = free.forward(x, y)
         rel = abs(loss - lo) / lo
-        worst = max(worst, rel)
+        worst_step = max(worst_step, rel)
         assert rel < 5e-3, (step, loss, lo)
+        worst_curve = max(worst_curve, abs(loss - lf) / lf)
         m.backward()
-        tr.backward()
+        synced.backward()
+        free.backward()
+        g = m.state(gpt2.GPT2_GRAD)
+        if step % 5 == 4:
+            for n, ref in synced.grads.items():
+                if not np.any(ref):
+                    continue
+                e, cs = rel_l2(g[n], ref), cosine(g[n], ref)
+                assert e <= 2e-2 and cs >= 0.999, (step, n, e, cs)
+        mom = (m.state(gpt2.GPT2_ADAM_M), m.state(gpt2.GPT2_ADAM_V))
         m.step(lr=1e-3)
-        tr.step(lr=1e-3)
-    print(f"char bf16 20-step trajectory: worst relative loss difference {worst:.2e}")
+        free.step(lr=1e-3)
+        # the library's update in isolation: the oracle's clip + AdamW (step
+        # t = step + 1) applied to the library's gradients and moments
+        p1 = m.state(gpt2.GPT2_PARAM)
+        gg = {n: a.astype(np.float64) for n, a in g.items()}
+        O.clip_grads(gg, 1.0)
+        for n in p1:
+            ref = p0[n].astype(np.float64)
+            mm, vv = mom[0][n].astype(np.float64), mom[1][n].astype(np.float64)
+            O.adamw_update(ref, gg[n], mm, vv, step + 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, ref.ndim >= 2)
+            d = float(np.abs(p1[n] - ref).max())
+            assert d < 1e-6, (step, n, d)
+    print(f"char bf16 20 steps: worst same-parameter loss difference {worst_step:.2e}; "
+          f"free-running curves differ by up to {worst_curve:.2e}")
 
 
 @pytest.mark.slow
