@@ -88,6 +88,7 @@ struct gpt2_model {
     float* rsf = nullptr;
     void* logits = nullptr;
     float* row_loss = nullptr;
+    float* last_logits = nullptr;   // fp32 [B, Vp]: the head on one position per sequence
 
     float* dres = nullptr;
     void* dres_act = nullptr;
@@ -381,6 +382,7 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     ALLOC(m, m->rsf, M * 4);
     ALLOC(m, m->logits, M * (size_t)m->Vp * A);
     ALLOC(m, m->row_loss, M * 4);
+    ALLOC(m, m->last_logits, (size_t)m->B * m->Vp * 4);
 
     ALLOC(m, m->dres, M * C * 4);
     if (m->use_bf16) ALLOC(m, m->dres_act, M * C * A);
@@ -593,8 +595,10 @@ static double attn_flops(const gpt2_model* m, int products) {
     return 2.0 * products * pairs * m->hs * (double)m->B * m->H;
 }
 
+// last_t > 0: generation's forward, the LM head only on position last_t - 1 of
+// every sequence, into m->last_logits (no loss).
 template <typename Act>
-static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
+static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt, int last_t = 0) {
     cudaStream_t s = m->stream;
     const int M = m->M, C = m->C, L = m->L, T = m->T, B = m->B, H = m->H;
     const double A = m->act_bytes, MC = (double)M * C;
@@ -655,6 +659,13 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt) {
     RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
         k::layernorm_fwd<Act>(m->la[L - 1].x_mid, (const Act*)m->yproj, m->x_final, m->P(m->lnf_g()),
                               m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf, m->rsf, M, C, s));
+    if (last_t > 0) {
+        // the tied head on one position per sequence: rows b*T + last_t - 1 of uf
+        const void* a = (const char*)m->uf + (size_t)(last_t - 1) * C * m->act_bytes;
+        GemmEpi e{EPI_STORE_F32, nullptr, m->last_logits, m->Vp, nullptr, 0, nullptr, 0};
+        OPR(op.gemm("gemm_lmhead_last", B, m->Vp, C, {a, (int64_t)T * C, true}, {m->W(0), C, true}, e));
+        return GPT2_OK;
+    }
     {
         // tied LM head: logits = uf wte^T over all Vp rows of wte (pad columns
         // are masked by the cross-entropy)
@@ -869,6 +880,19 @@ int gpt2_forward(gpt2_model* m, const int32_t* tok, const int32_t* tgt, float* h
         if (!tgt) return fail(m, GPT2_EINVAL, "h_loss requested without targets");
         return gpt2_get_loss(m, h_loss);
     }
+    return GPT2_OK;
+}
+
+int gpt2_forward_last(gpt2_model* m, const int32_t* tok, int t, float* d_logits) {
+    if (!m) return GPT2_EINVAL;
+    if (!tok || !d_logits) return fail(m, GPT2_EINVAL, "tokens or logits pointer is NULL");
+    if (t < 1 || t > m->T) return fail(m, GPT2_EINVAL, "t must be in [1, seq_len]");
+    m->have_targets = false;
+    int r = m->use_bf16 ? forward_impl<bf16>(m, tok, nullptr, t) : forward_impl<float>(m, tok, nullptr, t);
+    if (r) return r;
+    m->last_tok = tok;
+    CK(m, cudaMemcpy2DAsync(d_logits, (size_t)m->V * 4, m->last_logits, (size_t)m->Vp * 4, (size_t)m->V * 4,
+                            (size_t)m->B, cudaMemcpyDeviceToDevice, m->stream));
     return GPT2_OK;
 }
 
@@ -1388,6 +1412,18 @@ int gpt2_op_set_wait_limit(unsigned int cycles) {
                        cudaMemcpyHostToDevice);
         if (r != cudaSuccess) return fail_cuda(nullptr, "wait limit write", r);
     }
+    return GPT2_OK;
+}
+
+int gpt2_op_sample(const float* logits, int rows, int V, int64_t ld, float temperature, int top_k,
+                   const float* u, int32_t* out, int32_t* ctx, int T, int t, void* stream) {
+    if (!logits || !u || !out || rows <= 0 || V <= 0 || ld < V)
+        return fail(nullptr, GPT2_EINVAL, "bad sampling arguments");
+    if (ctx && (T < 1 || T > 1024 || t < 1 || t > T))
+        return fail(nullptr, GPT2_EINVAL, "context must have 1 <= t <= T <= 1024");
+    cudaError_t r = k::sample(logits, rows, V, ld, temperature, top_k, u, out, ctx, T, t,
+                              (cudaStream_t)stream);
+    if (r != cudaSuccess) return fail_cuda(nullptr, "sample", r);
     return GPT2_OK;
 }
 

@@ -172,6 +172,12 @@ cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int 
                           DevState* st, cudaStream_t s);
 cudaError_t loss_reduce(const float* row_loss, int M, DevState* st, cudaStream_t s);
 
+// One sampling step per row of logits (temperature, top-k keeping ties, softmax,
+// inverse-CDF draw from u[row]); ctx (optional, int32 [rows, T], t valid
+// tokens per row) receives the token at position t, or shifted in at T-1.
+cudaError_t sample(const float* logits, int rows, int V, int64_t ld, float temperature, int top_k,
+                   const float* u, int32_t* out, int32_t* ctx, int T, int t, cudaStream_t s);
+
 cudaError_t grad_norm(const float* g, int64_t n, double* partial, int nparts, cudaStream_t s);
 cudaError_t step_finalize(const double* partial, int nparts, float clip, float beta1, float beta2,
                           DevState* st, cudaStream_t s);

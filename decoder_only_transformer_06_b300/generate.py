@@ -1,75 +1,74 @@
-"""Sampling from a trained model, as the pages' generate loop does it ("Let's
-reproduce GPT-2", the sampling loop; nanoGPT guide, sample.py): crop the
-context to the block size, take the logits of the last position, divide by the
-temperature, keep the top k, softmax, draw one token, append, repeat. There is
-no KV cache: every new token runs the forward again on the whole context.
+"""Sampling from a trained model on the GPU, as the pages' generate loop does it
+("Let's reproduce GPT-2", 00:37:02 the sampling loop; nanoGPT guide, sample.py):
+crop the context to the block size, take the logits of the last position,
+divide by the temperature, keep the top k, softmax, draw one token, append,
+repeat. There is no KV cache: every new token runs the forward again on the
+whole context.
 
-The loop takes a `last_logits(ctx)` callable (ctx: int [B', t] -> float
-[B', V], the logits of position t-1 of each row), so that one loop serves the
-library (`library_last_logits`) and any other model of the same method.
-Randomness: one numpy Generator seeded by the caller, one uniform draw per row
-per token.
+Every step runs in the library: gpt2_forward_last (the blocks on the [B, T]
+context, the LM head on position t-1 only) and gpt2_op_sample (temperature,
+top-k, softmax, inverse-CDF draw, and the append to the context, shifting it
+left once it holds T tokens). The host only draws the uniforms the sampler
+consumes and copies the new tokens back at the end.
+
+Uniforms: u[step, row] = the top 24 bits of output number step*B + row of a
+SplitMix64 stream (Steele, Lea & Flood, OOPSLA 2014) started at the seed,
+times 2^-24 (exact in fp32, in [0, 1)). Callers may pass their own instead.
 """
+from __future__ import annotations
+
 import numpy as np
 
-
-def sample_next(logits, temperature, top_k, rng):
-    """One token per row from logits [B, V]: z = logits / temperature; with
-    top_k, entries below the k-th largest of the row become -inf; p =
-    softmax(z); the token is the first index whose cumulative p exceeds a
-    uniform draw (the pages' topk mask keeps ties with the k-th value too)."""
-    if temperature <= 0:
-        raise ValueError("temperature must be > 0")
-    z = np.asarray(logits, dtype=np.float64) / temperature
-    if z.ndim != 2:
-        raise ValueError("logits must be [B, V]")
-    V = z.shape[1]
-    if top_k is not None and 0 < top_k < V:
-        kth = np.partition(z, V - top_k, axis=1)[:, V - top_k][:, None]
-        z = np.where(z < kth, -np.inf, z)
-    z = z - z.max(axis=1, keepdims=True)
-    p = np.exp(z)
-    p /= p.sum(axis=1, keepdims=True)
-    cdf = np.cumsum(p, axis=1)
-    u = rng.random(z.shape[0])
-    j = (cdf <= u[:, None]).sum(axis=1)
-    # a draw above the rounded total falls to the last token that can be drawn
-    last = V - 1 - np.argmax(p[:, ::-1] > 0, axis=1)
-    return np.where(j >= V, last, j).astype(np.int64)
+_GAMMA = 0x9E3779B97F4A7C15
+_MASK = (1 << 64) - 1
 
 
-def generate(last_logits, prompt, max_new_tokens, block_size, temperature=1.0, top_k=None, seed=0):
-    """Extend every row of `prompt` (int [B, t0], t0 >= 1) by max_new_tokens
-    sampled tokens; returns int64 [B, t0 + max_new_tokens]."""
-    idx = np.asarray(prompt, dtype=np.int64)
-    if idx.ndim != 2 or idx.shape[1] < 1:
-        raise ValueError("prompt must be [B, t0] with t0 >= 1")
-    rng = np.random.default_rng(seed)
-    for _ in range(max_new_tokens):
-        ctx = idx[:, -block_size:]
-        nxt = sample_next(last_logits(ctx), temperature, top_k, rng)
-        idx = np.concatenate([idx, nxt[:, None]], axis=1)
-    return idx
+def draw_uniforms(seed: int, step: int, rows: int) -> np.ndarray:
+    """fp32 [rows]: u for one generation step (see the module docstring)."""
+    out = np.empty(rows, dtype=np.float32)
+    for r in range(rows):
+        z = (seed + (step * rows + r + 1) * _GAMMA) & _MASK
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK
+        z ^= z >> 31
+        out[r] = (z >> 40) * (2.0 ** -24)
+    return out
 
 
-def library_last_logits(model):
-    """`last_logits` for a gpt2.GPT2 model of batch B and sequence length T.
-    The context (B' <= B rows of t <= T tokens) is padded with token 0 to
-    [B, T]: causal attention makes the logits of position t-1 independent of
-    the padding. One forward (without targets) per call; the logits of the
-    rows' positions t-1 are copied back. Use block_size = T with it."""
+def generate(model, prompt, max_new_tokens, temperature=1.0, top_k=None, seed=0, uniforms=None):
+    """Extend every row of `prompt` (int [b, t0], b <= B, t0 >= 1) by
+    max_new_tokens tokens sampled by the library's model (a gpt2.GPT2 of batch
+    B and sequence length T, the block size of the loop). temperature <= 0
+    decodes greedily. uniforms: optional fp32 [max_new_tokens, B] to use
+    instead of the seeded draws. Returns int64 [b, t0 + max_new_tokens]."""
     import torch
+    from . import gpt2
 
-    B, T = model.cfg.batch_size, model.cfg.seq_len
-
-    def last_logits(ctx):
-        ctx = np.asarray(ctx)
-        b, t = ctx.shape
-        if b > B or t > T or t < 1:
-            raise ValueError(f"context {ctx.shape} does not fit the model's [{B}, {T}]")
-        buf = np.zeros((B, T), dtype=np.int32)
-        buf[:b, :t] = ctx
-        model.forward(torch.from_numpy(buf.reshape(-1)).cuda())
-        return np.stack([model.logits(r * T + t - 1, 1)[0] for r in range(b)])
-
-    return last_logits
+    idx = np.asarray(prompt, dtype=np.int64)
+    B, T, V = model.cfg.batch_size, model.cfg.seq_len, model.cfg.vocab_size
+    if idx.ndim != 2 or idx.shape[1] < 1 or idx.shape[0] > B:
+        raise ValueError(f"prompt must be [b <= {B}, t0 >= 1]")
+    b, t0 = idx.shape
+    if uniforms is not None:
+        uniforms = np.asarray(uniforms, dtype=np.float32)
+        if uniforms.shape != (max_new_tokens, B):
+            raise ValueError(f"uniforms must be [{max_new_tokens}, {B}]")
+    t = min(t0, T)
+    ctx = np.zeros((B, T), dtype=np.int32)
+    ctx[:b, :t] = idx[:, t0 - t:]
+    stream = model.stream
+    with torch.cuda.stream(stream):
+        d_ctx = torch.from_numpy(ctx).cuda()
+        d_logits = torch.empty(B, V, dtype=torch.float32, device="cuda")
+        d_new = torch.empty(max_new_tokens, B, dtype=torch.int32, device="cuda")
+        u_all = uniforms if uniforms is not None else np.stack(
+            [draw_uniforms(seed, s, B) for s in range(max_new_tokens)]) if max_new_tokens else \
+            np.zeros((0, B), np.float32)
+        d_u = torch.from_numpy(np.ascontiguousarray(u_all)).cuda()
+        for s in range(max_new_tokens):
+            model.forward_last(d_ctx.view(-1), t, d_logits)
+            gpt2.op_sample(d_logits, temperature, top_k, d_u[s], d_new[s], ctx=d_ctx, t=t,
+                           stream=stream)
+            t = min(t + 1, T)
+        new = d_new.cpu().numpy()
+    return np.concatenate([idx, new[:, :b].T.astype(np.int64)], axis=1)

@@ -60,6 +60,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_set_stream": (I, [P, P]),
         "gpt2_forward": (I, [P, P, P, FP]),
         "gpt2_backward": (I, [P]),
+        "gpt2_forward_last": (I, [P, P, I, P]),
         "gpt2_step": (I, [P, F, F, F, F, F, F, FP]),
         "gpt2_zero_grad": (I, [P]),
         "gpt2_lr_schedule": (D, [I64, I64, I64, D, D]),
@@ -89,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_op_gemm_bf16_gelu": (I, [I, I, I, P, I64, I, P, I64, I, P, I, P, P, I64, P]),
         "gpt2_op_sync": (I, [P]),
         "gpt2_op_set_wait_limit": (I, [ctypes.c_uint]),
+        "gpt2_op_sample": (I, [P, I, I, I64, F, I, P, P, P, I, I, P]),
         "gpt2_op_attention_fwd": (I, [I, I, I, I, I, P, P, P, P]),
         "gpt2_op_attention_bwd": (I, [I, I, I, I, I, P, P, P, P, P, P, P]),
         "gpt2_op_attention_bwd_noalloc": (I, [I, I, I, I, I, P, P, P, P, P, P]),
@@ -169,6 +171,7 @@ class GPT2:
         h = ctypes.c_void_p()
         _check(_lib.gpt2_create(ctypes.byref(self._c), seed, ctypes.byref(h)))
         self.h = h
+        self.stream = None           # the legacy default stream until set_stream
         if stream is not None:
             self.set_stream(stream)
         self._info = [self.tensor_info(i) for i in range(self.num_tensors())]
@@ -190,6 +193,7 @@ class GPT2:
 
     def set_stream(self, stream):
         self._ck(_lib.gpt2_set_stream(self.h, _stream_ptr(stream)))
+        self.stream = stream
 
     def forward(self, tokens, targets=None, sync_loss: bool = True):
         """tokens, targets: int32 CUDA tensors [B*T] (or [B, T]). Returns the
@@ -200,6 +204,13 @@ class GPT2:
                                    ctypes.c_void_p(targets.data_ptr()) if targets is not None else None,
                                    ctypes.byref(loss) if want else None))
         return loss.value if want else None
+
+    def forward_last(self, tokens, t: int, logits_out):
+        """Generation's forward: logits of position t-1 of each of the B
+        sequences into logits_out (fp32 CUDA tensor [B, V]); tokens: int32 CUDA
+        tensor [B*T] (positions >= t are ignored by causality)."""
+        self._ck(_lib.gpt2_forward_last(self.h, ctypes.c_void_p(tokens.data_ptr()), int(t),
+                                        ctypes.c_void_p(logits_out.data_ptr())))
 
     def backward(self):
         self._ck(_lib.gpt2_backward(self.h))
@@ -334,6 +345,19 @@ def op_sync(stream=None):
     """Synchronise the stream; raise GPT2Error(ETIMEOUT) if a bounded device
     wait expired in an op-level call since the last op_sync."""
     _check(_lib.gpt2_op_sync(_stream_ptr(stream)))
+
+
+def op_sample(logits, temperature, top_k, u, out, ctx=None, t=0, stream=None):
+    """One sampling step on the device (gpt2_op_sample): logits fp32 CUDA
+    [rows, V] (row-contiguous, stride V), u fp32 CUDA [rows] in [0, 1), out int32
+    CUDA [rows]; ctx (int32 CUDA [rows, T] with t tokens per row) receives the
+    token at position t, or shifted in at T-1 when t == T."""
+    rows, V = logits.shape
+    T = ctx.shape[1] if ctx is not None else 0
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr()) if x is not None else None
+    _check(_lib.gpt2_op_sample(ptr(logits), rows, V, logits.stride(0), float(temperature),
+                               int(top_k or 0), ptr(u), ptr(out), ptr(ctx), T, int(t),
+                               _stream_ptr(stream)))
 
 
 def op_set_wait_limit(cycles: int):

@@ -133,6 +133,21 @@ int gpt2_forward(gpt2_model* model, const int32_t* d_tokens, const int32_t* d_ta
                  float* h_loss);
 
 /*
+ * gpt2_forward_last -- the forward of generation ("Let's reproduce GPT-2",
+ * 00:37:02 the sampling loop; nanoGPT guide Deep dive 1, the LM head applied
+ * to the last position only at inference): the blocks run on the [B, T]
+ * context as in gpt2_forward, then the tied head on position t-1 of each
+ * sequence only. Positions t..T-1 may hold anything (causal attention keeps
+ * them out of position t-1).
+ *   d_tokens: device int32 [B*T] (the model's B and T); t in [1, T].
+ *   d_logits: device fp32 [B, V] row-major, caller-owned; receives the logits
+ *             of position t-1 of every sequence (real vocabulary only).
+ * No loss, no backward afterwards (ESTATE). Does not synchronise.
+ * Errors: EINVAL (NULL pointers, t outside [1, T]); ERANGE as gpt2_forward.
+ */
+int gpt2_forward_last(gpt2_model* model, const int32_t* d_tokens, int t, float* d_logits);
+
+/*
  * gpt2_backward -- gradient of (loss / grad_accum_steps) added (+=) into the
  * gradient buffers (nanoGPT guide Part IV Stage 4 "backward() accumulates
  * gradients"). Needs a preceding gpt2_forward with targets (else ESTATE).
@@ -317,6 +332,23 @@ int gpt2_op_sync(void* stream);
  * (0 = the default, about two seconds); see gpt2_set_wait_limit. Creates the
  * status word of the allocating op-level calls if it does not exist yet. */
 int gpt2_op_set_wait_limit(unsigned int cycles);
+
+/* One sampling step of generation ("Let's reproduce GPT-2", 00:37:02; nanoGPT
+ * guide, sample.py), per row r < rows of logits (device fp32, row stride ld
+ * >= V, V columns):
+ *   x = logits / temperature; with 0 < top_k < V only the entries >= the k-th
+ *   largest x are kept (ties with it too, as the pages' topk mask keeps them);
+ *   p = softmax over the kept entries; the token is the smallest j whose
+ *   cumulative p exceeds u[r] (device fp32, u in [0, 1), caller-drawn).
+ * temperature <= 0 takes the argmax (lowest index on ties) instead.
+ *   out: device int32 [rows] receives the tokens.
+ *   ctx: optional device int32 [rows, T] context holding t tokens per row
+ *        (1 <= t <= T <= 1024): the token is written at position t, or, when
+ *        t == T, the row shifts left by one and the token goes to T-1 (the
+ *        pages' crop of the context to the block size). NULL: no append.
+ * Deterministic (fixed-order reductions). Errors: EINVAL for bad sizes. */
+int gpt2_op_sample(const float* logits, int rows, int V, int64_t ld, float temperature, int top_k,
+                   const float* u, int32_t* out, int32_t* ctx, int T, int t, void* stream);
 
 /* Causal attention forward on a fused qkv buffer [B*T, 3C] (bf16 when
  * precision == GPT2_BF16, else fp32): out [B*T, C], lse fp32 [B, H, T]

@@ -14,7 +14,7 @@ from .gpt2_oracle import (  # noqa: F401
     Config, Trainer, adamw_update, attention_bwd, attention_fwd, backward,
     causal_lse, causal_softmax, clip_grads, decays, forward, gelu_tanh, gelu_tanh_grad,
     global_grad_norm, init_normals, init_params, layernorm_bwd, layernorm_fwd,
-    lr_schedule, num_params, param_shapes, zero_grads,
+    lr_schedule, num_params, param_shapes, sample_tokens, zero_grads,
 )
 
 # The five workloads the method is exercised on (tiny fp32 check, character

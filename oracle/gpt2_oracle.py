@@ -462,6 +462,33 @@ def lr_schedule(it: int, warmup: int, horizon: int, lr_max: float, lr_min: float
 
 
 # ----------------------------------------------------------------------------
+# generation: one sampling step
+# ----------------------------------------------------------------------------
+def sample_tokens(logits, temperature, top_k, u):
+    """One token per row of last-position logits [B, V] ("Let's reproduce
+    GPT-2" 00:37:02 the sampling loop; nanoGPT guide, sample.py): z = logits /
+    temperature; with 0 < top_k < V, entries below the k-th largest z become
+    -inf (the pages' topk mask keeps ties with the k-th value); p = softmax(z);
+    the token is the smallest j whose cumulative p exceeds the uniform u[row]
+    (inverse CDF). temperature <= 0 takes the argmax (lowest index on ties).
+    Returns int64 [B]."""
+    z = np.asarray(logits, dtype=np.float64)
+    if temperature <= 0:
+        return z.argmax(axis=1).astype(np.int64)
+    z = z / temperature
+    V = z.shape[1]
+    if top_k is not None and 0 < top_k < V:
+        kth = np.sort(z, axis=1)[:, V - top_k][:, None]
+        z = np.where(z < kth, -np.inf, z)
+    w = np.exp(z - z.max(axis=1, keepdims=True))
+    c = np.cumsum(w, axis=1)
+    target = np.asarray(u, dtype=np.float64) * c[:, -1]
+    j = (c <= target[:, None]).sum(axis=1)
+    last = V - 1 - np.argmax(w[:, ::-1] > 0, axis=1)
+    return np.where(j >= V, last, j).astype(np.int64)
+
+
+# ----------------------------------------------------------------------------
 # a training-state object mirroring the library's calls
 # ----------------------------------------------------------------------------
 @dataclass
