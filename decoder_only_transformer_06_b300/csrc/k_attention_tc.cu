@@ -7,48 +7,58 @@
 // softmax over key blocks: "Let's reproduce GPT-2" 02:00:18, Flash Attention).
 // Also writes lse = log sum_j exp(S_ij) per query for the backward.
 //
-// Work item = (128-query block, b, h); persistent CTAs, 192 threads:
-//   warps 0..3  softmax: one thread per query row (= its TMEM lane). Reads the
-//               row of S from TMEM, masks, tracks the running max, writes
-//               P = exp(S - max) in bf16 back to TMEM, where the P V product
-//               reads it as its A operand (keeping P out of shared memory,
-//               whose bandwidth the S and P V operand reads and the K/V
-//               copies already use up), rescales the O row in TMEM when the max grew
-//               by more than 2^8 (otherwise P may exceed 1 by up to 2^8, which
-//               the final division by the row sum absorbs exactly). The item's
-//               O / l leaves through a 4 KB shared-memory slab per warp and one
-//               TMA store (per-lane row stores cost 14% of the kernel).
-//   warp 4      TMA producer: Q once per item, then K and V of each block of
+// Work item = (128-query block, b, h); persistent CTAs, 384 threads:
+//   warps 0..7  softmax, two warps per query row: warp w reads TMEM lane
+//               quarter w % 4 (its 32 rows) and the key half hf = w / 4
+//               (columns 64 hf .. +63) of each 128-key block. Each half keeps
+//               its own running max m and row sum l and its own output
+//               accumulator O_hf (the online softmax of its keys), so the two
+//               warps of a row never wait for each other inside an item; at
+//               the item's end the halves combine exactly:
+//                 O = (O_0 2^(m_0 - M) + O_1 2^(m_1 - M)) / (l_0 2^(m_0 - M) + l_1 2^(m_1 - M)),
+//               M = max(m_0, m_1) (log2 units). P = exp(S - m) is written in
+//               bf16 over the warp's own, already read S columns in TMEM, where
+//               the P V product reads it as its A operand; a half rescales its
+//               O_hf when its max grew by more than 2^8 (otherwise P may exceed
+//               1 by up to 2^8, which the final division absorbs exactly).
+//   warp 8      TMA producer: Q once per item, then K and V of each block of
 //               128 keys into one slot of a three-slot ring.
-//   warp 5      allocates 512 TMEM columns (S double buffer, O double buffer,
-//               P double buffer); lane 0 issues S_j = Q K_j^T (M=128, N=128,
-//               K=64) into S[j%2].
-//   warp 6      lane 0 issues O += P_j V_j (M=128, N=64, K=128; A = P from
-//               TMEM), so the tensor core computes S_{j+1} and P_j V_j while
-//               the softmax works on S_{j+1}.
-// Every mbarrier wait is bounded; on expiry the CTA records ERR_TIMEOUT,
-// drains its copies and MMAs (bounded), frees TMEM and returns.
+//   warp 9      allocates 512 TMEM columns (S triple buffer, the two halves'
+//               O); lane 0 issues S_j = Q K_j^T (M=128, N=128, K=64) into
+//               S[j%3] once the P V products that read the P written over it
+//               are done.
+//   warps 10,11 lane 0 of warp 10 + hf issues O_hf += P_hf V_hf as soon as that
+//               half's P is in TMEM (M=128, N=64, K=64; A = P from TMEM): one
+//               issuing thread sustains about one tcgen05.mma per hundred
+//               cycles, so each half has its own. The tensor core computes
+//               S_{j+1}, S_{j+2} and P_j V_j while the softmax works on S_{j+1}.
+// The item's output leaves through a 4 KB shared-memory slab per row quarter
+// and one TMA store. Every mbarrier wait is bounded; on expiry the CTA records
+// ERR_TIMEOUT, drains its copies and MMAs (bounded), frees TMEM and returns.
 #include "attn_tc.cuh"
 
 namespace k {
 
 using namespace tc;
-
 using namespace attn;
 
 namespace {
 
 constexpr int AT_SLOTS = 3;                    // K and V ring depth
-constexpr int FW_THREADS = 224;                // forward: 4 softmax warps, producer, two MMA issuers
+constexpr int FW_THREADS = 384;                // forward: 8 softmax warps, producer, three MMA issuers
+constexpr int FW_PRODUCER = 8, FW_ISSUE_S = 9, FW_ISSUE_PV = 10;   // P V issuers: warps 10, 11
+constexpr int FW_SBUF = 3;                     // S buffers in TMEM
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
-constexpr int OFF_OUT = OFF_V + AT_SLOTS * AT_TILE;   // [4 softmax warps] O slabs
-constexpr int OFF_BAR = OFF_OUT + 4 * OUT_SLAB;
-constexpr size_t AT_SMEM = OFF_BAR + 256 + 1024;
-// forward TMEM columns: S[0] 0..127, S[1] 128..255, O[0] 256..319, O[1]
-// 320..383, P[0] 384..447, P[1] 448..511 (P: bf16 pairs, the A operand of P V)
-constexpr uint32_t TM_O = 256, TM_P = 384;
+constexpr int OFF_OUT = OFF_V + AT_SLOTS * AT_TILE;   // [4 row quarters] O slabs
+constexpr int OFF_ML = OFF_OUT + 4 * OUT_SLAB;        // [2 item buffers][128 rows] (m_1, l_1)
+constexpr int OFF_BAR = OFF_ML + 2 * 128 * 8;
+constexpr size_t AT_SMEM = OFF_BAR + 512 + 1024;
+// forward TMEM columns: S[i] 128 i .. 128 i + 127 for i < 3 (P of half hf in
+// bf16 pairs over columns 64 hf .. 64 hf + 31 of its S buffer), O_0 384..447,
+// O_1 448..511 (one item at a time)
+constexpr uint32_t TM_O = 384;
 constexpr uint32_t AT_TMEM_COLS = 512;
 
 }  // namespace
@@ -56,11 +66,8 @@ constexpr uint32_t AT_TMEM_COLS = 512;
 // Persistent: one CTA per SM walks work items w = blockIdx.x, +gridDim.x, ...
 // ordered heaviest first (query block qb = nqb-1 - w / (B*H)). Barrier phases
 // run on counters that every role advances identically: g counts key blocks
-// over all items (K/V ring slots, S and P buffers), `it` counts items (Q and O
-// double buffers), so the next item's Q, K and V load and its first S product
-// runs while the softmax warps finish the previous item. Two threads issue the
-// tensor-core work, one the S products and one the P V products, so that
-// neither chain of barrier waits delays the other.
+// over all items (K/V ring slots, S buffers), `it` counts items (Q double
+// buffer, the O accumulators, the (m, l) hand-off).
 __global__ void __launch_bounds__(FW_THREADS, 1)
 fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_out,
                  float* __restrict__ lse, int T, int H, int BH, DevState* st) {
@@ -69,18 +76,19 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
     uint8_t* sQ = smem + OFF_Q;
     uint8_t* sK = smem + OFF_K;
     uint8_t* sV = smem + OFF_V;
+    float2* sML = (float2*)(smem + OFF_ML);
     uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
     uint64_t* q_full = bars;           // [2]
     uint64_t* q_empty = bars + 2;      // [2]
     uint64_t* kv_full = bars + 4;      // [3] K and V block j
     uint64_t* kv_empty = bars + 7;     // [3]
-    uint64_t* s_full = bars + 10;      // [2]
-    uint64_t* s_empty = bars + 12;
-    uint64_t* p_full = bars + 14;
-    uint64_t* pv_done = bars + 16;
-    uint64_t* o_free = bars + 18;      // [2]
-    uint64_t* drain = bars + 20;       // [2] one per issuing thread
-    uint32_t* tmem_slot = (uint32_t*)(bars + 22);
+    uint64_t* s_full = bars + 10;      // [3]
+    uint64_t* p_full = bars + 13;      // [3 buffers][2 halves]
+    uint64_t* pv_done = bars + 19;     // [3] both halves' P V products of the block
+    uint64_t* o_free = bars + 22;      // the O accumulators have been read
+    uint64_t* ml_full = bars + 23;     // [2] the upper halves' (m, l) of an item are in smem
+    uint64_t* drain = bars + 25;       // [3] one per issuing thread
+    uint32_t* tmem_slot = (uint32_t*)(bars + 28);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
@@ -92,28 +100,31 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
         for (int i = 0; i < 2; i++) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
+            mbar_init(&ml_full[i], 4);
+        }
+        for (int i = 0; i < FW_SBUF; i++) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&pv_done[i], 1);
-            mbar_init(&o_free[i], 4);
+            mbar_init(&p_full[2 * i], 4);
+            mbar_init(&p_full[2 * i + 1], 4);
+            mbar_init(&pv_done[i], 2);
             mbar_init(&drain[i], 1);
         }
+        mbar_init(o_free, 4);
         for (int s = 0; s < AT_SLOTS; s++) {
             mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&kv_empty[s], 2);      // both P V issuers
         }
         abort_flag[0] = 0;
         abort_flag[1] = (int)wait_limit_of(st);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) tmem_alloc(tmem_slot, AT_TMEM_COLS);
+    if (warp == FW_ISSUE_S) tmem_alloc(tmem_slot, AT_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == FW_PRODUCER) {
         if (lane == 0) {
             // ---------------- TMA producer
             int g = 0, it = 0, nq = 0, nkv_l = 0;
@@ -143,7 +154,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                     wait_bounded(&kv_full[i % AT_SLOTS], (uint32_t)((i / AT_SLOTS) & 1));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == FW_ISSUE_S) {
         if (lane == 0) {
             // ---------------- S = Q K^T issuer
             constexpr uint32_t id_s = make_idesc(AT_BQ, AT_BK, false, false);
@@ -156,9 +167,11 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 const int qs = it & 1;
                 if (!mbar_wait(&q_full[qs], (uint32_t)((it >> 1) & 1), abort_flag)) { ok = false; break; }
                 for (int j = 0; j < nkv; j++) {
-                    const int G = g + j, s = G % AT_SLOTS, sb = G & 1;
+                    const int G = g + j, s = G % AT_SLOTS, sb = G % FW_SBUF;
                     if (!mbar_wait(&kv_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&s_empty[sb], (uint32_t)(((G >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                    // S[sb] is free once the P V products of three blocks ago (which read
+                    // the P written over it) are done
+                    if (!mbar_wait(&pv_done[sb], (uint32_t)(((G / FW_SBUF) & 1) ^ 1), abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t dq = desc_adv(dq0, qs * AT_TILE), dk = desc_adv(dk0, s * AT_TILE);
 #pragma unroll
@@ -176,29 +189,30 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 wait_bounded(&drain[0], 0);
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == FW_ISSUE_PV || warp == FW_ISSUE_PV + 1) {
         if (lane == 0) {
-            // ---------------- O += P V issuer (P read from TMEM, V MN-major)
+            // ---------------- O_hf += P_hf V_hf issuer, hf = warp - 10 (P from TMEM,
+            // V rows 64 hf .. +63 read MN-major)
+            const int hf = warp - FW_ISSUE_PV;
             constexpr uint32_t id_o = make_idesc(AT_BQ, AT_HS, false, true);
             const uint64_t dv0 = smem_desc(smem_u32(sV), 8192, 1024);
+            const uint32_t to = tmem_base + TM_O + 64 * hf;
             bool ok = true, any = false;
             int g = 0, it = 0;
             for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
                 const int qb = nqb - 1 - w / BH;
                 const int nkv = qb + 1;
-                const int ob = it & 1;
-                if (!mbar_wait(&o_free[ob], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag)) { ok = false; break; }
+                if (!mbar_wait(o_free, (uint32_t)((it & 1) ^ 1), abort_flag)) { ok = false; break; }
                 for (int j = 0; j < nkv; j++) {
-                    const int G = g + j, s = G % AT_SLOTS, pb = G & 1;
+                    const int G = g + j, s = G % AT_SLOTS, pb = G % FW_SBUF;
                     if (!mbar_wait(&kv_full[s], (uint32_t)((G / AT_SLOTS) & 1), abort_flag)) { ok = false; break; }
-                    if (!mbar_wait(&p_full[pb], (uint32_t)((G >> 1) & 1), abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&p_full[2 * pb + hf], (uint32_t)((G / FW_SBUF) & 1), abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t dv = desc_adv(dv0, s * AT_TILE);
-                    const uint32_t tp = tmem_base + TM_P + pb * (AT_BK / 2);
+                    const uint64_t dv = desc_adv(dv0, s * AT_TILE + hf * 8192);
+                    const uint32_t tp = tmem_base + pb * AT_BK + 64 * hf;
 #pragma unroll
-                    for (int kk = 0; kk < AT_BK / 16; kk++)
-                        mma_bf16_ta(tmem_base + TM_O + ob * AT_HS, tp + kk * 8, desc_adv(dv, kk * 2048), id_o,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16_ta(to, tp + kk * 8, desc_adv(dv, kk * 2048), id_o, (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&pv_done[pb]);
                     mma_commit(&kv_empty[s]);
                     any = true;
@@ -206,132 +220,148 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 g += nkv;
             }
             if (any) {
-                mma_commit(&drain[1]);
-                wait_bounded(&drain[1], 0);
+                mma_commit(&drain[1 + hf]);
+                wait_bounded(&drain[1 + hf], 0);
             }
         }
     } else {
-        // ---------------- softmax warps 0..3: thread r owns query row r (TMEM lane r)
-        const int r = threadIdx.x;
-        const float sl2 = 1.4426950408889634f * 0.125f;   // log2(e) / sqrt(64)
-        const uint32_t lane_base = tmem_base + ((uint32_t)(warp * 32) << 16);
-        uint8_t* slab = smem + OFF_OUT + warp * OUT_SLAB;
+        // ---------------- softmax warps 0..7: warp w owns rows r = 32 (w % 4) + lane
+        // (TMEM lane r) and the key half hf = w / 4 of every block
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = q4 * 32 + lane;
+        const float sl2 = LOG2E_F * 0.125f;   // log2(e) / sqrt(64)
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
+        uint8_t* slab = smem + OFF_OUT + q4 * OUT_SLAB;
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
             const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
             const int nkv = qb + 1;
             const int q = qb * AT_BQ + r;
-            const int ob = it & 1;
+            const int ob = it & 1;                 // the (m, l) hand-off buffer
+            const uint32_t o_half = lane_base + TM_O + 64 * hf;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < nkv; j++) {
-                const int G = g + j, sb = G & 1;
-                ok = mbar_wait(&s_full[sb], (uint32_t)((G >> 1) & 1), abort_flag);
+                const int G = g + j, sb = G % FW_SBUF;
+                ok = mbar_wait(&s_full[sb], (uint32_t)((G / FW_SBUF) & 1), abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t sr[128];
-#pragma unroll
-                for (int c = 0; c < 4; c++) tmem_ld32_nowait(lane_base + (uint32_t)(sb * AT_BK + 32 * c), sr + 32 * c);
+                uint32_t sr[64];
+                const uint32_t s_addr = lane_base + (uint32_t)(sb * AT_BK + 64 * hf);
+                tmem_ld32_nowait(s_addr, sr);
+                tmem_ld32_nowait(s_addr + 32, sr + 32);
                 tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
-                // mask (raw scores; the scale is applied in the exponent), row max
-                // as eight independent partial maxima
-                const int key0 = j * AT_BK;
-                const bool edge = (j == qb) || (key0 + AT_BK > T);
-                if (edge) {
+                // mask (raw scores; the scale is applied in the exponent), this half's max
+                const int key0 = j * AT_BK + 64 * hf;
+                if ((j == qb) || (key0 + 64 > T)) {
 #pragma unroll
-                    for (int i = 0; i < 128; i++)
+                    for (int i = 0; i < 64; i++)
                         if (key0 + i > q || key0 + i >= T) sr[i] = __float_as_uint(-INFINITY);
                 }
                 float pm[8];
 #pragma unroll
                 for (int t = 0; t < 8; t++) pm[t] = __uint_as_float(sr[t]);
 #pragma unroll
-                for (int i = 8; i < 120; i += 16)
+                for (int i = 8; i < 56; i += 16)
 #pragma unroll
                     for (int t = 0; t < 8; t++)
                         pm[t] = fmax3f(pm[t], __uint_as_float(sr[i + t]), __uint_as_float(sr[i + 8 + t]));
 #pragma unroll
-                for (int t = 0; t < 8; t++) pm[t] = fmaxf(pm[t], __uint_as_float(sr[120 + t]));
+                for (int t = 0; t < 8; t++) pm[t] = fmaxf(pm[t], __uint_as_float(sr[56 + t]));
                 const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                        fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sl2;
                 const float m_new = fmaxf(m_run, mx);
+                // a half whose keys were all masked so far keeps m = -inf, l = 0, O = 0
                 const bool resc = (j > 0) && (m_new > m_run + 8.f);
-                if (j == 0) m_run = m_new;
                 if (__any_sync(0xffffffffu, resc)) {
-                    // rescale the O row once the previous P V product has landed
-                    ok = mbar_wait(&pv_done[(G - 1) & 1], (uint32_t)(((G - 1) >> 1) & 1), abort_flag);
+                    // rescale O_hf once the previous block's P V products have landed
+                    ok = mbar_wait(&pv_done[(G - 1) % FW_SBUF], (uint32_t)(((G - 1) / FW_SBUF) & 1), abort_flag);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     tc_fence_after();
                     const float f = resc ? ex2f(m_run - m_new) : 1.f;
-                    const uint32_t oaddr = lane_base + TM_O + ob * AT_HS;
-                    uint32_t o[64];
-                    tmem_ld32_nowait(oaddr, o);
-                    tmem_ld32_nowait(oaddr + 32, o + 32);
-                    tmem_wait_ld();
+                    uint32_t o[32];
 #pragma unroll
-                    for (int i = 0; i < 64; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                    tmem_st32(oaddr, o);
-                    tmem_st32(oaddr + 32, o + 32);
+                    for (int c2 = 0; c2 < 2; c2++) {
+                        tmem_ld32(o_half + 32 * c2, o);
+#pragma unroll
+                        for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                        tmem_st32(o_half + 32 * c2, o);
+                    }
                     if (resc) {
                         l_run *= f;
                         m_run = m_new;
                     }
                 }
-                // the P buffer is free once the product that read it (two blocks ago) is done
-                if (G >= 2) {
-                    ok = mbar_wait(&pv_done[sb], (uint32_t)(((G - 2) >> 1) & 1), abort_flag);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    tc_fence_after();
-                }
+                if (j == 0) m_run = m_new;
+                const float msub = m_run == -INFINITY ? 0.f : m_run;   // all masked: exps of -inf are 0
                 float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                const uint32_t prow = lane_base + TM_P + sb * (AT_BK / 2);
+                uint32_t pk[32];                    // 64 probabilities as bf16 pairs
 #pragma unroll
-                for (int hf = 0; hf < 2; hf++) {
-                    uint32_t pk[32];                    // 64 probabilities as bf16 pairs
-#pragma unroll
-                    for (int c = 0; c < 32; c++) {
-                        const float e0 = ex2f(fmaf(__uint_as_float(sr[hf * 64 + 2 * c]), sl2, -m_run));
-                        const float e1 = ex2f(fmaf(__uint_as_float(sr[hf * 64 + 2 * c + 1]), sl2, -m_run));
-                        ps[(2 * c) & 7] += e0;
-                        ps[(2 * c + 1) & 7] += e1;
-                        pk[c] = pack2_bf16(e0, e1);
-                    }
-                    tmem_st32(prow + 32 * hf, pk);
+                for (int c = 0; c < 32; c++) {
+                    const float e0 = ex2f(fmaf(__uint_as_float(sr[2 * c]), sl2, -msub));
+                    const float e1 = ex2f(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -msub));
+                    ps[(2 * c) & 7] += e0;
+                    ps[(2 * c + 1) & 7] += e1;
+                    pk[c] = pack2_bf16(e0, e1);
                 }
+                // over this warp's own S columns, already in registers
+                tmem_st32(s_addr, pk);
                 l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[sb]);
+                if (lane == 0) mbar_arrive(&p_full[2 * sb + hf]);
             }
             if (!ok) break;
-            // the item's output: O / l and lse, once its last P V product is done
+            // the item's output once its last P V products are done
             const int GL = g + nkv - 1;
-            ok = mbar_wait(&pv_done[GL & 1], (uint32_t)((GL >> 1) & 1), abort_flag);
+            ok = mbar_wait(&pv_done[GL % FW_SBUF], (uint32_t)((GL / FW_SBUF) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t o[64];
-            tmem_ld32_nowait(lane_base + TM_O + ob * AT_HS, o);
-            tmem_ld32_nowait(lane_base + TM_O + ob * AT_HS + 32, o + 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&o_free[ob]);
-                tma_wait_read<0>();             // the previous item's store has read the slab
+            if (hf == 1) {
+                // hand this half's (m, l) to the lower half's warp of the same rows
+                sML[ob * 128 + r] = make_float2(m_run, l_run);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ml_full[ob]);
+            } else {
+                ok = mbar_wait(&ml_full[ob], (uint32_t)((it >> 1) & 1), abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const float2 ml1 = sML[ob * 128 + r];
+                const float M = fmaxf(m_run, ml1.x);
+                const float w0 = m_run == -INFINITY ? 0.f : ex2f(m_run - M);
+                const float w1 = ml1.x == -INFINITY ? 0.f : ex2f(ml1.x - M);
+                const float l_row = l_run * w0 + ml1.y * w1;
+                const float a0 = w0 / l_row, a1 = w1 / l_row;
+                tc_fence_after();
+                if (lane == 0) tma_wait_read<0>();           // the previous item's store has read the slab
+                __syncwarp();
+#pragma unroll 1
+                for (int c2 = 0; c2 < 4; c2++) {
+                    uint32_t o0[16], o1[16];
+                    tmem_ld16_nowait(lane_base + TM_O + 16 * c2, o0);
+                    tmem_ld16_nowait(lane_base + TM_O + 64 + 16 * c2, o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int pc = 0; pc < 2; pc++) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++)
+                            v[e] = __uint_as_float(o0[8 * pc + e]) * a0 + __uint_as_float(o1[8 * pc + e]) * a1;
+                        const int piece = 2 * c2 + pc;
+                        *(uint4*)(slab + lane * 128 + ((piece ^ (lane & 7)) << 4)) =
+                            make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
+                                       pack2_bf16(v[6], v[7]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tm_out, slab, h * AT_HS, qb * AT_BQ + q4 * 32, b);
+                    tma_commit();
+                }
+                if (q < T) lse[(int64_t)bh * T + q] = (M + log2f(l_row)) * LN2;
             }
-            __syncwarp();
-            // O / l through this warp's slab and one TMA store (rows beyond T clipped)
-            stage_out_slab(slab, lane, o, 1.f / l_run);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(&tm_out, slab, h * AT_HS, qb * AT_BQ + warp * 32, b);
-                tma_commit();
-            }
-            if (q < T) lse[(int64_t)bh * T + q] = (m_run + log2f(l_run)) * LN2;
             g += nkv;
         }
         if (lane == 0) tma_wait_all();
@@ -341,7 +371,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
         atomicOr(&st->err, ERR_TIMEOUT);
         st->timeout_site = 3;
     }
-    if (warp == 5) {
+    if (warp == FW_ISSUE_S) {
         tc_fence_after();
         tmem_dealloc(tmem_base, AT_TMEM_COLS);
     }
