@@ -239,9 +239,10 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- GPU arm
-def traffic_from_profiles(kernel_src: str):
-    """DRAM traffic per launch of the dominant kernel from the committed ncu
-    summary, if that summary was taken on the current kernel source."""
+def traffic_ratio_from_profiles(kernel_src: str):
+    """DRAM bytes per algorithmic byte of the dominant kernel, from the
+    committed ncu summary, if that summary was taken on the current kernel
+    source (single-kernel captures on a smaller case; see the file)."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_gpt2_124m_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -256,7 +257,7 @@ def traffic_from_profiles(kernel_src: str):
     if vals.get("kernel_source_sha256_16") != h:
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals["dram_to_algorithmic_ratio"])
     except (KeyError, ValueError):
         return None
 
@@ -379,8 +380,12 @@ def run_ours(args):
     g_launch = sum(r["calls"] for r in gemm)
     achieved_tf = g_flops / (g_ms / 1000.0) / 1e12 if g_ms > 0 else None
     total_ms = sum(r["ms"] for r in rep)
-    traffic = traffic_from_profiles(os.path.join(ROOT, "decoder_only_transformer_06_b300", "csrc",
-                                                 "k_gemm_tc.cu"))
+    # DRAM traffic per GEMM launch: the step's algorithmic GEMM bytes per launch
+    # times the DRAM/algorithmic ratio of the committed single-kernel capture
+    ratio = traffic_ratio_from_profiles(os.path.join(ROOT, "decoder_only_transformer_06_b300", "csrc",
+                                                     "k_gemm_tc.cu"))
+    g_bytes = sum(r["bytes"] for r in gemm)
+    traffic = ratio * g_bytes / g_launch if (ratio and g_launch) else None
     peak_tf, peak_src = tensor_peak(peaks, clk)
     roofline = {
         "bound": "tensor",
