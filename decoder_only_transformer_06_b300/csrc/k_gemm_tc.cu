@@ -67,18 +67,53 @@ __device__ __forceinline__ float tanh_hw(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Two fp32 values in one 64-bit register pair, for the packed fp32 pipe
+// (fma/mul/add .f32x2: one instruction does both lanes, each rounded as the
+// scalar instruction would be).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // gelu(x) = 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), and
-// gelu'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) du/dx from one tanh, written as
-// ten fp32 operations (the epilogue of the fc Linear is bound by them).
-__device__ __forceinline__ void gelu_and_grad_hw(float x, float& g, float& dg) {
+// gelu'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) du/dx from one tanh, for two
+// values at a time on the packed fp32 pipe (the epilogue of the fc Linear is
+// bound by these instructions):
+//   x2 = x*x, u = x (k0 + k1 x2), t = tanh(u), hx = x/2, g = hx t + hx,
+//   gelu' = (hx (t*t - 1)) (-(k0 + 3 k1 x2)) + (t/2 + 1/2).
+__device__ __forceinline__ void gelu_and_grad_x2(float& xa, float& xb, float& ga, float& gb) {
     const float k0 = 0.7978845608028654f;              // sqrt(2/pi)
     const float k1 = 0.7978845608028654f * 0.044715f;
-    const float x2 = x * x;
-    const float t = tanh_hw(x * fmaf(k1, x2, k0));
-    const float hx = 0.5f * x;
-    g = fmaf(hx, t, hx);
-    const float dudx = fmaf(3.0f * k1, x2, k0);
-    dg = fmaf(hx * fmaf(-t, t, 1.0f), dudx, fmaf(0.5f, t, 0.5f));
+    const uint64_t x = f2(xa, xb);
+    const uint64_t x2 = f2_mul(x, x);
+    float ua, ub;
+    f2_split(f2_mul(x, f2_fma(f2(k1, k1), x2, f2(k0, k0))), ua, ub);
+    const uint64_t t = f2(tanh_hw(ua), tanh_hw(ub));
+    const uint64_t half = f2(0.5f, 0.5f);
+    const uint64_t hx = f2_mul(half, x);
+    f2_split(f2_fma(hx, t, hx), ga, gb);
+    const uint64_t q = f2_mul(hx, f2_fma(t, t, f2(-1.0f, -1.0f)));
+    const uint64_t nd = f2_fma(f2(-3.0f * k1, -3.0f * k1), x2, f2(-k0, -k0));
+    f2_split(f2_fma(q, nd, f2_fma(half, t, half)), xa, xb);
 }
 
 // Staging tiles are laid out as the TMA expects them with swizzling, which
@@ -444,8 +479,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
                 float v[32];
+                if (bias != nullptr) {
 #pragma unroll
-                for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) + (bias != nullptr ? bv[j] : 0.f);
+                    for (int j = 0; j < 32; j += 2)
+                        f2_split(f2_add(f2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                        f2(bv[j], bv[j + 1])), v[j], v[j + 1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                }
                 if (KIND == EPI_GELU_BWD) {
                     const long q = a_used;
                     const int slot = (int)(q % NA);
@@ -455,7 +497,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     float dg[32];
                     unstage_bf16(aring + slot * 2048, lane, dg);
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] *= dg[j];
+                    for (int j = 0; j < 32; j += 2)
+                        f2_split(f2_mul(f2(v[j], v[j + 1]), f2(dg[j], dg[j + 1])), v[j], v[j + 1]);
                     __syncwarp();                        // every lane has read the slot
                     if (lane == 0) issue_aux();          // refill it NA chunks ahead
                 }
@@ -471,7 +514,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     // o1 = gelu'(pre) (saved for the backward), o2 = gelu(pre)
                     float g[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j++) gelu_and_grad_hw(v[j], g[j], v[j]);
+                    for (int j = 0; j < 32; j += 2) gelu_and_grad_x2(v[j], v[j + 1], g[j], g[j + 1]);
                     stage_bf16(sbuf, lane, v);
                     stage_bf16(sbuf + 2048, lane, g);
                 } else {
