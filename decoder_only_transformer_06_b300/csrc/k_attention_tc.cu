@@ -51,9 +51,9 @@ constexpr int FW_SBUF = 3;                     // S buffers in TMEM
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
-constexpr int OFF_OUT = OFF_V + AT_SLOTS * AT_TILE;   // [4 row quarters] O slabs
-constexpr int OFF_ML = OFF_OUT + 4 * OUT_SLAB;        // [2 item buffers][128 rows] (m_1, l_1)
-constexpr int OFF_BAR = OFF_ML + 2 * 128 * 8;
+constexpr int OFF_OUT = OFF_V + AT_SLOTS * AT_TILE;   // [4 row quarters][2 column halves] 2 KB O slabs
+constexpr int OFF_ML = OFF_OUT + 4 * OUT_SLAB;        // [2 item buffers][2 halves][128 rows] (m, l)
+constexpr int OFF_BAR = OFF_ML + 2 * 2 * 128 * 8;
 constexpr size_t AT_SMEM = OFF_BAR + 512 + 1024;
 // forward TMEM columns: S[i] 128 i .. 128 i + 127 for i < 3 (P of half hf in
 // bf16 pairs over columns 64 hf .. 64 hf + 31 of its S buffer), O_0 384..447,
@@ -86,7 +86,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
     uint64_t* p_full = bars + 13;      // [3 buffers][2 halves]
     uint64_t* pv_done = bars + 19;     // [3] both halves' P V products of the block
     uint64_t* o_free = bars + 22;      // the O accumulators have been read
-    uint64_t* ml_full = bars + 23;     // [2] the upper halves' (m, l) of an item are in smem
+    uint64_t* ml_full = bars + 23;     // [2] both halves' (m, l) of an item are in smem
     uint64_t* drain = bars + 25;       // [3] one per issuing thread
     uint32_t* tmem_slot = (uint32_t*)(bars + 28);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
@@ -100,7 +100,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
         for (int i = 0; i < 2; i++) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
-            mbar_init(&ml_full[i], 4);
+            mbar_init(&ml_full[i], 8);
         }
         for (int i = 0; i < FW_SBUF; i++) {
             mbar_init(&s_full[i], 1);
@@ -109,7 +109,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
             mbar_init(&pv_done[i], 2);
             mbar_init(&drain[i], 1);
         }
-        mbar_init(o_free, 4);
+        mbar_init(o_free, 8);
         for (int s = 0; s < AT_SLOTS; s++) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 2);      // both P V issuers
@@ -231,7 +231,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
         const int r = q4 * 32 + lane;
         const float sl2 = LOG2E_F * 0.125f;   // log2(e) / sqrt(64)
         const uint32_t lane_base = tmem_base + ((uint32_t)(q4 * 32) << 16);
-        uint8_t* slab = smem + OFF_OUT + q4 * OUT_SLAB;
+        uint8_t* slab = smem + OFF_OUT + q4 * OUT_SLAB + hf * (OUT_SLAB / 2);
         bool ok = true;
         int g = 0, it = 0;
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
@@ -294,19 +294,27 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 }
                 if (j == 0) m_run = m_new;
                 const float msub = m_run == -INFINITY ? 0.f : m_run;   // all masked: exps of -inf are 0
-                float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // exponents and partial sums two columns at a time on the packed
+                // fp32 pipe; ps[t] sums columns 2c, 2c+1 for c = t mod 4
+                uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t pk[32];                    // 64 probabilities as bf16 pairs
+                const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-msub, -msub);
 #pragma unroll
                 for (int c = 0; c < 32; c++) {
-                    const float e0 = ex2f(fmaf(__uint_as_float(sr[2 * c]), sl2, -msub));
-                    const float e1 = ex2f(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -msub));
-                    ps[(2 * c) & 7] += e0;
-                    ps[(2 * c + 1) & 7] += e1;
+                    float a0, a1;
+                    f2_split(f2_fma(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, nmx2),
+                             a0, a1);
+                    const float e0 = ex2f(a0), e1 = ex2f(a1);
+                    const uint64_t e = f2(e0, e1);
+                    ps[c & 3] = f2_add(ps[c & 3], e);
                     pk[c] = pack2_bf16(e0, e1);
                 }
                 // over this warp's own S columns, already in registers
                 tmem_st32(s_addr, pk);
-                l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                float psum[8];
+#pragma unroll
+                for (int t = 0; t < 4; t++) f2_split(ps[t], psum[2 * t], psum[2 * t + 1]);
+                l_run += ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[2 * sb + hf]);
@@ -316,28 +324,28 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
             const int GL = g + nkv - 1;
             ok = mbar_wait(&pv_done[GL % FW_SBUF], (uint32_t)((GL / FW_SBUF) & 1), abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            if (hf == 1) {
-                // hand this half's (m, l) to the lower half's warp of the same rows
-                sML[ob * 128 + r] = make_float2(m_run, l_run);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ml_full[ob]);
-            } else {
-                ok = mbar_wait(&ml_full[ob], (uint32_t)((it >> 1) & 1), abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                const float2 ml1 = sML[ob * 128 + r];
-                const float M = fmaxf(m_run, ml1.x);
-                const float w0 = m_run == -INFINITY ? 0.f : ex2f(m_run - M);
+            // the two halves exchange (m, l); each then writes output columns
+            // 32 hf .. 32 hf + 31 of its rows from both O halves
+            sML[(ob * 2 + hf) * 128 + r] = make_float2(m_run, l_run);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ml_full[ob]);
+            ok = mbar_wait(&ml_full[ob], (uint32_t)((it >> 1) & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            {
+                const float2 ml0 = sML[(ob * 2) * 128 + r], ml1 = sML[(ob * 2 + 1) * 128 + r];
+                const float M = fmaxf(ml0.x, ml1.x);
+                const float w0 = ml0.x == -INFINITY ? 0.f : ex2f(ml0.x - M);
                 const float w1 = ml1.x == -INFINITY ? 0.f : ex2f(ml1.x - M);
-                const float l_row = l_run * w0 + ml1.y * w1;
+                const float l_row = ml0.y * w0 + ml1.y * w1;
                 const float a0 = w0 / l_row, a1 = w1 / l_row;
                 tc_fence_after();
                 if (lane == 0) tma_wait_read<0>();           // the previous item's store has read the slab
                 __syncwarp();
 #pragma unroll 1
-                for (int c2 = 0; c2 < 4; c2++) {
+                for (int k2 = 0; k2 < 2; k2++) {
                     uint32_t o0[16], o1[16];
-                    tmem_ld16_nowait(lane_base + TM_O + 16 * c2, o0);
-                    tmem_ld16_nowait(lane_base + TM_O + 64 + 16 * c2, o1);
+                    tmem_ld16_nowait(lane_base + TM_O + 32 * hf + 16 * k2, o0);
+                    tmem_ld16_nowait(lane_base + TM_O + 64 + 32 * hf + 16 * k2, o1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int pc = 0; pc < 2; pc++) {
@@ -345,8 +353,8 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
 #pragma unroll
                         for (int e = 0; e < 8; e++)
                             v[e] = __uint_as_float(o0[8 * pc + e]) * a0 + __uint_as_float(o1[8 * pc + e]) * a1;
-                        const int piece = 2 * c2 + pc;
-                        *(uint4*)(slab + lane * 128 + ((piece ^ (lane & 7)) << 4)) =
+                        const int piece = 2 * k2 + pc;
+                        *(uint4*)(slab + lane * 64 + ((piece ^ ((lane >> 1) & 3)) << 4)) =
                             make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
                                        pack2_bf16(v[6], v[7]));
                     }
@@ -357,10 +365,10 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(&tm_out, slab, h * AT_HS, qb * AT_BQ + q4 * 32, b);
+                    tma_store_3d(&tm_out, slab, h * AT_HS + 32 * hf, qb * AT_BQ + q4 * 32, b);
                     tma_commit();
                 }
-                if (q < T) lse[(int64_t)bh * T + q] = (M + log2f(l_row)) * LN2;
+                if (hf == 0 && q < T) lse[(int64_t)bh * T + q] = (M + log2f(l_row)) * LN2;
             }
             g += nkv;
         }
@@ -383,9 +391,9 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     if (hs != AT_HS || T < 1 || B < 1 || H < 1 || !st) return cudaErrorInvalidValue;
     if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
     CUtensorMap map, omap;
-    // qkv [B, T, 3C] read in 128-row boxes; out written by per-warp 32-row stores
+    // qkv [B, T, 3C] read in 128-row boxes; out written by per-warp 32 x 32 stores
     if (!make_rows_map(&map, qkv, B, T, 3 * H * hs, AT_BQ, true) ||
-        !make_rows_map(&omap, out, B, T, H * hs, 32, false))
+        !make_rows_map(&omap, out, B, T, H * hs, 32, false, 32))
         return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> attr_done{0};   // per device
     const unsigned long long dbit = device_bit();
