@@ -244,7 +244,7 @@ def traffic_ratio_from_profiles(kernel_src: str):
     committed ncu summary, if that summary was taken on the current kernel
     source (single-kernel captures on a smaller case; see the file)."""
     path = os.path.join(ROOT, "profiles", "gemm_tc_gpt2_124m_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or not os.path.exists(kernel_src):
         return None
     with open(kernel_src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]

@@ -373,7 +373,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint8_t* wbuf = sEpi + ew * Cfg::EPI_WARP_BYTES;
         uint8_t* aring = wbuf + 2048;
         uint64_t* abar = auxbar + ew * NA;
-        const bool bias_vec = bias != nullptr && ((uintptr_t)bias & 15) == 0;
         // The GELU derivative chunks of this warp, in the order the epilogue uses
         // them (tile by tile, NCH chunks each), go into ring slot q % NA. The
         // next chunk to load is chunk a_c of tile a_w, whose corner is (a_x, a_y).
@@ -414,34 +413,27 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tile_coords(w - split * tiles, num_m, num_n, mt, nt);
             const int m_base = mt * TILE_M + (int)rank * TC_BM + q4 * 32;
             const int n_half = nt * BN + half * (BN / 2);
+            // this warp's bias values, column n_half + 32 c + lane in breg[c], loaded
+            // before the accumulator is waited for (their latency overlaps the wait)
+            float breg[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; c++) {
+                const int n = n_half + 32 * c + lane;
+                breg[c] = (bias != nullptr && n < N) ? __ldg(bias + n) : 0.f;
+            }
             ok = mbar_wait(&tfull[acc], acc_phase, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
+            const uint32_t t_row = tmem_base + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN + half * (BN / 2));
+            // the TMEM loads run one chunk ahead of the math
+            uint32_t rb[2][32];
+            tmem_ld32_nowait(t_row, rb[0]);
 #pragma unroll
             for (int c = 0; c < NCH; c++, seq++) {
                 const int n0 = n_half + 32 * c;
                 uint8_t* sbuf = wbuf + (ALT ? (seq & 1) * ALT_BYTES : 0);
-                // bias of columns n0..n0+31, the same for every lane (broadcast loads)
-                float bv[32];
-                if (bias != nullptr) {
-                    if (bias_vec && n0 + 32 <= N) {
-                        const float4* bp = (const float4*)(bias + n0);
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            const float4 t = __ldg(bp + q);
-                            bv[4 * q] = t.x;
-                            bv[4 * q + 1] = t.y;
-                            bv[4 * q + 2] = t.z;
-                            bv[4 * q + 3] = t.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; j++) bv[j] = n0 + j < N ? __ldg(bias + n0 + j) : 0.f;
-                    }
-                }
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) +
-                              (uint32_t)(acc * BN + half * (BN / 2) + c * 32), r);
+                tmem_wait_ld();
+                if (c + 1 < NCH) tmem_ld32_nowait(t_row + 32 * (c + 1), rb[(c + 1) & 1]);
                 if (c == NCH - 1) {
                     // the accumulator is free for the MMA once its last chunk is in registers
                     tc_fence_before();
@@ -451,15 +443,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         else mbar_arrive(&tempty[acc]);
                     }
                 }
+                const uint32_t(&rc)[32] = rb[c & 1];
                 float v[32];
                 if (bias != nullptr) {
 #pragma unroll
                     for (int j = 0; j < 32; j += 2)
-                        f2_split(f2_add(f2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                        f2(bv[j], bv[j + 1])), v[j], v[j + 1]);
+                        f2_split(f2_add(f2(__uint_as_float(rc[j]), __uint_as_float(rc[j + 1])),
+                                        f2(__shfl_sync(0xffffffffu, breg[c], j),
+                                           __shfl_sync(0xffffffffu, breg[c], j + 1))),
+                                 v[j], v[j + 1]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(rc[j]);
                 }
                 if (KIND == EPI_GELU_BWD) {
                     const long q = a_used;
@@ -509,6 +504,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        tmem_wait_ld();                              // no TMEM load left in flight after an abort
         if (lane == 0) {
             tma_wait_all();
             // after an abort, prefetches of the GELU derivative may still be in
