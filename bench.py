@@ -494,6 +494,48 @@ def run_op_workload(args):
                       "rounds": 4}), flush=True)
 
 
+def run_generate_workload(args):
+    """Generation throughput of the workload's model (bf16, random-init
+    weights, batch B): new tokens per second of the library's loop with the
+    key/value cache (one position per step after the first forward) and
+    without it (the full [B, T] forward per token, as the pages' loop does),
+    from a short and from a long synthetic prompt. Prints one JSON line."""
+    import torch
+    from decoder_only_transformer_06_b300 import gpt2
+    from decoder_only_transformer_06_b300.generate import generate
+    L, H, C, V, Vp, T, B, kind = WORKLOADS[args.workload]
+    if args.batch:
+        B = args.batch
+    cfg = gpt2.Config(n_layer=L, n_head=H, d_model=C, vocab_size=V, padded_vocab=Vp, block_size=T,
+                      batch_size=B, seq_len=T, precision=gpt2.GPT2_BF16)
+    stream = torch.cuda.Stream()
+    model = gpt2.GPT2(cfg, seed=1337, stream=stream)
+    new = 64
+    res = {}
+    for t0 in (32, T - new):
+        prompt, _ = synthdata.batch_for(kind, V, B, t0, 7)
+        for cache in (True, False):
+            generate(model, prompt, 4, temperature=1.0, top_k=50, seed=1, kv_cache=cache)   # warm-up
+            torch.cuda.synchronize()
+            t_start = time.perf_counter()
+            generate(model, prompt, new, temperature=1.0, top_k=50, seed=2, kv_cache=cache)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t_start
+            res[f"prompt{t0}_{'kv_cache' if cache else 'full_forward'}"] = {
+                "tokens_per_s": round(B * new / dt, 1), "ms_per_token_step": round(1e3 * dt / new, 3)}
+    # per-site device time of the cached steps (library profiling mode)
+    prompt, _ = synthdata.batch_for(kind, V, B, T - new, 7)
+    model.profile(True)
+    generate(model, prompt, 9, temperature=1.0, top_k=50, seed=3, kv_cache=True)
+    rep = model.profile_report()
+    model.profile(False)
+    sites = {r["name"]: round(r["ms"] / 8, 4) for r in rep if r["name"].startswith("decode_")}
+    model.close()
+    print(json.dumps({"op_workload": "generate", "workload": args.workload, "batch": B,
+                      "new_tokens": new, "sampling": "temperature 1.0, top-k 50", "results": res,
+                      f"decode_site_ms_per_step_at_prompt{T - new}": sites}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -504,9 +546,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (small profiling captures)")
-    ap.add_argument("--op-workload", choices=["attention", "mlp_gemms"], default=None,
-                    help="only run one block's op-level kernels (for ncu captures)")
+    ap.add_argument("--op-workload", choices=["attention", "mlp_gemms", "generate"], default=None,
+                    help="only run one block's op-level kernels (for ncu captures), or time generation")
     args = ap.parse_args()
+    if args.op_workload == "generate":
+        run_generate_workload(args)
+        return
     if args.op_workload:
         run_op_workload(args)
         return

@@ -89,6 +89,12 @@ struct gpt2_model {
     void* logits = nullptr;
     float* row_loss = nullptr;
     float* last_logits = nullptr;   // fp32 [B, Vp]: the head on one position per sequence
+    // Key/value cache of generation: the qkv buffer of every layer holds the
+    // keys and values of positions 0..kv_len-1 of the current generation
+    // context (set by gpt2_forward_last and gpt2_decode_step; any training
+    // forward or parameter change resets it to 0).
+    int kv_len = 0;
+    void* dec_ws = nullptr;         // row buffers of gpt2_decode_step (allocated on first use)
 
     float* dres = nullptr;
     void* dres_act = nullptr;
@@ -659,6 +665,7 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt, i
     RUN(m, "layernorm_fwd", 1, 0, add_ln_bytes,
         k::layernorm_fwd<Act>(m->la[L - 1].x_mid, (const Act*)m->yproj, m->x_final, m->P(m->lnf_g()),
                               m->P(m->lnf_g() + 1), (Act*)m->uf, m->muf, m->rsf, M, C, s));
+    m->kv_len = last_t;           // training forwards (last_t == 0) overwrite the cache
     if (last_t > 0) {
         // the tied head on one position per sequence: rows b*T + last_t - 1 of uf
         const void* a = (const char*)m->uf + (size_t)(last_t - 1) * C * m->act_bytes;
@@ -677,6 +684,77 @@ static int forward_impl(gpt2_model* m, const int32_t* tok, const int32_t* tgt, i
             k::cross_entropy<Act>((Act*)m->logits, tgt, m->row_loss, M, m->V, m->Vp, m->st, s));
         RUN(m, "loss_reduce", 1, 0, 4.0 * M, k::loss_reduce(m->row_loss, M, m->st, s));
     }
+    return GPT2_OK;
+}
+
+// One decoding step: the forward of position p = t - 1 of every sequence
+// alone, its query attending to the cached keys and values of positions
+// 0..p (this step writes row p of every layer's qkv buffer), the head on the
+// new row into m->last_logits. Row buffers (B rows each): residual stream x0,
+// x1 (fp32 [B, C]), LayerNorm statistics, u, att, y (act [B, C]), gelu'(pre)
+// and gelu(pre) (act [B, 4C]).
+template <typename Act>
+static int decode_impl(gpt2_model* m, const int32_t* tok, int t) {
+    cudaStream_t s = m->stream;
+    const int C = m->C, L = m->L, T = m->T, B = m->B, H = m->H, p = t - 1;
+    const double A = m->act_bytes, BC = (double)B * C;
+    Op op{m};
+    auto carve = [](char*& q, size_t bytes) {
+        char* r = q;
+        q += (bytes + 255) / 256 * 256;
+        return (void*)r;
+    };
+    char* q = (char*)m->dec_ws;
+    float* x0 = (float*)carve(q, (size_t)B * C * 4);
+    float* x1 = (float*)carve(q, (size_t)B * C * 4);
+    float* mu = (float*)carve(q, (size_t)B * 4);
+    float* rs = (float*)carve(q, (size_t)B * 4);
+    Act* u = (Act*)carve(q, (size_t)B * C * sizeof(Act));
+    Act* att = (Act*)carve(q, (size_t)B * C * sizeof(Act));
+    Act* y = (Act*)carve(q, (size_t)B * C * sizeof(Act));
+    Act* hpre = (Act*)carve(q, (size_t)B * 4 * C * sizeof(Act));
+    Act* hgel = (Act*)carve(q, (size_t)B * 4 * C * sizeof(Act));
+    float* part = (float*)carve(q, k::attention_decode_workspace_floats(B, T, H, m->hs) * 4);
+    const double ln_bytes = BC * (4 + A) + 8.0 * B, add_ln_bytes = ln_bytes + BC * (A + 4);
+    RUN(m, "decode_embed", 1, 0, 4.0 * B + 12.0 * BC,
+        k::embed_rows(tok, m->P(0), m->P(1), x0, B, p, C, m->V, m->st, s));
+    RUN(m, "decode_layernorm", 1, 0, ln_bytes,
+        k::layernorm_fwd<Act>(x0, nullptr, nullptr, m->P(m->lt(0, T_LN1G)), m->P(m->lt(0, T_LN1B)), u, mu, rs,
+                              B, C, s));
+    for (int l = 0; l < L; l++) {
+        LayerActs& a = m->la[l];
+        {
+            // q, k, v of the new row go to row p of the layer's qkv buffer
+            Act* qkv_p = (Act*)a.qkv + (size_t)p * 3 * C;
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_ATTB)), qkv_p, (int64_t)T * 3 * C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("decode_gemm_qkv", B, 3 * C, C, {u, C, true}, {m->W(m->lt(l, T_ATTW)), C, true}, e));
+        }
+        RUN(m, "decode_attention", 1, 4.0 * (p + 1) * m->hs * (double)B * H, 2.0 * A * (p + 1) * BC,
+            k::attention_decode<Act>((const Act*)a.qkv, att, part, B, T, H, m->hs, p, s));
+        {
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_APB)), y, C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("decode_gemm_attproj", B, C, C, {att, C, true}, {m->W(m->lt(l, T_APW)), C, true}, e));
+        }
+        RUN(m, "decode_layernorm", 1, 0, add_ln_bytes,
+            k::layernorm_fwd<Act>(x0, y, x1, m->P(m->lt(l, T_LN2G)), m->P(m->lt(l, T_LN2B)), u, mu, rs, B, C, s));
+        {
+            GemmEpi e{EPI_GELU, m->P(m->lt(l, T_FCB)), hpre, 4 * C, hgel, 4 * C, nullptr, 0};
+            OPR(op.gemm("decode_gemm_fc", B, 4 * C, C, {u, C, true}, {m->W(m->lt(l, T_FCW)), C, true}, e));
+        }
+        {
+            GemmEpi e{EPI_STORE_ACT, m->P(m->lt(l, T_MPB)), y, C, nullptr, 0, nullptr, 0};
+            OPR(op.gemm("decode_gemm_mlpproj", B, C, 4 * C, {hgel, 4 * C, true},
+                        {m->W(m->lt(l, T_MPW)), 4 * C, true}, e));
+        }
+        // x0 = x1 + y, and the next LayerNorm (ln_1 of block l + 1, or ln_f)
+        const bool last = l + 1 == L;
+        RUN(m, "decode_layernorm", 1, 0, add_ln_bytes,
+            k::layernorm_fwd<Act>(x1, y, x0, m->P(last ? m->lnf_g() : m->lt(l + 1, T_LN1G)),
+                                  m->P(last ? m->lnf_g() + 1 : m->lt(l + 1, T_LN1B)), u, mu, rs, B, C, s));
+    }
+    GemmEpi e{EPI_STORE_F32, nullptr, m->last_logits, m->Vp, nullptr, 0, nullptr, 0};
+    OPR(op.gemm("decode_gemm_lmhead", B, m->Vp, C, {u, C, true}, {m->W(0), C, true}, e));
+    m->kv_len = t;
     return GPT2_OK;
 }
 
@@ -896,6 +974,29 @@ int gpt2_forward_last(gpt2_model* m, const int32_t* tok, int t, float* d_logits)
     return GPT2_OK;
 }
 
+int gpt2_decode_step(gpt2_model* m, const int32_t* tok, int t, float* d_logits) {
+    if (!m) return GPT2_EINVAL;
+    if (!tok || !d_logits) return fail(m, GPT2_EINVAL, "tokens or logits pointer is NULL");
+    if (t < 1 || t > m->T) return fail(m, GPT2_EINVAL, "t must be in [1, seq_len]");
+    if (m->hs > 128) return fail(m, GPT2_EINVAL, "decoding needs a head size of at most 128");
+    if (t - 1 > m->kv_len)
+        return fail(m, GPT2_ESTATE, "the key/value cache does not hold positions 0..t-2: run gpt2_forward_last first");
+    if (int r = join_side(m)) return r;
+    if (!m->dec_ws) {
+        const size_t rows = (size_t)m->B, C = (size_t)m->C;
+        const size_t bytes = 2 * (rows * C * 4 + 256) + 2 * (rows * 4 + 256) + 3 * (rows * C * m->act_bytes + 256) +
+                             2 * (rows * 4 * C * m->act_bytes + 256) +
+                             k::attention_decode_workspace_floats(m->B, m->T, m->H, m->hs) * 4 + 256;
+        ALLOC(m, m->dec_ws, bytes);
+    }
+    m->have_targets = false;
+    int r = m->use_bf16 ? decode_impl<bf16>(m, tok, t) : decode_impl<float>(m, tok, t);
+    if (r) return r;
+    CK(m, cudaMemcpy2DAsync(d_logits, (size_t)m->V * 4, m->last_logits, (size_t)m->Vp * 4, (size_t)m->V * 4,
+                            (size_t)m->B, cudaMemcpyDeviceToDevice, m->stream));
+    return GPT2_OK;
+}
+
 int gpt2_backward(gpt2_model* m) {
     if (!m) return GPT2_EINVAL;
     {
@@ -916,6 +1017,7 @@ int gpt2_step(gpt2_model* m, float lr, float beta1, float beta2, float eps, floa
     }
     cudaStream_t s = m->stream;
     const double n = (double)m->n_arena;
+    m->kv_len = 0;                // the parameters change
     RUN(m, "grad_norm", 1, 0, 4.0 * n,
         k::grad_norm(m->grads, m->n_arena, m->norm_partial, m->norm_parts, s));
     RUN(m, "step_finalize", 1, 0, 8.0 * m->norm_parts,
@@ -1042,6 +1144,7 @@ int gpt2_copy_tensor(gpt2_model* m, int i, int which, float* dst) {
     if (int r0 = join_side(m)) return r0;
     float* buf = buffer_of(m, which);
     if (!buf) return fail(m, GPT2_EINVAL, "unknown buffer selector");
+    if (which == GPT2_PARAM) m->kv_len = 0;
     CK(m, cudaStreamSynchronize(m->stream));
     const TensorRec& r = m->tensors[i];
     CK(m, cudaMemcpy(dst, buf + r.offset, r.numel * sizeof(float), cudaMemcpyDeviceToHost));
@@ -1139,6 +1242,7 @@ int gpt2_save(gpt2_model* m, const char* path) {
 int gpt2_load(gpt2_model* m, const char* path) {
     if (!m || !path) return GPT2_EINVAL;
     if (int r0 = join_side(m)) return r0;
+    m->kv_len = 0;
     FILE* f = std::fopen(path, "rb");
     if (!f) return fail(m, GPT2_EINVAL, std::string("cannot open checkpoint file ") + path);
     char magic[16];

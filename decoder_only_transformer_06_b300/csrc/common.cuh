@@ -135,6 +135,18 @@ cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cu
 cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, int T, int C,
                             void* workspace, cudaStream_t s);
 
+// Decoding with the key/value cache (one new position p per sequence):
+// x[b] = wte[tok[b]] + wpe[p] for b < B (ids clamped and flagged), and the
+// causal attention of the query row p of qkv [B, T, 3C] over the key/value
+// rows 0..p, written to out [B, C] (hs <= 128), through a workspace of
+// attention_decode_workspace_floats floats.
+cudaError_t embed_rows(const int32_t* tok, const float* wte, const float* wpe, float* x, int B, int p, int C,
+                       int V, DevState* st, cudaStream_t s);
+size_t attention_decode_workspace_floats(int B, int T, int H, int hs);
+template <typename Act>
+cudaError_t attention_decode(const Act* qkv, Act* out, float* part, int B, int T, int H, int hs, int p,
+                             cudaStream_t s);
+
 // u = LN(x') with x' = x, or x' = x + y written to x_out when y != nullptr
 // (the residual add of the preceding branch fused into the LayerNorm).
 template <typename Act>

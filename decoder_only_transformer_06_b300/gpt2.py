@@ -61,6 +61,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_forward": (I, [P, P, P, FP]),
         "gpt2_backward": (I, [P]),
         "gpt2_forward_last": (I, [P, P, I, P]),
+        "gpt2_decode_step": (I, [P, P, I, P]),
         "gpt2_step": (I, [P, F, F, F, F, F, F, FP]),
         "gpt2_zero_grad": (I, [P]),
         "gpt2_lr_schedule": (D, [I64, I64, I64, D, D]),
@@ -211,6 +212,14 @@ class GPT2:
         tensor [B*T] (positions >= t are ignored by causality)."""
         self._ck(_lib.gpt2_forward_last(self.h, ctypes.c_void_p(tokens.data_ptr()), int(t),
                                         ctypes.c_void_p(logits_out.data_ptr())))
+
+    def decode_step(self, tokens, t: int, logits_out):
+        """One step with the key/value cache: logits of position t-1 of each
+        sequence into logits_out (fp32 CUDA tensor [B, V]); tokens: int32 CUDA
+        tensor [B], the token at position t-1 of every sequence (positions
+        0..t-2 cached by forward_last or earlier decode steps)."""
+        self._ck(_lib.gpt2_decode_step(self.h, ctypes.c_void_p(tokens.data_ptr()), int(t),
+                                       ctypes.c_void_p(logits_out.data_ptr())))
 
     def backward(self):
         self._ck(_lib.gpt2_backward(self.h))

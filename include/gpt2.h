@@ -148,6 +148,32 @@ int gpt2_forward(gpt2_model* model, const int32_t* d_tokens, const int32_t* d_ta
 int gpt2_forward_last(gpt2_model* model, const int32_t* d_tokens, int t, float* d_logits);
 
 /*
+ * gpt2_decode_step -- one generation step with the key/value cache. The
+ * pages' sampling loop ("Let's reproduce GPT-2", 00:37:02; nanoGPT guide,
+ * sample.py) runs the whole context through the model for every new token;
+ * with absolute position embeddings the keys and values of the earlier
+ * positions do not change, so this step computes position t-1 alone and
+ * reads the others' keys and values from the cache that gpt2_forward_last and
+ * earlier steps left in the model. The logits equal gpt2_forward_last's on
+ * the context extended by the new tokens, up to rounding.
+ *   d_tokens: device int32 [B], the token at position t-1 of every sequence.
+ *   t:        in [1, T]; positions 0..t-2 must be cached: the last call on
+ *             this model was gpt2_forward_last with a t' >= t-1 or
+ *             gpt2_decode_step with t' >= t-1, and no training forward,
+ *             optimizer step, gpt2_set_tensor or gpt2_load came after it.
+ *   d_logits: device fp32 [B, V] row-major, caller-owned; receives the logits
+ *             of position t-1 of every sequence (real vocabulary only).
+ * Once a context holds T tokens, the pages' crop shifts every position, so
+ * the next token needs gpt2_forward_last on the cropped context. The first
+ * call allocates the step's row buffers (B rows, about 44 C bytes per row);
+ * no backward afterwards (ESTATE). Does not synchronise.
+ * Errors: EINVAL (NULL pointers, t outside [1, T], a head size that does not
+ * divide 128); ESTATE (positions 0..t-2 not cached); ENOMEM; ERANGE as
+ * gpt2_forward.
+ */
+int gpt2_decode_step(gpt2_model* model, const int32_t* d_tokens, int t, float* d_logits);
+
+/*
  * gpt2_backward -- gradient of (loss / grad_accum_steps) added (+=) into the
  * gradient buffers (nanoGPT guide Part IV Stage 4 "backward() accumulates
  * gradients"). Needs a preceding gpt2_forward with targets (else ESTATE).

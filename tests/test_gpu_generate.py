@@ -1,7 +1,9 @@
 """Generation on the GPU through the C ABI: gpt2_op_sample against the
 oracle's sampler, gpt2_forward_last against the full forward and the oracle,
+gpt2_decode_step (the key/value cache) against the oracle's full forward,
 and the library's generation loop against the oracle's loop on the same
-uniforms (fp32 token for token; bf16 greedy within the bf16 logit error).
+uniforms (fp32 token for token, with and without the cache; bf16 greedy
+within the bf16 logit error).
 
 Where floating point decides the token (an inverse-CDF boundary), both sides
 decide in their own precision; the comparisons assert equality only where the
@@ -134,10 +136,13 @@ def test_forward_last_matches_the_full_forward_and_the_oracle(precision):
     m.close()
 
 
-def test_library_generation_matches_the_oracle_fp32():
-    """fp32-math mode: the library's loop (device forward_last + sampler)
-    against the oracle's loop on the same uniforms, greedy and sampled (top-k 5,
-    temperature 0.8), past the block size (the context is cropped)."""
+@pytest.mark.parametrize("kv_cache", [True, False])
+def test_library_generation_matches_the_oracle_fp32(kv_cache):
+    """fp32-math mode: the library's loop (device forward_last or the
+    key/value-cache step, + sampler) against the oracle's loop (a full forward
+    per token) on the same uniforms, greedy and sampled (top-k 5, temperature
+    0.8), past the block size (the context is cropped, after which the cached
+    positions no longer hold and the loop runs the full forward again)."""
     c = CONFIGS["tiny"]
     m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=4)
     params = O.init_params(c, 4)
@@ -145,9 +150,68 @@ def test_library_generation_matches_the_oracle_fp32():
     n = c.block_size + 4
     u = np.stack([draw_uniforms(3, s, c.batch_size) for s in range(n)])
     for top_k, temp in ((1, 1.0), (5, 0.8), (None, 0.0)):
-        a = generate(m, prompt, n, temperature=temp, top_k=top_k, uniforms=u)
+        a = generate(m, prompt, n, temperature=temp, top_k=top_k, uniforms=u, kv_cache=kv_cache)
         b = oracle_generate(params, c, prompt, n, temp, top_k, u)
         assert np.array_equal(a, b), (top_k, temp)
+    m.close()
+
+
+@pytest.mark.parametrize("precision", [gpt2.GPT2_FP32, gpt2.GPT2_BF16])
+def test_decode_step_matches_the_oracle(precision):
+    """A chain of cached steps after one forward_last: the logits of position
+    t-1 for t = t0+1 .. T (the last step fills the block) against the
+    oracle's full forward on the same context, and against forward_last on
+    that context afterwards (same library, no cache)."""
+    c = O.Config(n_layer=2, n_head=2, d_model=128, vocab_size=65, block_size=64, batch_size=3,
+                 seq_len=64)
+    m = gpt2.GPT2(gpu_cfg(c, precision), seed=9)
+    params = O.init_params(c, 9)
+    x, _ = synthdata.uniform_batch(65, c.batch_size, c.seq_len, 5)
+    _, ref, _ = O.forward(params, c, x)
+    t0 = 57
+    out = torch.empty(c.batch_size, c.vocab_size, dtype=torch.float32, device="cuda")
+    d_x = dev(x).view(c.batch_size, c.seq_len)
+    m.forward_last(d_x.reshape(-1), t0, out)
+    got = {}
+    for t in range(t0 + 1, c.seq_len + 1):
+        tok = d_x[:, t - 1].contiguous()
+        m.decode_step(tok, t, out)
+        got[t] = out.cpu().numpy().copy()
+    for t, g in got.items():
+        m.forward_last(d_x.reshape(-1), t, out)
+        nocache = out.cpu().numpy()
+        want = ref[:, t - 1]
+        if precision == gpt2.GPT2_FP32:
+            assert np.allclose(g, want, rtol=1e-4, atol=1e-5), t
+            assert np.allclose(g, nocache, rtol=1e-5, atol=1e-5), t
+        else:
+            err = np.linalg.norm(g - want) / np.linalg.norm(want)
+            assert err < 2e-2, (t, err)
+            err2 = np.linalg.norm(g - nocache) / np.linalg.norm(nocache)
+            assert err2 < 1e-2, (t, err2)
+    m.close()
+
+
+def test_decode_step_needs_the_cached_positions():
+    c = CONFIGS["tiny"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=2)
+    x, y = synthdata.uniform_batch(c.vocab_size, c.batch_size, c.seq_len, 6)
+    out = torch.empty(c.batch_size, c.vocab_size, dtype=torch.float32, device="cuda")
+    d_x = dev(x)
+    tok = d_x.view(c.batch_size, c.seq_len)[:, 0].contiguous()
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.decode_step(tok, 2, out)                     # nothing cached yet
+    assert e.value.code == gpt2.GPT2_ESTATE
+    m.decode_step(tok, 1, out)                         # position 0 needs no cache
+    m.forward_last(d_x, 5, out)
+    m.decode_step(d_x.view(c.batch_size, c.seq_len)[:, 5].contiguous(), 6, out)
+    m.forward(d_x, dev(y))                             # a training forward overwrites the cache
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.decode_step(tok, 7, out)
+    assert e.value.code == gpt2.GPT2_ESTATE
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.decode_step(tok, c.seq_len + 1, out)
+    assert e.value.code == gpt2.GPT2_EINVAL
     m.close()
 
 
