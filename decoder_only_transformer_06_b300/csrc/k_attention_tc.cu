@@ -44,7 +44,7 @@ using namespace attn;
 
 namespace {
 
-constexpr int AT_SLOTS = 3;                    // K and V ring depth
+constexpr int AT_SLOTS = 5;                    // K and V ring depth (32 KB a slot)
 constexpr int FW_THREADS = 384;                // forward: 8 softmax warps, producer, three MMA issuers
 constexpr int FW_PRODUCER = 8, FW_ISSUE_S = 9, FW_ISSUE_PV = 10;   // P V issuers: warps 10, 11
 constexpr int FW_SBUF = 3;                     // S buffers in TMEM
@@ -80,15 +80,15 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
     uint64_t* bars = (uint64_t*)(smem + OFF_BAR);
     uint64_t* q_full = bars;           // [2]
     uint64_t* q_empty = bars + 2;      // [2]
-    uint64_t* kv_full = bars + 4;      // [3] K and V block j
-    uint64_t* kv_empty = bars + 7;     // [3]
-    uint64_t* s_full = bars + 10;      // [3]
-    uint64_t* p_full = bars + 13;      // [3 buffers][2 halves]
-    uint64_t* pv_done = bars + 19;     // [3] both halves' P V products of the block
-    uint64_t* o_free = bars + 22;      // the O accumulators have been read
-    uint64_t* ml_full = bars + 23;     // [2] both halves' (m, l) of an item are in smem
-    uint64_t* drain = bars + 25;       // [3] one per issuing thread
-    uint32_t* tmem_slot = (uint32_t*)(bars + 28);
+    uint64_t* kv_full = bars + 4;                  // [AT_SLOTS] K and V block j
+    uint64_t* kv_empty = kv_full + AT_SLOTS;       // [AT_SLOTS]
+    uint64_t* s_full = kv_empty + AT_SLOTS;        // [FW_SBUF]
+    uint64_t* p_full = s_full + FW_SBUF;           // [FW_SBUF buffers][2 halves]
+    uint64_t* pv_done = p_full + 2 * FW_SBUF;      // [FW_SBUF] both halves' P V products of the block
+    uint64_t* o_free = pv_done + FW_SBUF;          // the O accumulators have been read
+    uint64_t* ml_full = o_free + 1;                // [2] both halves' (m, l) of an item are in smem
+    uint64_t* drain = ml_full + 2;                 // [3] one per issuing thread
+    uint32_t* tmem_slot = (uint32_t*)(drain + 3);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
     const int nqb = (T + AT_BQ - 1) / AT_BQ;
