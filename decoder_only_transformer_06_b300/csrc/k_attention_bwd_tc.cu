@@ -53,7 +53,7 @@ constexpr int OUT32 = 32 * 32 * 2;              // one warp's 32 x 32 output sla
 
 // dK/dV kernel: K and V of the item double buffered (by item), Q and dO in a
 // ring of 64-query sub-blocks with their lse and D values staged beside them
-constexpr int KV_NS = 5;
+constexpr int KV_NS = 7;
 constexpr int KV_OFF_K = 0;                                  // [2] 16 KB
 constexpr int KV_OFF_V = KV_OFF_K + 2 * AT_TILE;             // [2]
 constexpr int KV_OFF_Q = KV_OFF_V + 2 * AT_TILE;             // [NS] 8 KB
@@ -69,7 +69,7 @@ constexpr uint32_t KV_TM_ST = 0, KV_TM_DPT = 128, KV_TM_DV = 256, KV_TM_DK = 320
 
 // dQ kernel: Q, dO and O of the item double buffered (by item), K and V in a
 // ring of 64-key sub-blocks
-constexpr int DQ_NS = 4;
+constexpr int DQ_NS = 6;
 constexpr int DQ_OFF_Q = 0;                                  // [2] 16 KB
 constexpr int DQ_OFF_DO = DQ_OFF_Q + 2 * AT_TILE;            // [2]
 constexpr int DQ_OFF_O = DQ_OFF_DO + 2 * AT_TILE;            // [2] forward output tile (for D)
