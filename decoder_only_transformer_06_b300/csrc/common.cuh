@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 #include <atomic>
+#include <cstdlib>
+#include <utility>
 
 typedef __nv_bfloat16 bf16;
 
@@ -60,6 +62,45 @@ struct GemmEpi {
 };
 
 #define CUDA_OK(expr) do { cudaError_t e__ = (expr); if (e__ != cudaSuccess) return e__; } while (0)
+
+// Programmatic dependent launch. Every kernel is launched with programmatic
+// stream serialization (when enabled), so it may start while the kernel before
+// it on the stream is finishing: it first runs its own set-up (barriers, TMEM,
+// tensor-map prefetch), then pdl_wait() blocks until the previous kernel has
+// completed and its writes are visible; nothing touches global memory before
+// that. pdl_trigger() lets the next kernel be scheduled once every CTA of this
+// one has issued it or exited: the short kernels issue it at their start (the
+// next kernel's CTAs then fill the SMs their last wave frees), the persistent
+// tensor-core kernels once a CTA has issued its last copies (so that waiting
+// successors do not hold SMs while there is still work for them).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// PDL on unless GPT2_PDL=0 in the environment (read once per process).
+inline bool pdl_on() {
+    static const bool on = [] {
+        const char* e = getenv("GPT2_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// kern<<<grid, block, smem, s>>>(args...) with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+inline cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_on() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // tanh-form GELU (Hendrycks & Gimpel) and its derivative, fp32. The forward
 // Linear that applies GELU saves gelu'(pre) (not pre): the backward then only

@@ -163,6 +163,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();                              // the previous kernel's outputs are visible
 
     if (warp == BW_PRODUCER) {
         // ---------------- producer warp: lane 0 issues the TMA copies; all lanes
@@ -206,6 +207,7 @@ fa_tc_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_con
             }
             g += n;
         }
+        if (lane == 0) pdl_trigger();        // every copy of this CTA is issued
         if (lane == 0 && (!ok || *abort_flag)) {
             for (int i = (nkvl > 2 ? nkvl - 2 : 0); i < nkvl; i++) wait_bounded(&kv_full[i & 1], (uint32_t)((i >> 1) & 1));
             for (int i = (nql > KV_NS ? nql - KV_NS : 0); i < nql; i++)
@@ -435,6 +437,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();                              // the previous kernel's outputs are visible
     // sub-blocks of the item whose query block is qb: keys 0 .. min(T, 128 qb + 128)
     auto nsub = [&](int qb) { return min(nsb, 2 * qb + 2); };
 
@@ -463,6 +466,7 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
                 g += n;
             }
+            pdl_trigger();                   // every copy of this CTA is issued
             if (!ok || *abort_flag) {
                 for (int i = (nql > 2 ? nql - 2 : 0); i < nql; i++) wait_bounded(&qd_full[i & 1], (uint32_t)((i >> 1) & 1));
                 for (int i = (nkvl > DQ_NS ? nkvl - DQ_NS : 0); i < nkvl; i++)
@@ -675,10 +679,10 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* out, const bf16* dout,
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
     // the dQ kernel also computes D = rowsum(dO * O), which the dK/dV kernel reads
-    fa_tc_bwd_dq_kernel<<<grid, DQ_THREADS, DQ_SMEM, s>>>(q128, q64, do128, o128, dqkv_out, lse, D, T, H,
+    (void)pdl_launch(fa_tc_bwd_dq_kernel, grid, DQ_THREADS, DQ_SMEM, s, q128, q64, do128, o128, dqkv_out, lse, D, T, H,
                                                           B * H, st);
     CUDA_OK(cudaGetLastError());
-    fa_tc_bwd_dkv_kernel<<<grid, KV_THREADS, KV_SMEM, s>>>(q128, q64, do64, dqkv_out, lse, D, T, H, B * H, st);
+    (void)pdl_launch(fa_tc_bwd_dkv_kernel, grid, KV_THREADS, KV_SMEM, s, q128, q64, do64, dqkv_out, lse, D, T, H, B * H, st);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,8 @@ __device__ __forceinline__ float dot_row(const float* a, const float* __restrict
 __global__ void __launch_bounds__(AW * 32)
 attn_fwd_f32_kernel(const float* __restrict__ qkv, float* __restrict__ out,
                     float* __restrict__ lse, int B, int T, int H, int hs) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float qs[AW][HS_MAX];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t gw = (int64_t)blockIdx.x * AW + warp;
@@ -80,6 +82,8 @@ attn_fwd_f32_kernel(const float* __restrict__ qkv, float* __restrict__ out,
 // D[b,h,i] = sum_c dout[i, h*hs+c] * out[i, h*hs+c]  (= rowsum(dP * P))
 __global__ void attn_bwd_d_f32(const float* __restrict__ out, const float* __restrict__ dout,
                                float* __restrict__ D, int B, int T, int H, int hs) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t gw = (int64_t)blockIdx.x * AW + warp;
     if (gw >= (int64_t)B * H * T) return;
@@ -99,6 +103,8 @@ __global__ void __launch_bounds__(AW * 32)
 attn_bwd_dq_f32(const float* __restrict__ qkv, const float* __restrict__ lse,
                 const float* __restrict__ dout, const float* __restrict__ D,
                 float* __restrict__ dqkv, int B, int T, int H, int hs) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float qs[AW][HS_MAX];
     __shared__ float ds_[AW][HS_MAX];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -153,6 +159,8 @@ __global__ void __launch_bounds__(AW * 32)
 attn_bwd_dkv_f32(const float* __restrict__ qkv, const float* __restrict__ lse,
                  const float* __restrict__ dout, const float* __restrict__ D,
                  float* __restrict__ dqkv, int B, int T, int H, int hs) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float ks[AW][HS_MAX];
     __shared__ float vs[AW][HS_MAX];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -216,7 +224,7 @@ cudaError_t attention_fwd_f32(const float* qkv, float* out, float* lse, int B, i
                               cudaStream_t s) {
     if (hs > HS_MAX) return cudaErrorInvalidValue;
     int64_t rows = (int64_t)B * H * T;
-    attn_fwd_f32_kernel<<<(unsigned)((rows + AW - 1) / AW), AW * 32, 0, s>>>(qkv, out, lse, B, T,
+    (void)pdl_launch(attn_fwd_f32_kernel, (unsigned)((rows + AW - 1) / AW), AW * 32, 0, s, qkv, out, lse, B, T,
                                                                            H, hs);
     return cudaGetLastError();
 }
@@ -227,11 +235,11 @@ cudaError_t attention_bwd_f32(const float* qkv, const float* out, const float* l
     if (hs > HS_MAX) return cudaErrorInvalidValue;
     int64_t rows = (int64_t)B * H * T;
     unsigned g = (unsigned)((rows + AW - 1) / AW);
-    attn_bwd_d_f32<<<g, AW * 32, 0, s>>>(out, dout, Dbuf, B, T, H, hs);
+    (void)pdl_launch(attn_bwd_d_f32, g, AW * 32, 0, s, out, dout, Dbuf, B, T, H, hs);
     CUDA_OK(cudaGetLastError());
-    attn_bwd_dq_f32<<<g, AW * 32, 0, s>>>(qkv, lse, dout, Dbuf, dqkv, B, T, H, hs);
+    (void)pdl_launch(attn_bwd_dq_f32, g, AW * 32, 0, s, qkv, lse, dout, Dbuf, dqkv, B, T, H, hs);
     CUDA_OK(cudaGetLastError());
-    attn_bwd_dkv_f32<<<g, AW * 32, 0, s>>>(qkv, lse, dout, Dbuf, dqkv, B, T, H, hs);
+    (void)pdl_launch(attn_bwd_dkv_f32, g, AW * 32, 0, s, qkv, lse, dout, Dbuf, dqkv, B, T, H, hs);
     return cudaGetLastError();
 }
 

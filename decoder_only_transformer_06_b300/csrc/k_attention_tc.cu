@@ -123,6 +123,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();                              // the previous kernel's outputs are visible
 
     if (warp == FW_PRODUCER) {
         if (lane == 0) {
@@ -147,6 +148,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 }
                 g += nkv;
             }
+            pdl_trigger();                   // every copy of this CTA is issued
             if (!ok || *abort_flag) {
                 // wait (bounded) for every copy still in flight before the CTA exits
                 for (int i = (nq > 2 ? nq - 2 : 0); i < nq; i++) wait_bounded(&q_full[i & 1], (uint32_t)((i >> 1) & 1));
@@ -404,7 +406,7 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     }
     const int items = ((T + AT_BQ - 1) / AT_BQ) * B * H;
     const int grid = items < num_sms() ? items : num_sms();
-    fa_tc_fwd_kernel<<<grid, FW_THREADS, AT_SMEM, s>>>(map, omap, lse, T, H, B * H, st);
+    (void)pdl_launch(fa_tc_fwd_kernel, grid, FW_THREADS, AT_SMEM, s, map, omap, lse, T, H, B * H, st);
     return cudaGetLastError();
 }
 

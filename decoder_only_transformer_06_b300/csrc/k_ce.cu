@@ -73,6 +73,8 @@ template <typename Act, int NCH>
 __global__ void __launch_bounds__(CE_THREADS)
 ce_kernel(Act* __restrict__ logits, const int32_t* __restrict__ tgt, float* __restrict__ row_loss,
           int V, int Vp, const DevState* __restrict__ st) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int VEC = Vec16<Act>::N;
     __shared__ float sm[CE_THREADS / 32];
     const int row = blockIdx.x;
@@ -177,6 +179,8 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
         ptx::fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();                       // the previous kernel's outputs are visible
+    pdl_trigger();
     const int nvec = Vp / 8;          // 16-byte chunks per row
     const int nfull = V / 8;          // chunks entirely below V
     const float L2E = 1.4426950408889634f;
@@ -298,14 +302,14 @@ cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int 
             CUDA_OK(cudaFuncSetAttribute(ce_bulk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          100));
             int grid = M < 2 * num_sms() ? M : 2 * num_sms();
-            ce_bulk_kernel<<<grid, CEB_THREADS, smem, s>>>((bf16*)logits, tgt, row_loss, M, V, Vp, st);
+            (void)pdl_launch(ce_bulk_kernel, grid, CEB_THREADS, smem, s, (bf16*)logits, tgt, row_loss, M, V, Vp, st);
             return cudaGetLastError();
         }
     }
     int nch = (Vp / VEC + CE_THREADS - 1) / CE_THREADS;
 #define CE_CASE(NC)                                                                     \
     if (nch <= NC) {                                                                    \
-        ce_kernel<Act, NC><<<M, CE_THREADS, 0, s>>>(logits, tgt, row_loss, V, Vp, st); \
+        (void)pdl_launch(ce_kernel<Act, NC>, M, CE_THREADS, 0, s, logits, tgt, row_loss, V, Vp, st); \
         return cudaGetLastError();                                                      \
     }
     CE_CASE(1)

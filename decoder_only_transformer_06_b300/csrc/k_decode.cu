@@ -24,6 +24,8 @@ __device__ __forceinline__ void from_f(bf16& d, float x) { d = __float2bfloat16_
 __global__ void embed_rows_kernel(const int32_t* __restrict__ tok, const float* __restrict__ wte,
                                   const float* __restrict__ wpe, float* __restrict__ x, int p, int C, int V,
                                   DevState* st) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x;
     int t = tok[b];
     if (t < 0 || t >= V) {
@@ -74,6 +76,8 @@ template <typename Act>
 __global__ void __launch_bounds__(DEC_THREADS)
 attention_decode_span_kernel(const Act* __restrict__ qkv, float* __restrict__ part, int T, int H, int hs, int p,
                              int nspan) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float sw[DEC_SPAN];
     __shared__ float so[DEC_THREADS / 32][128];
     __shared__ float red[DEC_THREADS / 32];
@@ -156,6 +160,8 @@ attention_decode_span_kernel(const Act* __restrict__ qkv, float* __restrict__ pa
 template <typename Act>
 __global__ void __launch_bounds__(DEC_THREADS)
 attention_decode_combine_kernel(const float* __restrict__ part, Act* __restrict__ out, int H, int hs, int nspan) {
+    pdl_wait();
+    pdl_trigger();
     const int bh = blockIdx.x, b = bh / H, h = bh % H, C = H * hs;
     const float* pp = part + (int64_t)bh * nspan * (hs + 2);
     float M = -INFINITY;
@@ -177,7 +183,7 @@ attention_decode_combine_kernel(const float* __restrict__ part, Act* __restrict_
 cudaError_t embed_rows(const int32_t* tok, const float* wte, const float* wpe, float* x, int B, int p, int C,
                        int V, DevState* st, cudaStream_t s) {
     if (B < 1 || C < 1 || p < 0) return cudaErrorInvalidValue;
-    embed_rows_kernel<<<B, 256, 0, s>>>(tok, wte, wpe, x, p, C, V, st);
+    (void)pdl_launch(embed_rows_kernel, B, 256, 0, s, tok, wte, wpe, x, p, C, V, st);
     return cudaGetLastError();
 }
 
@@ -190,9 +196,9 @@ cudaError_t attention_decode(const Act* qkv, Act* out, float* part, int B, int T
                              cudaStream_t s) {
     if (B < 1 || H < 1 || hs < 1 || hs > 128 || p < 0 || p >= T || !part) return cudaErrorInvalidValue;
     const int nspan = (p + 1 + DEC_SPAN - 1) / DEC_SPAN;
-    attention_decode_span_kernel<Act><<<dim3(nspan, B * H), DEC_THREADS, 0, s>>>(qkv, part, T, H, hs, p, nspan);
+    (void)pdl_launch(attention_decode_span_kernel<Act>, dim3(nspan, B * H), DEC_THREADS, 0, s, qkv, part, T, H, hs, p, nspan);
     CUDA_OK(cudaGetLastError());
-    attention_decode_combine_kernel<Act><<<B * H, DEC_THREADS, 0, s>>>(part, out, H, hs, nspan);
+    (void)pdl_launch(attention_decode_combine_kernel<Act>, B * H, DEC_THREADS, 0, s, part, out, H, hs, nspan);
     return cudaGetLastError();
 }
 

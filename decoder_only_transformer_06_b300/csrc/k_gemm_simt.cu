@@ -14,6 +14,8 @@ __device__ __forceinline__ float ld_op(const float* p, int64_t ld, bool kmajor, 
 __global__ void __launch_bounds__(256)
 gemm_f32_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda, bool ak,
                 const float* __restrict__ B, int64_t ldb, bool bk, GemmEpi epi) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float As[SK][SB + 4];
     __shared__ float Bs[SK][SB + 4];
     const int m0 = blockIdx.y * SB, n0 = blockIdx.x * SB;
@@ -85,7 +87,7 @@ gemm_f32_kernel(int M, int N, int K, const float* __restrict__ A, int64_t lda, b
 cudaError_t gemm_f32(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                      cudaStream_t s) {
     dim3 grid((N + SB - 1) / SB, (M + SB - 1) / SB);
-    gemm_f32_kernel<<<grid, 256, 0, s>>>(M, N, K, (const float*)A.ptr, A.ld, A.kmajor,
+    (void)pdl_launch(gemm_f32_kernel, grid, 256, 0, s, M, N, K, (const float*)A.ptr, A.ld, A.kmajor,
                                          (const float*)B.ptr, B.ld, B.kmajor, epi);
     return cudaGetLastError();
 }

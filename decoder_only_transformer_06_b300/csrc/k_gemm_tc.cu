@@ -211,6 +211,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();                              // the previous kernel's outputs are visible
     // work is dealt per pair: both CTAs of a cluster walk the same tile list
     const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -278,6 +279,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
+            pdl_trigger();                   // every copy of this CTA is issued
             // the peer's copies complete on the leader's barriers, which the
             // leader's MMA issuer waits for; only the leader drains here
             if (leader && (!ok || *abort_flag)) {
@@ -611,11 +613,13 @@ bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, c
 template <typename Kern>
 static int max_pairs(Kern kern, size_t smem) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
@@ -670,21 +674,23 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     const int total = tiles * splits;
     if (!PAIR) {
         const int grid = total < num_sms() ? total : num_sms();
-        kern<<<grid, TC_THREADS, Cfg::SMEM, s>>>(ta, tb, maps, M, N, K, splits, epi.bias, st);
+        (void)pdl_launch(kern, grid, TC_THREADS, Cfg::SMEM, s, ta, tb, maps, M, N, K, splits, epi.bias, st);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * (total < pairs ? total : pairs), 1, 1);
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_on() ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, M, N, K, splits, epi.bias, st);
 }
 

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 ln_fwd_kernel(const float* __restrict__ x, const Act* __restrict__ y, float* __restrict__ x_out,
               const float* __restrict__ g, const float* __restrict__ b, Act* __restrict__ u,
               float* __restrict__ mu_out, float* __restrict__ rstd_out, int M, int C) {
+    pdl_wait();
+    pdl_trigger();
     int row = blockIdx.x * LN_WARPS + threadIdx.x / 32;
     int lane = threadIdx.x % 32;
     if (row >= M) return;
@@ -68,6 +70,8 @@ ln_bwd_kernel(const Act* __restrict__ du, const float* __restrict__ x,
               const float* __restrict__ rstd_in, float* __restrict__ dres,
               Act* __restrict__ dres_act, int accumulate, int want_sum,
               float* __restrict__ partial, int M, int C) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float sm[];   // [LN_WARPS][3][C]
     int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     float pg[EPL], pb[EPL], ps[EPL], gv[EPL];
@@ -171,6 +175,8 @@ __global__ void __launch_bounds__(LN_WARPS * 32)
 ln_fwd_vec(const float* __restrict__ x, const Act* __restrict__ y, float* __restrict__ x_out,
            const float* __restrict__ g, const float* __restrict__ b, Act* __restrict__ u,
            float* __restrict__ mu_out, float* __restrict__ rstd_out, int M, int C) {
+    pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.x * LN_WARPS + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     if (row >= M) return;
@@ -220,6 +226,8 @@ ln_bwd_vec(const Act* __restrict__ du, const float* __restrict__ x, const float*
            const float* __restrict__ mu, const float* __restrict__ rstd_in,
            float* __restrict__ dres, Act* __restrict__ dres_act, int accumulate, int want_sum,
            float* __restrict__ partial, int M, int C) {
+    pdl_wait();
+    pdl_trigger();
     // each warp accumulates its partials (dg, db and, if asked, the column sum
     // of the new dres) in its own slice of shared memory ([LN_WARPS][3][C]);
     // slices are combined in warp order at the end
@@ -303,6 +311,8 @@ static constexpr int LNR_SLICES = 32;
 __global__ void __launch_bounds__(32 * LNR_SLICES)
 ln_param_reduce(const float* __restrict__ partial, int nblocks, int C, float* __restrict__ dg,
                 float* __restrict__ db, float* __restrict__ dsum) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float sm[3][LNR_SLICES][33];
     const int cx = threadIdx.x & 31, sl = threadIdx.x >> 5;
     const int c = blockIdx.x * 32 + cx;
@@ -349,14 +359,14 @@ cudaError_t layernorm_fwd(const float* x, const Act* y, float* x_out, const floa
         switch (C / 128) {
 #define LNV(V)                                                                                      \
     case V:                                                                                         \
-        ln_fwd_vec<Act, V><<<blocks, LN_WARPS * 32, 0, s>>>(x, y, x_out, g, b, u, mu, rstd, M, C);            \
+        (void)pdl_launch(ln_fwd_vec<Act, V>, blocks, LN_WARPS * 32, 0, s, x, y, x_out, g, b, u, mu, rstd, M, C);            \
         return cudaGetLastError();
             LNV(1) LNV(2) LNV(3) LNV(4) LNV(5) LNV(6) LNV(7) LNV(8)
             LNV(9) LNV(10) LNV(11) LNV(12) LNV(13) LNV(14) LNV(15) LNV(16)
 #undef LNV
         }
     }
-#define LNF(E) ln_fwd_kernel<Act, E><<<blocks, LN_WARPS * 32, 0, s>>>(x, y, x_out, g, b, u, mu, rstd, M, C)
+#define LNF(E) (void)pdl_launch(ln_fwd_kernel<Act, E>, blocks, LN_WARPS * 32, 0, s, x, y, x_out, g, b, u, mu, rstd, M, C)
     LN_DISPATCH(2, LNF)
     LN_DISPATCH(4, LNF)
     LN_DISPATCH(8, LNF)
@@ -372,7 +382,7 @@ cudaError_t layernorm_fwd(const float* x, const Act* y, float* x_out, const floa
 
 cudaError_t layernorm_bwd_params(const float* partial, int M, int C, float* dg, float* db, float* dsum,
                                  cudaStream_t s) {
-    ln_param_reduce<<<(C + 31) / 32, 32 * LNR_SLICES, 0, s>>>(partial, ln_bwd_blocks(M), C, dg, db, dsum);
+    (void)pdl_launch(ln_param_reduce, (C + 31) / 32, 32 * LNR_SLICES, 0, s, partial, ln_bwd_blocks(M), C, dg, db, dsum);
     return cudaGetLastError();
 }
 
@@ -391,7 +401,7 @@ cudaError_t layernorm_bwd_rows(const Act* du, const float* x, const float* g, co
     case V:                                                                                        \
         cudaFuncSetAttribute(ln_bwd_vec<Act, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,      \
                              (int)smem);                                                           \
-        ln_bwd_vec<Act, V><<<blocks, LN_WARPS * 32, smem, s>>>(du, x, g, mu, rstd, dres, dres_act, \
+        (void)pdl_launch(ln_bwd_vec<Act, V>, blocks, LN_WARPS * 32, smem, s, du, x, g, mu, rstd, dres, dres_act, \
                                                                accumulate ? 1 : 0, want_sum,       \
                                                                partial, M, C);                     \
         e = cudaGetLastError();                                                                    \
@@ -405,7 +415,7 @@ cudaError_t layernorm_bwd_rows(const Act* du, const float* x, const float* g, co
     do {                                                                                        \
         cudaFuncSetAttribute(ln_bwd_kernel<Act, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              (int)smem);                                                        \
-        ln_bwd_kernel<Act, E><<<blocks, LN_WARPS * 32, smem, s>>>(                              \
+        (void)pdl_launch(ln_bwd_kernel<Act, E>, blocks, LN_WARPS * 32, smem, s,                               \
             du, x, g, mu, rstd, dres, dres_act, accumulate ? 1 : 0, want_sum, partial, M, C);   \
         e = cudaGetLastError();                                                                 \
     } while (0)

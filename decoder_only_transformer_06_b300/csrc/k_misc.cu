@@ -25,6 +25,8 @@ int num_sms() {
 // cross-entropy gradient scale 1 / (n_valid * grad_accum_steps).
 __global__ void validate_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ tgt,
                                 int M, int V, DevState* st, int accum) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_cnt[32];
     __shared__ unsigned s_err[32];
     int cnt = 0;
@@ -59,7 +61,7 @@ __global__ void validate_kernel(const int32_t* __restrict__ tok, const int32_t* 
 
 cudaError_t validate_inputs(const int32_t* tok, const int32_t* tgt, int M, int V, DevState* st,
                             int accum, cudaStream_t s) {
-    validate_kernel<<<1, 1024, 0, s>>>(tok, tgt, M, V, st, accum);
+    (void)pdl_launch(validate_kernel, 1, 1024, 0, s, tok, tgt, M, V, st, accum);
     return cudaGetLastError();
 }
 
@@ -69,6 +71,8 @@ cudaError_t validate_inputs(const int32_t* tok, const int32_t* tgt, int M, int V
 __global__ void embed_fwd_kernel(const int32_t* __restrict__ tok, const float4* __restrict__ wte,
                                  const float4* __restrict__ wpe, float4* __restrict__ x, int M,
                                  int T, int C4, int V) {
+    pdl_wait();
+    pdl_trigger();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int64_t n = (int64_t)M * C4;
     if (i >= n) return;
@@ -83,7 +87,7 @@ cudaError_t embed_fwd(const int32_t* tok, const float* wte, const float* wpe, fl
                       int T, int C, int V, cudaStream_t s) {
     int C4 = C / 4;
     int64_t n = (int64_t)M * C4;
-    embed_fwd_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+    (void)pdl_launch(embed_fwd_kernel, (unsigned)((n + 255) / 256), 256, 0, s, 
         tok, (const float4*)wte, (const float4*)wpe, (float4*)x, M, T, C4, V);
     return cudaGetLastError();
 }
@@ -100,6 +104,8 @@ static constexpr int EMB_R = 32;
 __global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restrict__ tok, int M,
                                                           int V, int P2, int* __restrict__ s_tok,
                                                           int* __restrict__ s_pos) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint32_t keys[];
     for (int i = threadIdx.x; i < P2; i += blockDim.x) {
         if (i < M) {
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restr
 __global__ void embed_chunk_kernel(const int* __restrict__ s_tok, const int* __restrict__ s_pos,
                                    const float4* __restrict__ dx, float4* __restrict__ dwte,
                                    float4* __restrict__ carry, int M, int C4) {
+    pdl_wait();
+    pdl_trigger();
     int c = threadIdx.x;
     if (c >= C4) return;
     int i0 = blockIdx.x * EMB_R;
@@ -163,6 +171,8 @@ __global__ void embed_chunk_kernel(const int* __restrict__ s_tok, const int* __r
 
 __global__ void embed_carry_kernel(const int* __restrict__ s_tok, const float4* __restrict__ carry,
                                    float4* __restrict__ dwte, int M, int C4) {
+    pdl_wait();
+    pdl_trigger();
     int c = threadIdx.x;
     if (c >= C4) return;
     int i0 = blockIdx.x * EMB_R;
@@ -186,6 +196,8 @@ __global__ void embed_carry_kernel(const int* __restrict__ s_tok, const float4* 
 // dwpe[t, :] += sum over b of dx[b*T + t, :], b in increasing order.
 __global__ void embed_pos_kernel(const float4* __restrict__ dx, float4* __restrict__ dwpe, int B,
                                  int T, int C4) {
+    pdl_wait();
+    pdl_trigger();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)T * C4) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -214,7 +226,7 @@ cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cu
     size_t smem = (size_t)P2 * sizeof(uint32_t);
     CUDA_OK(cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem));
-    embed_sort_kernel<<<1, 1024, smem, s>>>(tok, M, V, P2, s_tok, s_pos);
+    (void)pdl_launch(embed_sort_kernel, 1, 1024, smem, s, tok, M, V, P2, s_tok, s_pos);
     return cudaGetLastError();
 }
 
@@ -231,14 +243,14 @@ cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, in
     float* carry = (float*)(((uintptr_t)(s_pos + M) + 255) & ~(uintptr_t)255);
     int C4 = C / 4;
     int chunks = (M + EMB_R - 1) / EMB_R;
-    embed_chunk_kernel<<<chunks, C4, 0, s>>>(s_tok, s_pos, (const float4*)dx, (float4*)dwte,
+    (void)pdl_launch(embed_chunk_kernel, chunks, C4, 0, s, s_tok, s_pos, (const float4*)dx, (float4*)dwte,
                                              (float4*)carry, M, C4);
     CUDA_OK(cudaGetLastError());
-    embed_carry_kernel<<<chunks, C4, 0, s>>>(s_tok, (const float4*)carry, (float4*)dwte, M, C4);
+    (void)pdl_launch(embed_carry_kernel, chunks, C4, 0, s, s_tok, (const float4*)carry, (float4*)dwte, M, C4);
     CUDA_OK(cudaGetLastError());
     int B = M / T;
     int64_t n = (int64_t)T * C4;
-    embed_pos_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const float4*)dx, (float4*)dwpe,
+    (void)pdl_launch(embed_pos_kernel, (unsigned)((n + 255) / 256), 256, 0, s, (const float4*)dx, (float4*)dwpe,
                                                                  B, T, C4);
     return cudaGetLastError();
 }
@@ -254,6 +266,8 @@ static constexpr int CS_ROWS_PER_SPLIT = 256;
 template <typename T>
 __global__ void __launch_bounds__(256)
 colsum_stage1(const T* __restrict__ dy, int64_t ld, int M, int N, float* __restrict__ partial) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int VEC = 16 / sizeof(T);
     __shared__ float sm[8][32 * VEC + 1];
     const int n = (blockIdx.x * 32 + threadIdx.x) * VEC;
@@ -299,6 +313,8 @@ colsum_stage1(const T* __restrict__ dy, int64_t ld, int M, int N, float* __restr
 // combined in slice order (deterministic).
 __global__ void __launch_bounds__(256)
 colsum_stage2(const float* __restrict__ partial, int splits, int N, float* __restrict__ db) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float sm[8][33];
     const int cx = threadIdx.x & 31, sl = threadIdx.x >> 5;
     const int n = blockIdx.x * 32 + cx;
@@ -326,9 +342,9 @@ cudaError_t colsum_add(const T* dy, int64_t ld, int M, int N, float* db, float* 
     if ((N % VEC) || (ld % VEC) || ((uintptr_t)dy & 15)) return cudaErrorInvalidValue;
     int splits = (M + CS_ROWS_PER_SPLIT - 1) / CS_ROWS_PER_SPLIT;
     dim3 grid((N / VEC + 31) / 32, splits);
-    colsum_stage1<T><<<grid, dim3(32, 8), 0, s>>>(dy, ld, M, N, partial);
+    (void)pdl_launch(colsum_stage1<T>, grid, dim3(32, 8), 0, s, dy, ld, M, N, partial);
     CUDA_OK(cudaGetLastError());
-    colsum_stage2<<<(N + 31) / 32, 256, 0, s>>>(partial, splits, N, db);
+    (void)pdl_launch(colsum_stage2, (N + 31) / 32, 256, 0, s, partial, splits, N, db);
     return cudaGetLastError();
 }
 template cudaError_t colsum_add<float>(const float*, int64_t, int, int, float*, float*,
@@ -339,6 +355,8 @@ template cudaError_t colsum_add<bf16>(const bf16*, int64_t, int, int, float*, fl
 // ---------------------------------------------------------------- split-K
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int64_t n,
                                      float* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int64_t n4 = n / 4;
     if (i >= n4) return;
@@ -356,13 +374,15 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
 cudaError_t splitk_reduce_add(const float* partial, int splits, int64_t n, float* out,
                               cudaStream_t s) {
     int64_t n4 = n / 4;
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(partial, splits, n, out);
+    (void)pdl_launch(splitk_reduce_kernel, (unsigned)((n4 + 255) / 256), 256, 0, s, partial, splits, n, out);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- conversion
 __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                    int64_t n4) {
+    pdl_wait();
+    pdl_trigger();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     float4 v = src[i];
@@ -376,13 +396,15 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ src, uint2* __rest
 cudaError_t f32_to_bf16(const float* src, bf16* dst, int64_t n, cudaStream_t s) {
     int64_t n4 = n / 4;
     if (n4 == 0) return cudaSuccess;
-    f32_to_bf16_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>((const float4*)src,
+    (void)pdl_launch(f32_to_bf16_kernel, (unsigned)((n4 + 255) / 256), 256, 0, s, (const float4*)src,
                                                                      (uint2*)dst, n4);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- loss mean
 __global__ void loss_reduce_kernel(const float* __restrict__ row_loss, int M, DevState* st) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ double sm[32];
     double acc = 0.0;
     for (int i = threadIdx.x; i < M; i += blockDim.x) acc += (double)row_loss[i];
@@ -398,7 +420,7 @@ __global__ void loss_reduce_kernel(const float* __restrict__ row_loss, int M, De
 }
 
 cudaError_t loss_reduce(const float* row_loss, int M, DevState* st, cudaStream_t s) {
-    loss_reduce_kernel<<<1, 1024, 0, s>>>(row_loss, M, st);
+    (void)pdl_launch(loss_reduce_kernel, 1, 1024, 0, s, row_loss, M, st);
     return cudaGetLastError();
 }
 
@@ -408,6 +430,8 @@ cudaError_t loss_reduce(const float* row_loss, int M, DevState* st, cudaStream_t
 // combined in order by step_finalize.
 __global__ void grad_norm_kernel(const float4* __restrict__ g, int64_t n4, int64_t per_block,
                                  double* __restrict__ partial) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ double sm[32];
     int64_t b0 = (int64_t)blockIdx.x * per_block;
     int64_t b1 = min(b0 + per_block, n4);
@@ -429,7 +453,7 @@ __global__ void grad_norm_kernel(const float4* __restrict__ g, int64_t n4, int64
 cudaError_t grad_norm(const float* g, int64_t n, double* partial, int nparts, cudaStream_t s) {
     int64_t n4 = n / 4;
     int64_t per_block = (n4 + nparts - 1) / nparts;
-    grad_norm_kernel<<<nparts, 512, 0, s>>>((const float4*)g, n4, per_block, partial);
+    (void)pdl_launch(grad_norm_kernel, nparts, 512, 0, s, (const float4*)g, n4, per_block, partial);
     return cudaGetLastError();
 }
 
@@ -438,6 +462,8 @@ cudaError_t grad_norm(const float* g, int64_t n, double* partial, int nparts, cu
 // Stage 5); a non-finite norm skips the update and leaves t unchanged.
 __global__ void step_finalize_kernel(const double* __restrict__ partial, int nparts, float clip,
                                      float beta1, float beta2, DevState* st) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ double sm[32];
     double acc = 0.0;
     for (int i = threadIdx.x; i < nparts; i += blockDim.x) acc += partial[i];
@@ -466,7 +492,7 @@ __global__ void step_finalize_kernel(const double* __restrict__ partial, int npa
 
 cudaError_t step_finalize(const double* partial, int nparts, float clip, float beta1, float beta2,
                           DevState* st, cudaStream_t s) {
-    step_finalize_kernel<<<1, 256, 0, s>>>(partial, nparts, clip, beta1, beta2, st);
+    (void)pdl_launch(step_finalize_kernel, 1, 256, 0, s, partial, nparts, clip, beta1, beta2, st);
     return cudaGetLastError();
 }
 
@@ -479,6 +505,8 @@ __global__ void adamw_kernel(float4* __restrict__ p, const float4* __restrict__ 
                              uint2* __restrict__ pb, int64_t n4, int64_t decay_end4,
                              int64_t bf16_end4, float lr, float beta1, float beta2, float eps,
                              float wd, const DevState* __restrict__ st) {
+    pdl_wait();
+    pdl_trigger();
     if (st->skip) return;
     const float c = st->clip_coef;
     const float inv_bc1 = 1.0f / st->bc1;
@@ -515,7 +543,7 @@ cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* p_bf16, in
     int64_t n4 = n / 4;
     const int64_t want = (n4 + 511) / 512;
     int blocks = want < num_sms() * 4 ? (int)(want > 0 ? want : 1) : num_sms() * 4;
-    adamw_kernel<<<blocks, 512, 0, s>>>((float4*)p, (const float4*)g, (float4*)m, (float4*)v,
+    (void)pdl_launch(adamw_kernel, blocks, 512, 0, s, (float4*)p, (const float4*)g, (float4*)m, (float4*)v,
                                         (uint2*)p_bf16, n4, decay_end / 4,
                                         p_bf16 ? bf16_end / 4 : 0, lr, beta1, beta2, eps, wd, st);
     return cudaGetLastError();

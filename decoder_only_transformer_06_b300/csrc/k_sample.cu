@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(SMP_THREADS)
 sample_kernel(const float* __restrict__ logits, int V, int64_t ld, float temperature, int top_k,
               const float* __restrict__ uni, int32_t* __restrict__ out, int32_t* __restrict__ ctx, int T,
               int t) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float shv[SMP_WARPS];
     __shared__ int shi[SMP_WARPS];
     __shared__ float sh_scan[SMP_WARPS];
@@ -202,7 +204,7 @@ cudaError_t sample(const float* logits, int rows, int V, int64_t ld, float tempe
                                      SMP_KEYS_MAX * 4));
         attr_done.fetch_or(dbit);
     }
-    sample_kernel<<<rows, SMP_THREADS, smem, s>>>(logits, V, ld, temperature, top_k, u, out, ctx, T, t);
+    (void)pdl_launch(sample_kernel, rows, SMP_THREADS, smem, s, logits, V, ld, temperature, top_k, u, out, ctx, T, t);
     return cudaGetLastError();
 }
 
