@@ -93,8 +93,10 @@ cudaError_t embed_fwd(const int32_t* tok, const float* wte, const float* wpe, fl
 }
 
 // Embedding backward, deterministic (no floating-point atomics):
-//  1. one CTA sorts the keys tok*M + m in shared memory (bitonic), so equal
-//     tokens form contiguous segments ordered by position;
+//  1. one CTA sorts the entries by (token, position) in shared memory (a
+//     stable radix sort on the token id; a bitonic sort of tok*M + m for
+//     larger M or V), so equal tokens form contiguous segments ordered by
+//     position;
 //  2. fixed chunks of R sorted entries are summed in order; a segment wholly
 //     inside its chunk is added to dwte directly, otherwise the chunk's partial
 //     goes to a carry slot at the segment's first index in that chunk;
@@ -137,40 +139,182 @@ __global__ void __launch_bounds__(1024) embed_sort_kernel(const int32_t* __restr
     }
 }
 
+// The same order (token, then position) by a stable LSD radix sort over the
+// token id, for V <= 65536 and M <= EMB_RADIX_MAX_M: keys token << 16 | position
+// start in position order; each pass ranks one 8-bit digit of the token.
+// Warp w takes a contiguous slice of the keys in rounds of 32 (lanes in key
+// order, equal digits of a round found with __match_any_sync), so equal digits
+// keep their order within a round, across rounds and across warps: every pass
+// is stable. Also writes, for every chunk of EMB_R sorted entries, the end of
+// the segment that holds the chunk's last entry (seg_end), so that the carry
+// pass needs no search.
+static constexpr int RS_THREADS = 1024, RS_WARPS = RS_THREADS / 32;
+static constexpr int EMB_RADIX_MAX_M = 24576;
+
+__global__ void __launch_bounds__(RS_THREADS) embed_radix_kernel(const int32_t* __restrict__ tok, int M, int V,
+                                                                 int passes, int* __restrict__ s_tok,
+                                                                 int* __restrict__ s_pos,
+                                                                 int* __restrict__ seg_end) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ uint32_t rs_sm[];
+    uint32_t* a = rs_sm;                         // [M]
+    uint32_t* b = rs_sm + M;                     // [M]
+    uint32_t* cnt = rs_sm + 2 * M;               // [RS_WARPS][256]: counts, then running bases
+    __shared__ uint32_t wsum[RS_WARPS];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = threadIdx.x; i < M; i += RS_THREADS) {
+        int t = tok[i];
+        t = t < 0 ? 0 : (t >= V ? V - 1 : t);
+        a[i] = ((uint32_t)t << 16) | (uint32_t)i;
+    }
+    const int per = (M + RS_WARPS - 1) / RS_WARPS;
+    const int w0 = min(M, warp * per), w1 = min(M, w0 + per);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int pass = 0; pass < passes; pass++) {
+        const int shift = 16 + 8 * pass;
+        for (int i = threadIdx.x; i < 256 * RS_WARPS; i += RS_THREADS) cnt[i] = 0u;
+        __syncthreads();
+        for (int r = w0; r < w1; r += 32) {
+            const int i = r + lane;
+            const bool v = i < w1;
+            const uint32_t d = v ? (a[i] >> shift) & 255u : 256u;
+            const unsigned peers = __match_any_sync(0xffffffffu, d);
+            if (v && (peers & lt) == 0u) cnt[warp * 256 + d] += (uint32_t)__popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        // exclusive scan over (digit, warp) in digit-major order: logical index
+        // j = d * RS_WARPS + w at cnt[w * 256 + d]; thread t owns j = 8t .. 8t+7
+        {
+            uint32_t loc[8], sum = 0u;
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int j = threadIdx.x * 8 + k;
+                loc[k] = cnt[(j % RS_WARPS) * 256 + j / RS_WARPS];
+                sum += loc[k];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) wsum[warp] = incl;
+            __syncthreads();
+            uint32_t before = 0u;
+            for (int w = 0; w < warp; w++) before += wsum[w];
+            uint32_t ex = before + incl - sum;
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int j = threadIdx.x * 8 + k;
+                cnt[(j % RS_WARPS) * 256 + j / RS_WARPS] = ex;
+                ex += loc[k];
+            }
+        }
+        __syncthreads();
+        for (int r = w0; r < w1; r += 32) {
+            const int i = r + lane;
+            const bool v = i < w1;
+            const uint32_t key = v ? a[i] : 0u;
+            const uint32_t d = v ? (key >> shift) & 255u : 256u;
+            const unsigned peers = __match_any_sync(0xffffffffu, d);
+            const uint32_t base = v ? cnt[warp * 256 + d] : 0u;
+            __syncwarp();
+            if (v) {
+                b[base + (uint32_t)__popc(peers & lt)] = key;
+                if ((peers & lt) == 0u) cnt[warp * 256 + d] = base + (uint32_t)__popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        uint32_t* t = a;
+        a = b;
+        b = t;
+    }
+    for (int i = threadIdx.x; i < M; i += RS_THREADS) {
+        s_tok[i] = (int)(a[i] >> 16);
+        s_pos[i] = (int)(a[i] & 0xffffu);
+    }
+    const int chunks = (M + EMB_R - 1) / EMB_R;
+    for (int c = threadIdx.x; c < chunks; c += RS_THREADS) {
+        const int last = min(M, (c + 1) * EMB_R) - 1;
+        const uint32_t t = a[last] >> 16;
+        int lo = last + 1, hi = M;                  // first entry after last with another token
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if ((a[mid] >> 16) == t) lo = mid + 1;
+            else hi = mid;
+        }
+        seg_end[c] = lo;
+    }
+}
+
+// seg_end for the bitonic path: per chunk, the end of the segment that holds
+// its last sorted entry (binary search over the sorted tokens).
+__global__ void embed_seg_end_kernel(const int* __restrict__ s_tok, int M, int* __restrict__ seg_end) {
+    pdl_wait();
+    pdl_trigger();
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= (M + EMB_R - 1) / EMB_R) return;
+    const int last = min(M, (c + 1) * EMB_R) - 1;
+    const int t = s_tok[last];
+    int lo = last + 1, hi = M;
+    while (lo < hi) {
+        const int mid = (lo + hi) / 2;
+        if (s_tok[mid] == t) lo = mid + 1;
+        else hi = mid;
+    }
+    seg_end[c] = lo;
+}
+
 __global__ void embed_chunk_kernel(const int* __restrict__ s_tok, const int* __restrict__ s_pos,
                                    const float4* __restrict__ dx, float4* __restrict__ dwte,
                                    float4* __restrict__ carry, int M, int C4) {
     pdl_wait();
     pdl_trigger();
-    int c = threadIdx.x;
+    // the chunk's entries, with the tokens just before and after it, staged in
+    // shared memory so that the row loads below do not wait on index loads
+    __shared__ int st[EMB_R + 2], sp[EMB_R];
+    const int i0 = blockIdx.x * EMB_R;
+    const int i1 = min(i0 + EMB_R, M);
+    const int n = i1 - i0;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        st[j + 1] = s_tok[i0 + j];
+        sp[j] = s_pos[i0 + j];
+    }
+    if (threadIdx.x == 0) {
+        st[0] = i0 > 0 ? s_tok[i0 - 1] : -1;
+        st[n + 1] = i1 < M ? s_tok[i1] : -1;
+    }
+    __syncthreads();
+    const int c = threadIdx.x;
     if (c >= C4) return;
-    int i0 = blockIdx.x * EMB_R;
-    int i1 = min(i0 + EMB_R, M);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int seg = i0;
-    for (int i = i0; i < i1; i++) {
-        int t = s_tok[i];
-        float4 v = dx[(int64_t)s_pos[i] * C4 + c];
+    int seg = 0;
+#pragma unroll 8
+    for (int j = 0; j < n; j++) {
+        const int t = st[j + 1];
+        const float4 v = dx[(int64_t)sp[j] * C4 + c];
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        bool last = (i + 1 == i1) || (s_tok[i + 1] != t);
-        if (last) {
-            bool from_before = (seg == i0) && (i0 > 0) && (s_tok[i0 - 1] == t);
-            bool to_after = (i + 1 == i1) && (i1 < M) && (s_tok[i1] == t);
+        if (st[j + 2] != t || j + 1 == n) {
+            const bool from_before = seg == 0 && st[0] == t;
+            const bool to_after = j + 1 == n && st[n + 1] == t;
             if (!from_before && !to_after) {
                 float4* w = dwte + (int64_t)t * C4 + c;
-                float4 o = *w;
+                const float4 o = *w;
                 *w = make_float4(o.x + acc.x, o.y + acc.y, o.z + acc.z, o.w + acc.w);
             } else {
-                carry[(int64_t)seg * C4 + c] = acc;
+                carry[(int64_t)(i0 + seg) * C4 + c] = acc;
             }
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            seg = i + 1;
+            seg = j + 1;
         }
     }
 }
 
-__global__ void embed_carry_kernel(const int* __restrict__ s_tok, const float4* __restrict__ carry,
-                                   float4* __restrict__ dwte, int M, int C4) {
+__global__ void embed_carry_kernel(const int* __restrict__ s_tok, const int* __restrict__ seg_end,
+                                   const float4* __restrict__ carry, float4* __restrict__ dwte, int M, int C4) {
     pdl_wait();
     pdl_trigger();
     int c = threadIdx.x;
@@ -184,8 +328,11 @@ __global__ void embed_carry_kernel(const int* __restrict__ s_tok, const float4* 
     while (s > i0 && s_tok[s - 1] == t) s--;
     if (s == i0 && i0 > 0 && s_tok[i0 - 1] == t) return;   // owned by an earlier chunk
     float4 acc = carry[(int64_t)s * C4 + c];
-    for (int b = i1; b < M && s_tok[b] == t; b += EMB_R) {
-        float4 v = carry[(int64_t)b * C4 + c];
+    // the later chunks' pieces start at their first entry, up to the segment's end
+    const int e = seg_end[blockIdx.x];
+#pragma unroll 4
+    for (int b = i1; b < e; b += EMB_R) {
+        const float4 v = carry[(int64_t)b * C4 + c];
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     float4* w = dwte + (int64_t)t * C4 + c;
@@ -215,18 +362,32 @@ static int pow2_at_least(int m) {
     return p;
 }
 
+// workspace: s_tok [M], s_pos [M], one spare word and seg_end [chunks] (ints),
+// then the carries (fp32 [M, C], 256-byte aligned)
+static int emb_chunks(int M) { return (M + EMB_R - 1) / EMB_R; }
 size_t embed_bwd_workspace(int M, int C) {
-    return (size_t)2 * M * sizeof(int) + (size_t)M * C * sizeof(float) + 256;
+    return (size_t)(2 * M + 1 + emb_chunks(M)) * sizeof(int) + (size_t)M * C * sizeof(float) + 256;
 }
 
 cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cudaStream_t s) {
     int* s_tok = (int*)workspace;
     int* s_pos = s_tok + M;
+    int* seg_end = s_pos + M + 1;
+    if (V <= 65536 && M <= EMB_RADIX_MAX_M) {
+        const size_t smem = ((size_t)2 * M + 256 * RS_WARPS) * sizeof(uint32_t);
+        CUDA_OK(cudaFuncSetAttribute(embed_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem));
+        (void)pdl_launch(embed_radix_kernel, 1, RS_THREADS, smem, s, tok, M, V, V <= 256 ? 1 : 2, s_tok,
+                         s_pos, seg_end);
+        return cudaGetLastError();
+    }
     int P2 = pow2_at_least(M);
     size_t smem = (size_t)P2 * sizeof(uint32_t);
     CUDA_OK(cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem));
     (void)pdl_launch(embed_sort_kernel, 1, 1024, smem, s, tok, M, V, P2, s_tok, s_pos);
+    CUDA_OK(cudaGetLastError());
+    (void)pdl_launch(embed_seg_end_kernel, (emb_chunks(M) + 255) / 256, 256, 0, s, s_tok, M, seg_end);
     return cudaGetLastError();
 }
 
@@ -240,13 +401,15 @@ cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, in
                             void* workspace, cudaStream_t s) {
     int* s_tok = (int*)workspace;
     int* s_pos = s_tok + M;
-    float* carry = (float*)(((uintptr_t)(s_pos + M) + 255) & ~(uintptr_t)255);
+    float* carry = (float*)(((uintptr_t)(s_pos + M + 1 + emb_chunks(M)) + 255) & ~(uintptr_t)255);
     int C4 = C / 4;
     int chunks = (M + EMB_R - 1) / EMB_R;
     (void)pdl_launch(embed_chunk_kernel, chunks, C4, 0, s, s_tok, s_pos, (const float4*)dx, (float4*)dwte,
                                              (float4*)carry, M, C4);
     CUDA_OK(cudaGetLastError());
-    (void)pdl_launch(embed_carry_kernel, chunks, C4, 0, s, s_tok, (const float4*)carry, (float4*)dwte, M, C4);
+    const int* seg_end = s_pos + M + 1;      // written by embed_bwd_sort
+    (void)pdl_launch(embed_carry_kernel, chunks, C4, 0, s, s_tok, seg_end, (const float4*)carry, (float4*)dwte,
+                     M, C4);
     CUDA_OK(cudaGetLastError());
     int B = M / T;
     int64_t n = (int64_t)T * C4;

@@ -217,6 +217,19 @@ def test_char_bf16_loss_trajectory():
 
 
 @pytest.mark.slow
+def test_full_vocabulary_fp32_embedding_gradients():
+    """fp32-math mode at GPT-2's vocabulary and sequence length with Zipf-hot
+    ids (4,096 rows): the embedding backward's token sort runs both 8-bit
+    passes of the radix sort and the hot tokens' segments span many chunks
+    (the carry pass); every gradient, wte and wpe included, within 1e-4 of the
+    oracle."""
+    c = O.Config(n_layer=1, n_head=2, d_model=64, vocab_size=50257, padded_vocab=50304,
+                 block_size=1024, batch_size=4, seq_len=1024)
+    r = _compare_step(c, gpt2.GPT2_FP32, "zipf", lr=6e-4)
+    _check_fp32(r)
+    _pad_rows_zero(r)
+
+
 def test_gpt2_width_full_batch_bf16_gradients():
     """The benchmark's batch shape (B=16, T=1024: 16,384 rows) at GPT-2 width
     and full vocabulary with two layers: every gradient against the oracle.
