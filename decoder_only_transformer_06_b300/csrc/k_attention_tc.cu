@@ -48,6 +48,13 @@ constexpr int AT_SLOTS = 5;                    // K and V ring depth (32 KB a sl
 constexpr int FW_THREADS = 384;                // forward: 8 softmax warps, producer, three MMA issuers
 constexpr int FW_PRODUCER = 8, FW_ISSUE_S = 9, FW_ISSUE_PV = 10;   // P V issuers: warps 10, 11
 constexpr int FW_SBUF = 3;                     // S buffers in TMEM
+// Registers: the launch gives each of the 384 threads FW_REGS; the producer
+// and issuer warpgroup (warps 8..11) then drops to FW_REGS_LOW and the two
+// softmax warpgroups rise to FW_REGS_HIGH (setmaxnreg). The shares must add up
+// to no more than the launch's total, or the increase would wait forever; the
+// host checks that the kernel was compiled with FW_REGS registers.
+constexpr int FW_REGS = 168, FW_REGS_LOW = 56, FW_REGS_HIGH = 224;
+static_assert(4 * FW_REGS_LOW + 8 * FW_REGS_HIGH <= 12 * FW_REGS, "register split exceeds the launch");
 constexpr int OFF_Q = 0;                       // Q double buffer
 constexpr int OFF_K = OFF_Q + 2 * AT_TILE;
 constexpr int OFF_V = OFF_K + AT_SLOTS * AT_TILE;
@@ -125,6 +132,9 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
     const uint32_t tmem_base = *tmem_slot;
     pdl_wait();                              // the previous kernel's outputs are visible
 
+    if (warp >= FW_PRODUCER) {
+    // one register-split instruction per warpgroup (all four warps run it)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(FW_REGS_LOW));
     if (warp == FW_PRODUCER) {
         if (lane == 0) {
             // ---------------- TMA producer
@@ -191,7 +201,7 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 wait_bounded(&drain[0], 0);
             }
         }
-    } else if (warp == FW_ISSUE_PV || warp == FW_ISSUE_PV + 1) {
+    } else {
         if (lane == 0) {
             // ---------------- O_hf += P_hf V_hf issuer, hf = warp - 10 (P from TMEM,
             // V rows 64 hf .. +63 read MN-major)
@@ -226,9 +236,11 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 wait_bounded(&drain[1 + hf], 0);
             }
         }
+    }
     } else {
         // ---------------- softmax warps 0..7: warp w owns rows r = 32 (w % 4) + lane
         // (TMEM lane r) and the key half hf = w / 4 of every block
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(FW_REGS_HIGH));
         const int q4 = warp & 3, hf = warp >> 2;
         const int r = q4 * 32 + lane;
         const float sl2 = LOG2E_F * 0.125f;   // log2(e) / sqrt(64)
@@ -236,8 +248,60 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
         uint8_t* slab = smem + OFF_OUT + q4 * OUT_SLAB + hf * (OUT_SLAB / 2);
         bool ok = true;
         int g = 0, it = 0;
+        // The output of an item is written after the first key block of the
+        // next one (its last P V products have landed by then, so nothing waits
+        // for them). The pending item is the previous one of this CTA: work
+        // item p_w, item count p_it, its last key block p_GL.
+        auto item_output = [&](int p_w, int p_it, int p_GL) -> bool {
+            const int p_qb = nqb - 1 - p_w / BH, p_bh = p_w % BH;
+            const int p_h = p_bh % H, p_b = p_bh / H, pq = p_qb * AT_BQ + r, pob = p_it & 1;
+            bool okk = mbar_wait(&pv_done[p_GL % FW_SBUF], (uint32_t)((p_GL / FW_SBUF) & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, okk)) return false;
+            okk = mbar_wait(&ml_full[pob], (uint32_t)((p_it >> 1) & 1), abort_flag);
+            if (!__all_sync(0xffffffffu, okk)) return false;
+            // each half writes output columns 32 hf .. 32 hf + 31 of its rows
+            // from both O halves
+            const float2 ml0 = sML[(pob * 2) * 128 + r], ml1 = sML[(pob * 2 + 1) * 128 + r];
+            const float M = fmaxf(ml0.x, ml1.x);
+            const float w0 = ml0.x == -INFINITY ? 0.f : ex2f(ml0.x - M);
+            const float w1 = ml1.x == -INFINITY ? 0.f : ex2f(ml1.x - M);
+            const float l_row = ml0.y * w0 + ml1.y * w1;
+            const float a0 = w0 / l_row, a1 = w1 / l_row;
+            tc_fence_after();
+            if (lane == 0) tma_wait_read<0>();           // the previous output store has read the slab
+            __syncwarp();
+#pragma unroll 1
+            for (int k2 = 0; k2 < 2; k2++) {
+                uint32_t o0[16], o1[16];
+                tmem_ld16_nowait(lane_base + TM_O + 32 * hf + 16 * k2, o0);
+                tmem_ld16_nowait(lane_base + TM_O + 64 + 32 * hf + 16 * k2, o1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int pc = 0; pc < 2; pc++) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++)
+                        v[e] = __uint_as_float(o0[8 * pc + e]) * a0 + __uint_as_float(o1[8 * pc + e]) * a1;
+                    const int piece = 2 * k2 + pc;
+                    *(uint4*)(slab + lane * 64 + ((piece ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
+                                   pack2_bf16(v[6], v[7]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&tm_out, slab, p_h * AT_HS + 32 * hf, p_qb * AT_BQ + q4 * 32, p_b);
+                tma_commit();
+            }
+            if (hf == 0 && pq < T) lse[(int64_t)p_bh * T + pq] = (M + log2f(l_row)) * LN2;
+            return true;
+        };
         for (int w = blockIdx.x; w < items && ok; w += gridDim.x, it++) {
-            const int qb = nqb - 1 - w / BH, bh = w % BH, h = bh % H, b = bh / H;
+            const int qb = nqb - 1 - w / BH;
             const int nkv = qb + 1;
             const int q = qb * AT_BQ + r;
             const int ob = it & 1;                 // the (m, l) hand-off buffer
@@ -320,60 +384,20 @@ fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[2 * sb + hf]);
+                if (j == 0 && it > 0) {
+                    ok = item_output(w - (int)gridDim.x, it - 1, g - 1);
+                    if (!ok) break;
+                }
             }
             if (!ok) break;
-            // the item's output once its last P V products are done
-            const int GL = g + nkv - 1;
-            ok = mbar_wait(&pv_done[GL % FW_SBUF], (uint32_t)((GL / FW_SBUF) & 1), abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            // the two halves exchange (m, l); each then writes output columns
-            // 32 hf .. 32 hf + 31 of its rows from both O halves
+            // hand this half's (m, l) to the item's output, written after the
+            // next item's first key block
             sML[(ob * 2 + hf) * 128 + r] = make_float2(m_run, l_run);
             __syncwarp();
             if (lane == 0) mbar_arrive(&ml_full[ob]);
-            ok = mbar_wait(&ml_full[ob], (uint32_t)((it >> 1) & 1), abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            {
-                const float2 ml0 = sML[(ob * 2) * 128 + r], ml1 = sML[(ob * 2 + 1) * 128 + r];
-                const float M = fmaxf(ml0.x, ml1.x);
-                const float w0 = ml0.x == -INFINITY ? 0.f : ex2f(ml0.x - M);
-                const float w1 = ml1.x == -INFINITY ? 0.f : ex2f(ml1.x - M);
-                const float l_row = ml0.y * w0 + ml1.y * w1;
-                const float a0 = w0 / l_row, a1 = w1 / l_row;
-                tc_fence_after();
-                if (lane == 0) tma_wait_read<0>();           // the previous item's store has read the slab
-                __syncwarp();
-#pragma unroll 1
-                for (int k2 = 0; k2 < 2; k2++) {
-                    uint32_t o0[16], o1[16];
-                    tmem_ld16_nowait(lane_base + TM_O + 32 * hf + 16 * k2, o0);
-                    tmem_ld16_nowait(lane_base + TM_O + 64 + 32 * hf + 16 * k2, o1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int pc = 0; pc < 2; pc++) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; e++)
-                            v[e] = __uint_as_float(o0[8 * pc + e]) * a0 + __uint_as_float(o1[8 * pc + e]) * a1;
-                        const int piece = 2 * k2 + pc;
-                        *(uint4*)(slab + lane * 64 + ((piece ^ ((lane >> 1) & 3)) << 4)) =
-                            make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
-                                       pack2_bf16(v[6], v[7]));
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(o_free);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&tm_out, slab, h * AT_HS + 32 * hf, qb * AT_BQ + q4 * 32, b);
-                    tma_commit();
-                }
-                if (hf == 0 && q < T) lse[(int64_t)bh * T + q] = (M + log2f(l_row)) * LN2;
-            }
             g += nkv;
         }
+        if (ok && it > 0) ok = item_output(blockIdx.x + (it - 1) * (int)gridDim.x, it - 1, g - 1);
         if (lane == 0) tma_wait_all();
     }
     __syncthreads();
@@ -400,6 +424,10 @@ cudaError_t attention_fwd_bf16(const bf16* qkv, bf16* out, float* lse, int B, in
     static std::atomic<unsigned long long> attr_done{0};   // per device
     const unsigned long long dbit = device_bit();
     if (!(attr_done.load() & dbit)) {
+        // the register split assumes the launch's FW_REGS per thread
+        cudaFuncAttributes fa;
+        CUDA_OK(cudaFuncGetAttributes(&fa, fa_tc_fwd_kernel));
+        if (fa.numRegs != FW_REGS) return cudaErrorInvalidConfiguration;
         CUDA_OK(cudaFuncSetAttribute(fa_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)AT_SMEM));
         attr_done.fetch_or(dbit);
