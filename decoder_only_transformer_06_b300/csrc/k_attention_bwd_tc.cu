@@ -81,6 +81,14 @@ constexpr size_t DQ_SMEM = DQ_OFF_BAR + 512 + 1024;
 // dQ TMEM columns: S[2] 0..127, dP[2] 128..255, dQ[2] 256..383 (by item),
 // dS[2] 384..447 (bf16 pairs)
 constexpr uint32_t DQ_TM_S = 0, DQ_TM_DP = 128, DQ_TM_DQ = 256, DQ_TM_DS = 384;
+// dQ kernel registers: the launch gives each of the 640 threads DQ_REGS; the
+// producer and issuer warpgroup (warps 16..19) drops to DQ_REGS_LOW and the
+// four elementwise warpgroups rise to DQ_REGS_HIGH (setmaxnreg). The shares
+// must add up to no more than the launch's total, or the increase would wait
+// forever; the host checks that the kernel was compiled with DQ_REGS.
+constexpr int DQ_REGS = 96, DQ_REGS_LOW = 56, DQ_REGS_HIGH = 104;
+static_assert(4 * DQ_REGS_LOW + 16 * DQ_REGS_HIGH <= 20 * DQ_REGS, "register split exceeds the launch");
+static_assert(DQ_THREADS == 640 && BW_PRODUCER == 16, "warpgroup layout of the dQ kernel");
 constexpr uint32_t BW_TMEM_COLS = 512;
 
 // Four K=16 products of a 64-row step into one accumulator: D (+)= A B over
@@ -441,6 +449,9 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // sub-blocks of the item whose query block is qb: keys 0 .. min(T, 128 qb + 128)
     auto nsub = [&](int qb) { return min(nsb, 2 * qb + 2); };
 
+    if (warp >= BW_PRODUCER) {
+    // one register-split instruction per warpgroup (all four warps run it)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(DQ_REGS_LOW));
     if (warp == BW_PRODUCER) {
         if (lane == 0) {
             // ---------------- TMA producer
@@ -524,7 +535,9 @@ fa_tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 wait_bounded(&drain[role], 0);
             }
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(DQ_REGS_HIGH));
         // ---------------- warps 0..15: warp w reads TMEM lane quarter q4 = w % 4
         // (thread row r = query r of the item) and key columns 16 cg .. +15 of
         // each 64-key sub-block, cg = w / 4
@@ -670,6 +683,10 @@ cudaError_t attention_bwd_tc(const bf16* qkv, const bf16* out, const bf16* dout,
     static std::atomic<unsigned long long> attr_done{0};   // per device
     const unsigned long long dbit = device_bit();
     if (!(attr_done.load() & dbit)) {
+        // the dQ kernel's register split assumes the launch's DQ_REGS per thread
+        cudaFuncAttributes fa;
+        CUDA_OK(cudaFuncGetAttributes(&fa, fa_tc_bwd_dq_kernel));
+        if (fa.numRegs != DQ_REGS) return cudaErrorInvalidConfiguration;
         CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)KV_SMEM));
         CUDA_OK(cudaFuncSetAttribute(fa_tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
