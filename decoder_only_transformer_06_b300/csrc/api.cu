@@ -1116,6 +1116,12 @@ int gpt2_get_loss(gpt2_model* m, float* h_loss) {
     return GPT2_OK;
 }
 
+int gpt2_get_loss_async(gpt2_model* m, float* h_loss) {
+    if (!m || !h_loss) return GPT2_EINVAL;
+    CK(m, cudaMemcpyAsync(h_loss, &m->st->loss, sizeof(float), cudaMemcpyDeviceToHost, m->stream));
+    return GPT2_OK;
+}
+
 int gpt2_num_tensors(const gpt2_model* m) { return m ? (int)m->tensors.size() : GPT2_EINVAL; }
 
 int gpt2_tensor_info(const gpt2_model* m, int i, const char** name, int* ndim, int64_t shape[2],

@@ -67,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "gpt2_lr_schedule": (D, [I64, I64, I64, D, D]),
         "gpt2_sync": (I, [P]),
         "gpt2_get_loss": (I, [P, FP]),
+        "gpt2_get_loss_async": (I, [P, P]),
         "gpt2_set_wait_limit": (I, [P, ctypes.c_uint]),
         "gpt2_join": (I, [P]),
         "gpt2_num_tensors": (I, [P]),
@@ -250,6 +251,12 @@ class GPT2:
         v = ctypes.c_float()
         self._ck(_lib.gpt2_get_loss(self.h, ctypes.byref(v)))
         return v.value
+
+    def loss_async(self, out) -> None:
+        """Enqueue a copy of the last forward's loss into out (a float32 CPU
+        tensor of one element, pinned for the copy to be asynchronous) on the
+        model's stream; it is valid after the next sync."""
+        self._ck(_lib.gpt2_get_loss_async(self.h, ctypes.c_void_p(out.data_ptr())))
 
     def num_tensors(self) -> int:
         return _lib.gpt2_num_tensors(self.h)

@@ -220,6 +220,14 @@ int gpt2_join(gpt2_model* model);
 /* Mean loss of the last forward with targets (synchronises). */
 int gpt2_get_loss(gpt2_model* model, float* h_loss);
 
+/* Enqueue a copy of the last forward's mean loss into h_loss (4 bytes of host
+ * memory, page-locked for the copy to be asynchronous) on the model's stream,
+ * without synchronising: the value is there once the stream has reached this
+ * point (e.g. after gpt2_sync). A training loop reads the loss of every step
+ * this way without stalling the device. Device-side conditions are reported by
+ * the next synchronising call. Errors: EINVAL (NULL pointers). */
+int gpt2_get_loss_async(gpt2_model* model, float* h_loss);
+
 /* Testing hook for failure detection (no counterpart on the pages). Every
  * pipeline wait inside the library's single-CTA tensor-core kernels gives up
  * after `cycles` SM cycles (0 restores the default, about two seconds), after
