@@ -514,7 +514,10 @@ struct Op {
         double ob = (e.kind == EPI_RESID || e.kind == EPI_ACCUM_F32) ? 8.0 : (e.kind == EPI_GELU ? 2 * ab : ab);
         if (e.kind == EPI_GELU_BWD) ob = 2 * ab;
         bytes += ob * (double)M * N;
-        if (m->use_bf16)
+        if (m->use_bf16 && k::gemm_rows_supported(M, N, K, A, B, e))
+            // a handful of rows (generation): weight streaming, no tensor-core tiles
+            RUN(m, site, 1, 2.0 * M * N * K, bytes, k::gemm_rows_bf16(M, N, K, A, B, e, m->stream));
+        else if (m->use_bf16)
             RUN(m, site, 1, 2.0 * M * N * K, bytes, k::gemm_bf16_tc(M, N, K, A, B, e, 1, m->st, m->stream));
         else
             RUN(m, site, 1, 2.0 * M * N * K, bytes, k::gemm_f32(M, N, K, A, B, e, m->stream));

@@ -267,6 +267,11 @@ cudaError_t gemm_f32(int M, int N, int K, GemmOperand A, GemmOperand B, const Ge
 cudaError_t gemm_bf16_tc(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
                          int splits, DevState* st, cudaStream_t s);
 bool gemm_bf16_tc_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi);
+// D = A B^T for at most 16 rows of A (bf16, both operands K-major), weight
+// streaming without tensor cores; epilogues STORE_ACT, GELU, STORE_F32.
+bool gemm_rows_supported(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi);
+cudaError_t gemm_rows_bf16(int M, int N, int K, GemmOperand A, GemmOperand B, const GemmEpi& epi,
+                           cudaStream_t s);
 
 int num_sms();   // SM count of the current device
 // Bit of the current device in a per-device set-up mask: kernel attributes

@@ -332,6 +332,24 @@ def test_grad_accumulation_matches_one_big_batch():
         assert rel_l2(ga[n], gb[n]) < 1e-5, n
 
 
+def test_async_loss_read_matches_the_synchronous_one():
+    """gpt2_get_loss_async enqueues the copy on the model's stream: after a
+    sync the pinned host value equals gpt2_get_loss's, step after step."""
+    c = CONFIGS["tiny"]
+    m = gpt2.GPT2(gpu_cfg(c, gpt2.GPT2_FP32), seed=3)
+    h = torch.zeros(3, dtype=torch.float32).pin_memory()
+    for i in range(3):
+        x, y = synthdata.uniform_batch(c.vocab_size, c.batch_size, c.seq_len, 20 + i)
+        m.forward(dev(x), dev(y), sync_loss=False)
+        m.loss_async(h[i:i + 1])
+        m.backward()
+        m.step(lr=1e-3, sync_norm=False)
+        m.zero_grad()
+        m.sync()
+        assert h[i].item() == m.loss()
+    m.close()
+
+
 def test_runs_are_bit_reproducible():
     c = oracle_cfg(CONFIGS["char"], batch_size=4, n_layer=2)
     x, y = synthdata.markov_batch(65, c.batch_size, c.seq_len, 1)
