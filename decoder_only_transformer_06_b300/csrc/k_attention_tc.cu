@@ -22,7 +22,7 @@
 //               O_hf when its max grew by more than 2^8 (otherwise P may exceed
 //               1 by up to 2^8, which the final division absorbs exactly).
 //   warp 8      TMA producer: Q once per item, then K and V of each block of
-//               128 keys into one slot of a three-slot ring.
+//               128 keys into one slot of a five-slot ring.
 //   warp 9      allocates 512 TMEM columns (S triple buffer, the two halves'
 //               O); lane 0 issues S_j = Q K_j^T (M=128, N=128, K=64) into
 //               S[j%3] once the P V products that read the P written over it
@@ -32,9 +32,13 @@
 //               issuing thread sustains about one tcgen05.mma per hundred
 //               cycles, so each half has its own. The tensor core computes
 //               S_{j+1}, S_{j+2} and P_j V_j while the softmax works on S_{j+1}.
-// The item's output leaves through a 4 KB shared-memory slab per row quarter
-// and one TMA store. Every mbarrier wait is bounded; on expiry the CTA records
-// ERR_TIMEOUT, drains its copies and MMAs (bounded), frees TMEM and returns.
+// An item's output is written after the next item's first key block (by then
+// its last P V products have landed): each softmax warp combines the halves
+// for its 32 rows and 32 of the 64 columns and sends them through a 2 KB
+// shared-memory slab and one TMA store. Warps 8..11 give up registers to the
+// softmax warpgroups (setmaxnreg). Every mbarrier wait is bounded; on expiry
+// the CTA records ERR_TIMEOUT, drains its copies and MMAs (bounded), frees TMEM
+// and returns.
 #include "attn_tc.cuh"
 
 namespace k {
