@@ -30,9 +30,11 @@
 // elementwise warps (four per SM sub-partition) hide the latency of the
 // exponentials and TMEM copies. The 64-row sub-blocks make every per-step
 // buffer double-buffered inside the 512 TMEM columns, so the products of step
-// j+1 run while the elementwise warps work on step j. Every mbarrier wait is
-// bounded; on expiry the CTA records ERR_TIMEOUT, drains its copies and
-// products (bounded), frees TMEM and returns.
+// j+1 run while the elementwise warps work on step j. In the dQ kernel the
+// producer/issuer warpgroup (warps 16..19) gives up registers to the four
+// elementwise warpgroups (setmaxnreg), which then run without spills. Every
+// mbarrier wait is bounded; on expiry the CTA records ERR_TIMEOUT, drains its
+// copies and products (bounded), frees TMEM and returns.
 #include "attn_tc.cuh"
 
 namespace k {
