@@ -106,6 +106,7 @@ struct gpt2_model {
     float* Dbuf = nullptr;
     float* ln_partial = nullptr;
     float* cs_partial = nullptr;
+    float* fc_cs_part = nullptr;   // bf16: [ceil(M/32), 4C] column sums of dh from the c_proj dX GEMM
     float* splitk_ws = nullptr;
     size_t splitk_ws_floats = 0;
     void* emb_ws = nullptr;
@@ -403,6 +404,7 @@ static int create_impl(gpt2_model* m, const gpt2_config* cfg, uint64_t seed) {
     ALLOC(m, m->ln_partial, 2 * k::layernorm_bwd_partial_floats(m->M, m->C) * 4);
     size_t cs = k::colsum_partial_floats(m->M, 4 * m->C);
     ALLOC(m, m->cs_partial, cs * 4);
+    if (m->use_bf16) ALLOC(m, m->fc_cs_part, (size_t)((m->M + 31) / 32) * 4 * m->C * 4);
     ALLOC(m, m->emb_ws, k::embed_bwd_workspace(m->M, m->C));
     m->norm_parts = 2 * k::num_sms();
     ALLOC(m, m->norm_partial, (size_t)m->norm_parts * sizeof(double));
@@ -824,7 +826,10 @@ static int backward_impl(gpt2_model* m) {
         LayerActs& a = m->la[l];
         // MLP projection: x_out = x_mid + hgel W_mp^T + b_mp
         {
-            GemmEpi e{EPI_GELU_BWD, nullptr, m->dh, 4 * C, nullptr, 0, a.hpre, 4 * C};
+            // bf16: the GEMM also leaves the column sums of dh (fc's bias
+            // gradient) per 32-row group in fc_cs_part
+            GemmEpi e{EPI_GELU_BWD, nullptr, m->dh, 4 * C, m->use_bf16 ? m->fc_cs_part : nullptr, 4 * C,
+                      a.hpre, 4 * C};
             OPR(to_side());
             OPR(op.gemm_dw("gemm_mlpproj_dw", C, 4 * C, m->dres_act, C, a.hgel, 4 * C,
                            m->G(m->lt(l, T_MPW)), s2));
@@ -838,9 +843,15 @@ static int backward_impl(gpt2_model* m) {
             GemmEpi e{EPI_STORE_ACT, nullptr, m->du, C, nullptr, 0, nullptr, 0};
             OPR(to_side());
             OPR(op.gemm_dw("gemm_fc_dw", 4 * C, C, m->dh, 4 * C, a.u2, C, m->G(m->lt(l, T_FCW)), s2));
-            RUN(m, "bias_colsum", 2, 0, 4.0 * MC * A,
-                k::colsum_add<Act>((const Act*)m->dh, 4 * C, M, 4 * C, m->G(m->lt(l, T_FCB)),
-                                   m->cs_partial, s2));
+            if (m->use_bf16) {
+                const int groups = (M + 31) / 32;
+                RUN(m, "bias_colsum", 1, 0, 4.0 * groups * 4 * C,
+                    k::colsum_partials_add(m->fc_cs_part, groups, 4 * C, m->G(m->lt(l, T_FCB)), s2));
+            } else {
+                RUN(m, "bias_colsum", 2, 0, 4.0 * MC * A,
+                    k::colsum_add<Act>((const Act*)m->dh, 4 * C, M, 4 * C, m->G(m->lt(l, T_FCB)),
+                                       m->cs_partial, s2));
+            }
             OPR(side_done(&dh_free));
             OPR(op.gemm("gemm_fc_dx", M, C, 4 * C, {m->dh, 4 * C, true}, {m->W(m->lt(l, T_FCW)), C, false}, e));
         }

@@ -219,6 +219,8 @@ template <typename T>
 cudaError_t colsum_add(const T* dy, int64_t ld, int M, int N, float* db, float* partial,
                        cudaStream_t s);
 size_t colsum_partial_floats(int M, int N);
+// db[n] += sum over g < groups of partial[g * N + n], in group order.
+cudaError_t colsum_partials_add(const float* partial, int groups, int N, float* db, cudaStream_t s);
 
 template <typename Act>
 cudaError_t cross_entropy(Act* logits, const int32_t* tgt, float* row_loss, int M, int V, int Vp,

@@ -164,7 +164,7 @@ template <int BN, bool A_MN, bool B_MN, int KIND, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ EpiMaps maps, int M, int N, int K, int splits,
-               const float* __restrict__ bias, DevState* st) {
+               const float* __restrict__ bias, float* __restrict__ colsum, DevState* st) {
     using Cfg = TcCfg<BN, PAIR, KIND>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -490,6 +490,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 } else {
                     stage_bf16(sbuf, lane, v);
                 }
+                if (KIND == EPI_GELU_BWD && colsum != nullptr) {
+                    // lane j sums column n0 + j of this warp's 32 rows of the
+                    // staged bf16 result, rows in order; one partial per
+                    // (32-row group, column), reduced in group order later
+                    __syncwarp();
+                    float csum = 0.f;
+                    const int cq = lane >> 3, ce = lane & 7;
+#pragma unroll
+                    for (int rr = 0; rr < 32; rr++)
+                        csum += __bfloat162float(*(const bf16*)(sbuf + sw64(rr, cq) + 2 * ce));
+                    if (n0 + lane < N && m_base < M) colsum[(int64_t)(m_base / 32) * N + n0 + lane] = csum;
+                }
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0 && n0 < N && m_base < M) {
@@ -658,6 +670,9 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     if (KIND == EPI_GELU_BWD)
         ok = ok && make_map(&maps.aux, epi.aux, BF, 2, N, M, epi.ld_aux, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return cudaErrorInvalidValue;
+    // GELU_BWD with out2 set: per-32-row column sums of the result (the
+    // bias gradient of the Linear whose input gradient it is)
+    float* colsum = KIND == EPI_GELU_BWD ? (float*)epi.out2 : nullptr;
     auto kern = gemm_tc_kernel<BN, A_MN, B_MN, KIND, PAIR>;
     static bool attr_set = false;
     static int pairs = 0;
@@ -674,7 +689,7 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     const int total = tiles * splits;
     if (!PAIR) {
         const int grid = total < num_sms() ? total : num_sms();
-        (void)pdl_launch(kern, grid, TC_THREADS, Cfg::SMEM, s, ta, tb, maps, M, N, K, splits, epi.bias, st);
+        (void)pdl_launch(kern, grid, TC_THREADS, Cfg::SMEM, s, ta, tb, maps, M, N, K, splits, epi.bias, colsum, st);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -691,7 +706,7 @@ static cudaError_t launch_tc(int M, int N, int K, GemmOperand A, GemmOperand B, 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_on() ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, M, N, K, splits, epi.bias, st);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, maps, M, N, K, splits, epi.bias, colsum, st);
 }
 
 // BN = 256 tiles run as CTA pairs (cta_group::2); BN = 128 as single CTAs.

@@ -494,6 +494,12 @@ colsum_stage2(const float* __restrict__ partial, int splits, int N, float* __res
     }
 }
 
+cudaError_t colsum_partials_add(const float* partial, int groups, int N, float* db, cudaStream_t s) {
+    if (groups < 1 || N < 1) return cudaErrorInvalidValue;
+    (void)pdl_launch(colsum_stage2, (N + 31) / 32, 256, 0, s, partial, groups, N, db);
+    return cudaGetLastError();
+}
+
 size_t colsum_partial_floats(int M, int N) {
     return (size_t)((M + CS_ROWS_PER_SPLIT - 1) / CS_ROWS_PER_SPLIT) * N;
 }
