@@ -212,6 +212,13 @@ def test_decode_step_needs_the_cached_positions():
     with pytest.raises(gpt2.GPT2Error) as e:
         m.decode_step(tok, c.seq_len + 1, out)
     assert e.value.code == gpt2.GPT2_EINVAL
+    # an id outside the vocabulary is clamped and reported by the next synchronising call
+    m.forward_last(d_x, 5, out)
+    bad = torch.full((c.batch_size,), c.vocab_size + 3, dtype=torch.int32, device="cuda")
+    m.decode_step(bad, 6, out)
+    with pytest.raises(gpt2.GPT2Error) as e:
+        m.sync()
+    assert e.value.code == gpt2.GPT2_ERANGE
     m.close()
 
 
