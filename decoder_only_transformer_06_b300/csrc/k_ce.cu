@@ -171,11 +171,12 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
     const uint32_t rowbytes = (uint32_t)Vp * 2;
     const uint32_t padbytes = (rowbytes + 127) & ~127u;
     bf16* cur = (bf16*)ce_smem;
-    uint64_t* bar = (uint64_t*)(ce_smem + padbytes);
-    float* red = (float*)(bar + 1);
+    uint64_t* bar = (uint64_t*)(ce_smem + padbytes);   // [2]: the row's two halves
+    float* red = (float*)(bar + 2);
     const int tid = threadIdx.x;
     if (tid == 0) {
-        ptx::mbar_init(bar, 1);
+        ptx::mbar_init(&bar[0], 1);
+        ptx::mbar_init(&bar[1], 1);
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -183,16 +184,42 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
     pdl_trigger();
     const int nvec = Vp / 8;          // 16-byte chunks per row
     const int nfull = V / 8;          // chunks entirely below V
+    // The row moves in two halves (chunks [0, nh) and [nh, nvec)), each with its
+    // own barrier and bulk copies: the maximum pass starts on the first half
+    // while the second is arriving, and the first half's gradients leave while
+    // the second half's are computed.
+    const int nh = nvec / 2;
+    const uint32_t h0 = (uint32_t)nh * 16u, h1 = rowbytes - h0;
     const float L2E = 1.4426950408889634f;
     const float scale_valid = st->inv_count;
     uint32_t par = 0;
     for (int row = blockIdx.x; row < M; row += gridDim.x, par ^= 1) {
         if (tid == 0) {
-            ptx::bulk_wait_read_all();            // the previous row's store has read the buffer
-            ptx::mbar_arrive_expect_tx(bar, rowbytes);
-            ptx::bulk_g2s(cur, logits + (int64_t)row * Vp, rowbytes, bar);
+            const bf16* src = logits + (int64_t)row * Vp;
+            ptx::bulk_wait_read_1();              // the previous row's first-half store has read it
+            ptx::mbar_arrive_expect_tx(&bar[0], h0);
+            ptx::bulk_g2s(cur, src, h0, &bar[0]);
+            ptx::bulk_wait_read_all();            // and the second half's
+            ptx::mbar_arrive_expect_tx(&bar[1], h1);
+            ptx::bulk_g2s((uint8_t*)cur + h0, (const uint8_t*)src + h0, h1, &bar[1]);
         }
-        const bool ok = ptx::mbar_wait_bounded(bar, par);
+        int y = tgt[row];
+        const bool ignore = (y == -1);
+        y = (y < 0 || y >= V) ? 0 : y;
+        const uint4* cv = (const uint4*)cur;
+        // pass 1: max, first half as soon as it has landed, then the second
+        __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+        bool ok = ptx::mbar_wait_bounded(&bar[0], par);
+        const int e0 = nh < nfull ? nh : nfull;
+        if (ok) {
+#pragma unroll 4
+            for (int vi = tid; vi < e0; vi += CEB_THREADS) {
+                uint4 w = cv[vi];
+                const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+                mx2 = __hmax2(mx2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
+            }
+            ok = ptx::mbar_wait_bounded(&bar[1], par);
+        }
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
                 atomicOr(&st->err, ERR_TIMEOUT);
@@ -200,19 +227,13 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
             }
             break;
         }
-        int y = tgt[row];
-        const bool ignore = (y == -1);
-        y = (y < 0 || y >= V) ? 0 : y;
-        const float zy = __bfloat162float(cur[y]);
-        const uint4* cv = (const uint4*)cur;
-        // pass 1: max
-        __nv_bfloat162 mx2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
 #pragma unroll 4
-        for (int vi = tid; vi < nfull; vi += CEB_THREADS) {
+        for (int vi = e0 + tid; vi < nfull; vi += CEB_THREADS) {
             uint4 w = cv[vi];
             const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
             mx2 = __hmax2(mx2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
         }
+        const float zy = __bfloat162float(cur[y]);
         float mx = fmaxf(__low2float(mx2), __high2float(mx2));
         if (tid == 0) {
             for (int j = nfull * 8; j < V; j++) mx = fmaxf(mx, __bfloat162float(cur[j]));
@@ -230,9 +251,9 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
 #pragma unroll
             for (int t = 0; t < 4; t++) {
                 float2 f = __bfloat1622float2(h[t]);
-                float e0 = ptx::ex2(fmaf(f.x, L2E, -mxl)), e1 = ptx::ex2(fmaf(f.y, L2E, -mxl));
-                sum += e0 + e1;
-                __nv_bfloat162 p = __floats2bfloat162_rn(e0, e1);
+                float e0f = ptx::ex2(fmaf(f.x, L2E, -mxl)), e1f = ptx::ex2(fmaf(f.y, L2E, -mxl));
+                sum += e0f + e1f;
+                __nv_bfloat162 p = __floats2bfloat162_rn(e0f, e1f);
                 op[t] = *(uint32_t*)&p;
             }
             ((uint4*)cur)[vi] = o;
@@ -247,43 +268,47 @@ ce_bulk_kernel(bf16* __restrict__ logits, const int32_t* __restrict__ tgt,
         sum = block_reduce_n(sum, false, red);
         const float inv = 1.0f / sum;
         const float scale = ignore ? 0.f : scale_valid;
-        // pass 3: gradient in place
+        // pass 3: gradient in place, half by half; each half leaves by one bulk store
+        for (int hh = 0; hh < 2; hh++) {
+            const int v0 = hh == 0 ? 0 : nh, v1 = hh == 0 ? nh : nvec;
 #pragma unroll 2
-        for (int vi = tid; vi < nvec; vi += CEB_THREADS) {
-            uint4 o;
-            uint32_t* op = (uint32_t*)&o;
-            if (vi < nfull) {
-                uint4 w = cv[vi];
-                const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
+            for (int vi = v0 + tid; vi < v1; vi += CEB_THREADS) {
+                uint4 o;
+                uint32_t* op = (uint32_t*)&o;
+                if (vi < nfull) {
+                    uint4 w = cv[vi];
+                    const __nv_bfloat162* h = (const __nv_bfloat162*)&w;
 #pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    float2 f = __bfloat1622float2(h[t]);
-                    const int j = vi * 8 + 2 * t;
-                    float d0 = (f.x * inv - (j == y ? 1.f : 0.f)) * scale;
-                    float d1 = (f.y * inv - (j + 1 == y ? 1.f : 0.f)) * scale;
-                    __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
-                    op[t] = *(uint32_t*)&p;
-                }
-            } else {
-                const bf16* e = cur + vi * 8;
+                    for (int t = 0; t < 4; t++) {
+                        float2 f = __bfloat1622float2(h[t]);
+                        const int j = vi * 8 + 2 * t;
+                        float d0 = (f.x * inv - (j == y ? 1.f : 0.f)) * scale;
+                        float d1 = (f.y * inv - (j + 1 == y ? 1.f : 0.f)) * scale;
+                        __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
+                        op[t] = *(uint32_t*)&p;
+                    }
+                } else {
+                    const bf16* e = cur + vi * 8;
 #pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    const int j = vi * 8 + 2 * t;
-                    float d0 = j < V ? (__bfloat162float(e[2 * t]) * inv - (j == y ? 1.f : 0.f)) * scale : 0.f;
-                    float d1 = j + 1 < V ? (__bfloat162float(e[2 * t + 1]) * inv - (j + 1 == y ? 1.f : 0.f)) * scale : 0.f;
-                    __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
-                    op[t] = *(uint32_t*)&p;
+                    for (int t = 0; t < 4; t++) {
+                        const int j = vi * 8 + 2 * t;
+                        float d0 = j < V ? (__bfloat162float(e[2 * t]) * inv - (j == y ? 1.f : 0.f)) * scale : 0.f;
+                        float d1 = j + 1 < V ? (__bfloat162float(e[2 * t + 1]) * inv - (j + 1 == y ? 1.f : 0.f)) * scale : 0.f;
+                        __nv_bfloat162 p = __floats2bfloat162_rn(d0, d1);
+                        op[t] = *(uint32_t*)&p;
+                    }
                 }
+                ((uint4*)cur)[vi] = o;
             }
-            ((uint4*)cur)[vi] = o;
+            ptx::fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                ptx::bulk_s2g((uint8_t*)(logits + (int64_t)row * Vp) + (hh == 0 ? 0u : h0),
+                              (const uint8_t*)cur + (hh == 0 ? 0u : h0), hh == 0 ? h0 : h1);
+                ptx::bulk_commit();
+            }
         }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            ptx::bulk_s2g(logits + (int64_t)row * Vp, cur, rowbytes);
-            ptx::bulk_commit();
-            row_loss[row] = ignore ? 0.f : (mx + logf(sum) - zy);
-        }
+        if (tid == 0) row_loss[row] = ignore ? 0.f : (mx + logf(sum) - zy);
     }
     if (tid == 0) ptx::bulk_wait_all();
 }
