@@ -18,6 +18,7 @@ of the same workload on the host cores, as the comparison arm.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -100,7 +101,7 @@ def flops_per_token(L, C, V_padded, T, block):
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -116,12 +117,15 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, regions=None):
+        """Median SM clock, its maximum and the throttle reasons seen over all
+        samples; with regions ({name: (t0, t1)} in time.time() seconds) also
+        the median SM clock of the samples taken inside each region."""
         if not self.proc:
             return None
         self.proc.terminate()
@@ -130,22 +134,49 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.path)
+        return self.summarize(lines, regions)
+
+    @staticmethod
+    def summarize(lines, regions=None):
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+
+        def mhz(r, i):
+            return float(r[i]) if r[i].replace(".", "").isdigit() else None
+
+        sm = [v for v in (mhz(r, 2) for r in rows) if v is not None]
+        mx = [v for v in (mhz(r, 3) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(rows)}
+        if regions:
+            # nvidia-smi stamps each sample in the host's local time
+            stamped = []
+            for r in rows:
+                try:
+                    t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                v = mhz(r, 2)
+                if v is not None:
+                    stamped.append((t, v))
+            by_region = {}
+            for name, (t0, t1) in regions.items():
+                inside = [v for t, v in stamped if t0 <= t <= t1]
+                by_region[name] = {"sm_mhz": statistics.median(inside) if inside else None,
+                                   "samples": len(inside)}
+            out["by_region"] = by_region
+        return out
 
 
 # ----------------------------------------------------------------- distributed
@@ -313,6 +344,7 @@ def run_ours(args):
     model.profile(False)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_dev0 = time.time()
     e0.record(stream)
     for k in range(args.steps):
         train_step(args.warmup + k, args.warmup + k)
@@ -321,6 +353,7 @@ def run_ours(args):
     model.join()
     e1.record(stream)
     torch.cuda.synchronize()
+    t_dev1 = time.time()
     launches_timed = sum(r["kernels"] for r in model.profile_report())
     if world > 1:
         torch.distributed.barrier()
@@ -354,19 +387,24 @@ def run_ours(args):
         model.step(lr(it), sync_norm=False)
         model.zero_grad()
 
-    for i in range(2):
+    # as many warm-up steps as the device-timed region had: the power cap sets
+    # the clock from recent power draw, and the host set-up above idled the GPU
+    for i in range(args.warmup):
         e2e_step(i, i)
     model.sync()
     if world > 1:
         torch.distributed.barrier()
+    t_e2e0 = time.time()
     t0 = time.perf_counter()
     for k in range(e2e_steps):
         e2e_step(k, k)
     model.sync()                     # the last step's update and loss copy have landed
+    t_e2e1 = time.time()
     e2e_s = barrier_max(time.perf_counter() - t0, world, torch)
     # the clock sampler (nvidia-smi polling) ran through both timed regions,
-    # so that whatever it perturbs, it perturbs both alike
-    clk = clocks.stop()
+    # so that whatever it perturbs, it perturbs both alike; the power cap moves
+    # the clock between them, so each region's own median is reported too
+    clk = clocks.stop({"device_timed": (t_dev0, t_dev1), "e2e": (t_e2e0, t_e2e1)})
     if not all(math.isfinite(v) for v in h_loss[:e2e_steps].tolist()):
         raise RuntimeError("non-finite loss in the end-to-end loop")
     e2e_value = tokens_step * e2e_steps / e2e_s
@@ -549,7 +587,7 @@ def run_generate_workload(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2_124m")
