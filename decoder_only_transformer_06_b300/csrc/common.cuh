@@ -142,7 +142,7 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // Bounded device-side waits measure elapsed time on the SM's own cycle
 // counter (monotonic for the warp that reads it) and give up after
 // WAIT_LIMIT_CYCLES, about two seconds at B300 clocks; they then report
-// ERR_TIMEOUT. The global nanosecond timer is not used: the driver may adjust
+// ERR_TIMEOUT. The global nanosecond timer is not used: the CUDA driver may adjust
 // it while a kernel runs, which would end a wait early.
 __device__ __forceinline__ long long wait_clock() { return clock64(); }
 #define WAIT_LIMIT_CYCLES 4000000000ll
