@@ -166,12 +166,10 @@ cudaError_t validate_inputs(const int32_t* tok, const int32_t* tgt, int M, int V
                             int accum, cudaStream_t s);
 cudaError_t embed_fwd(const int32_t* tok, const float* wte, const float* wpe, float* x, int M,
                       int T, int C, int V, cudaStream_t s);
-// dwte[tok[m]] += dx[m]; dwpe[t] += sum_b dx[b*T+t]; deterministic.
+// Embedding backward, dwte[tok[m]] += dx[m] and dwpe[t] += sum_b dx[b*T+t],
+// deterministic, in two parts: the sort of the token ids (depends on the
+// tokens only) and the segmented sums of dx rows that use it.
 size_t embed_bwd_workspace(int M, int C);
-cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
-                      int C, int V, void* workspace, cudaStream_t s);
-// embed_bwd in its two parts: the sort of the token ids (depends on the tokens
-// only) and the segmented sums of dx rows that use it.
 cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cudaStream_t s);
 cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, int T, int C,
                             void* workspace, cudaStream_t s);

@@ -391,12 +391,6 @@ cudaError_t embed_bwd_sort(const int32_t* tok, int M, int V, void* workspace, cu
     return cudaGetLastError();
 }
 
-cudaError_t embed_bwd(const int32_t* tok, const float* dx, float* dwte, float* dwpe, int M, int T,
-                      int C, int V, void* workspace, cudaStream_t s) {
-    CUDA_OK(embed_bwd_sort(tok, M, V, workspace, s));
-    return embed_bwd_apply(dx, dwte, dwpe, M, T, C, workspace, s);
-}
-
 cudaError_t embed_bwd_apply(const float* dx, float* dwte, float* dwpe, int M, int T, int C,
                             void* workspace, cudaStream_t s) {
     int* s_tok = (int*)workspace;
