@@ -16,8 +16,9 @@
  *     device (bad token ids, an expired bounded wait) are recorded in a device
  *     status word and reported by the next call that synchronises.
  *   - The library owns every parameter, gradient, optimizer-state and
- *     activation buffer (device memory it allocates in gpt2_create and frees
- *     in gpt2_destroy). The caller owns the token/target buffers and the
+ *     activation buffer (device memory it allocates in gpt2_create, or for
+ *     the decoding step on its first call, and frees in gpt2_destroy). The
+ *     caller owns the token/target buffers and the
  *     stream; they must stay valid until the stream has passed the call.
  *   - Tokens are int32 (ids < 2^16 on the pages; nanoGPT guide Deep dive 3).
  *   - Not thread-safe: one host thread per model at a time.
@@ -165,11 +166,11 @@ int gpt2_forward_last(gpt2_model* model, const int32_t* d_tokens, int t, float* 
  *             of position t-1 of every sequence (real vocabulary only).
  * Once a context holds T tokens, the pages' crop shifts every position, so
  * the next token needs gpt2_forward_last on the cropped context. The first
- * call allocates the step's row buffers (B rows, about 44 C bytes per row);
- * no backward afterwards (ESTATE). Does not synchronise.
- * Errors: EINVAL (NULL pointers, t outside [1, T], a head size that does not
- * divide 128); ESTATE (positions 0..t-2 not cached); ENOMEM; ERANGE as
- * gpt2_forward.
+ * call allocates the step's row buffers (B rows of 30 C bytes in bf16, 52 C
+ * in fp32) and the decoding attention's span partials (B H ceil(T/64)
+ * (hs + 2) floats); no backward afterwards (ESTATE). Does not synchronise.
+ * Errors: EINVAL (NULL pointers, t outside [1, T], a head size above 128);
+ * ESTATE (positions 0..t-2 not cached); ENOMEM; ERANGE as gpt2_forward.
  */
 int gpt2_decode_step(gpt2_model* model, const int32_t* d_tokens, int t, float* d_logits);
 
